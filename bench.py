@@ -1,0 +1,385 @@
+#!/usr/bin/env python3
+"""Benchmark: SGEMM TFLOP/s at M=N=K=4096 (FP32, row-major, alpha=1.5, beta=0.5,
+A, B, C uniform[-1,1) from seed 1) on GB300, as a fraction of the FP32 FFMA peak.
+
+One step = one C = alpha*A*B + beta*C call of the library on operands already
+resident in HBM. Prints ONE JSON line (rank 0). ``--impl reference`` times the
+FP64 CPU oracle instead (a bounded sample of the same workload per step).
+
+Multi-GPU: the path does not shard across GPUs here; ``--gpus N`` under
+torchrun runs N independent replicas (weak scaling), max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM TFLOP/s at M=N=K=4096 FP32 and % of GB300 FP32 FFMA peak"
+WORKLOAD = "square4096"
+L2_BYTES = 126 * 2**20  # GB300 L2 (nvidia-smi reports ~126 MiB)
+KERNEL_SOURCES = ["dense_fp32_gemm_04_gb300/csrc/ffma_kernels.cu", "dense_fp32_gemm_04_gb300/csrc/device_ptx.cuh",
+                  "dense_fp32_gemm_04_gb300/csrc/tile_table.h"]
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "ffma_sgemm_4096_traffic.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed
+class World:
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.size = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+
+    def init(self, backend):
+        if self.size > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend=backend)
+            self.pg = True
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        import torch.distributed as dist
+
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+def aggregate(per_rank_seconds, flops_per_rank):
+    """Whole-job throughput: all ranks' flops over the slowest rank's time (TFLOP/s)."""
+    t = max(per_rank_seconds)
+    return sum(flops_per_rank) / t / 1e12, t
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if t0 is not None and (ts < t0 or ts > t1 + 0.2):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"^kernel_source_sha256_16:\s*([0-9a-f]+)", text, re.M)
+    m_val = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_val.group(1))
+
+
+def problem(name):
+    from dense_fp32_gemm_04_gb300 import inputs
+
+    p = dict(inputs.PROBLEMS[name])
+    return p
+
+
+def cpu_oracle_sample(name, seconds, A=None, B=None, C=None):
+    """Time the FP64 oracle on rows of the workload for about ``seconds`` (all host threads)."""
+    import numpy as np
+
+    import oracle
+    from dense_fp32_gemm_04_gb300 import inputs
+
+    p = problem(name)
+    if A is None:
+        A, B, C = inputs.problem_operands(name)
+    M, N, K = p["M"], p["N"], p["K"]
+    threads = oracle.max_threads()
+    rows_done, elapsed, r = 0, 0.0, 4
+    while elapsed < seconds and rows_done < M:
+        rows = np.arange(rows_done, min(M, rows_done + r))
+        t = time.perf_counter()
+        oracle.sgemm_f64(A, B, C, p["alpha"], p["beta"], rows=rows, with_mag=False)
+        dt = time.perf_counter() - t
+        elapsed += dt
+        rows_done += len(rows)
+        # grow the batch toward the remaining budget
+        per_row = dt / len(rows)
+        r = max(1, min(M - rows_done, int((seconds - elapsed) / max(per_row, 1e-9)) + 1, 4 * r))
+    flops = 2.0 * rows_done * N * K
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows_done} of {M} rows of C for M=N=K={K} ({rows_done}x{N}x{K} MACs, FP64 accumulate, "
+                      f"i-k-j loop, {threads} threads), {elapsed:.1f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, world):
+    if world.rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from dense_fp32_gemm_04_gb300 import inputs
+
+    p = problem(args.workload)
+    A, B, C = inputs.problem_operands(args.workload)
+    M, N, K = p["M"], p["N"], p["K"]
+    rows_per_step = 8
+    threads = oracle.max_threads()
+
+    def step(i):
+        lo = (i * rows_per_step) % M
+        rows = np.arange(lo, min(M, lo + rows_per_step))
+        oracle.sgemm_f64(A, B, C, p["alpha"], p["beta"], rows=rows, with_mag=False)
+        return len(rows)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    rows = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"sgemm M=N=K={K} alpha={p['alpha']} beta={p['beta']} uniform[-1,1) seed {p['seed']}",
+                   "step": f"{rows_per_step} rows of C per step (bounded sample of the workload)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} of {M} rows of C per step, FP64 i-k-j oracle, {threads} threads"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, world):
+    import numpy as np
+    import torch
+
+    import dense_fp32_gemm_04_gb300 as sg
+    from dense_fp32_gemm_04_gb300 import _build, inputs
+
+    _build.build()
+    torch.cuda.set_device(world.local_rank)
+    dev = torch.device("cuda", world.local_rank)
+    world.init("nccl" if world.size > 1 else "gloo")
+
+    p = problem(args.workload)
+    M, N, K, alpha, beta = p["M"], p["N"], p["K"], p["alpha"], p["beta"]
+    A, B, C = inputs.problem_operands(args.workload)
+    dA, dB, dC = (torch.from_numpy(x).to(dev) for x in (A, B, C))
+    h = sg.Sgemm(world.local_rank)
+    stream = torch.cuda.current_stream(dev)
+    flops = 2.0 * M * N * K
+    operand_bytes = 4 * (M * K + K * N + M * N)
+
+    for _ in range(max(3, args.warmup)):
+        h.run(dA, dB, dC, alpha, beta, stream=stream)
+    torch.cuda.synchronize()
+    st, code = h.check_device_status()
+    if st != sg.SGEMM_OK:
+        raise RuntimeError(f"device status {code:#x} after warm-up")
+    plan = h.last_plan()
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "")) or None
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(world.local_rank)))
+    sampler.start()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    world.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        h.run(dA, dB, dC, alpha, beta, stream=stream)
+        ends[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    world.barrier()
+    t_wall1 = time.time()
+    sampler.stop()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    st, code = h.check_device_status()
+    if st != sg.SGEMM_OK:
+        raise RuntimeError(f"device status {code:#x} in the timed region")
+
+    t_max = world.max(elapsed)
+    value = flops * args.steps * world.size / t_max / 1e12
+
+    # End to end through the host-buffer entry point: pinned host operands,
+    # H2D of A, B, C and D2H of C inside every step.
+    pA, pB = (torch.from_numpy(x).pin_memory() for x in (A, B))
+    pC = torch.from_numpy(C).pin_memory()
+    h.run_host(pA, pB, pC, alpha, beta, stream=stream)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, args.e2e_steps)
+    world.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        h.run_host(pA, pB, pC, alpha, beta, stream=stream)
+    torch.cuda.synchronize()
+    e2e_t = world.max(time.perf_counter() - t0)
+    e2e_value = flops * e2e_steps * world.size / e2e_t / 1e12
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+    nsm = props.multi_processor_count
+    avg_kernel_s = statistics.fmean(kernel_ms) / 1e3
+    achieved = flops / avg_kernel_s / 1e12
+    sm_mhz = clocks["sm_mhz"] if clocks else None
+    peak = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if peak else None, "traffic": recorded_traffic(),
+                "kernel": "ffma_sgemm_kernel (plan config %d, %dx%d tile)" % (plan.config, plan.bm, plan.bn),
+                "peak_basis": f"{nsm} SMs x 128 FP32 FMA/clk x 2 FLOP x median SM clock under load "
+                              f"({sm_mhz} MHz, nvidia-smi during the timed region)",
+                "frac_at_max_clock": (achieved / (nsm * 256 * clocks["sm_max_mhz"] * 1e-6)) if clocks else None}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world.size, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"sgemm M=N=K={K} alpha={alpha} beta={beta} A,B,C uniform[-1,1) seed {p['seed']}",
+                   "M": M, "N": N, "K": K, "layout": "row-major",
+                   "l2": f"no flush: operands {operand_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB",
+                   "parallelism": f"replicas x{world.size}", "plan": plan.as_dict()},
+        "pct_fp32_ffma_peak": (100.0 * achieved / peak) if peak else None,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 4 * (M * K + K * N + M * N),
+                "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps, "api": "sgemm_run_host (pinned host buffers)"},
+        "gpu_launches": plan.launches * args.steps,
+        "clocks": clocks,
+    }
+    if world.rank == 0 and world.size == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds, A, B, C)
+    if world.rank == 0:
+        print(json.dumps(line), flush=True)
+    h.close()
+    world.close()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = World()
+    if args.impl == "reference":
+        return run_reference(args, world)
+    return run_ours(args, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

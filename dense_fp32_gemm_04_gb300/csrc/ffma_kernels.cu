@@ -1,0 +1,480 @@
+// FP32 FFMA SGEMM mainloop for sm_103a, plus the split-K reduction, the
+// beta-only scaling kernel and the operand repack used for unaligned inputs.
+//
+// C = alpha * A * B + beta * C, row-major ("SGEMM CUDA kernel (First Half)",
+// opening definition). The structure follows the tiling ladder of the pages —
+// a CTA owns a BM x BN tile of C and walks K in BK-deep phases ("Shared memory
+// and register blocking"; "SGEMM CUDA kernel (First Half)", Part 3), each
+// thread accumulates an 8 x 8 register microtile as a sum of outer products
+// (same page, Part 4 "Thread Tile"; "Optimizing Matrix Multiplication in
+// CUDA", 2D thread tiling), warps own 32 x 64 sub-tiles (same page, warp
+// tiling) — rebuilt for Blackwell:
+//
+//  * Staging: one producer thread issues TMA tile copies (A box 32 x BM with
+//    the 128-byte swizzle, B box BN x 32) into a STAGES-deep ring guarded by
+//    full/empty mbarriers, in place of the pages' load / __syncthreads /
+//    compute / __syncthreads phase loop. Out-of-range rows and columns are
+//    zero-filled by the copy engine, which is the pages' zero-fill
+//    predication ("SGEMM CUDA kernel (First Half)", Part 5 load_ast) done in
+//    hardware.
+//  * Bank conflicts: the pages transpose A in shared memory so a thread's TM
+//    values of A are contiguous (same page, Part 5). Here A stays K-major as
+//    the copy engine writes it, and a thread instead takes its 8 rows 4 apart
+//    (rows r, r+4, ..., r+28 of its warp tile) and reads 4 consecutive k of
+//    one row per 128-bit load. The four row groups of a warp then read four
+//    consecutive rows, which the 128-byte swizzle places in four distinct
+//    bank quads: every 128-bit shared load is conflict-free without a
+//    transposing copy.
+//  * Arithmetic: packed FFMA2 (two FP32 fused multiply-adds per instruction,
+//    round-to-nearest-even, sm_100+) halves the issue slots the 64 FMAs of a
+//    k-step need, leaving room for the loads. Each output is still one chain
+//    of IEEE FP32 FMAs in ascending k.
+//  * Persistent grid: CTAs loop over (tile, split) work units in a grouped
+//    order; the producer keeps prefetching across unit boundaries.
+//  * Watchdog: every mbarrier wait is bounded; on expiry the CTA records
+//    SGEMM_ERR_TIMEOUT in the status word, waits (bounded) for its own copies
+//    in flight and returns — it never traps or spins forever.
+#include <cuda_runtime.h>
+
+#include "device_ptx.cuh"
+#include "sgemm_internal.h"
+
+namespace sgemm_impl {
+namespace {
+
+using namespace sgemm_dev;
+using sgemm_cfg::kFfmaBK;
+
+constexpr int kTimeoutCode = 5 << 16;  // SGEMM_ERR_TIMEOUT << 16
+constexpr int kGroupM = 8;             // tile rows per raster group (L2 reuse of B)
+
+template <int BM_, int BN_, int STAGES_, int MINB_>
+struct Tile {
+    static constexpr int BM = BM_, BN = BN_, STAGES = STAGES_, MINB = MINB_, BK = kFfmaBK;
+    static constexpr int WM = 32, WN = 64;
+    static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
+    static constexpr int CONSUMERS = WARPS_M * WARPS_N;
+    static constexpr int THREADS = (CONSUMERS + 1) * 32;
+    static constexpr int A_BYTES = BM * BK * 4;
+    static constexpr int B_BYTES = BK * BN * 4;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SMEM_BYTES = sgemm_cfg::ffma_smem_bytes(BM, BN, STAGES);
+    static_assert(BM % WM == 0 && BN % WN == 0, "CTA tile must be a multiple of the warp tile");
+    static_assert(BM <= 256 && BN <= 256, "a TMA box side is at most 256 elements");
+    static_assert(A_BYTES % 1024 == 0, "A stages must keep the 1024-byte swizzle alignment");
+};
+
+// Work unit u -> (tile row tm, tile column tn, K split ks). Splits of a tile
+// are adjacent; tiles run in groups of kGroupM tile rows, column by column,
+// so concurrently running CTAs share B columns and A rows in L2.
+__device__ __forceinline__ void decode_unit(const FfmaParams &p, int u, int &tm, int &tn, int &ks)
+{
+    ks = u % p.splits;
+    const int t = u / p.splits;
+    const int per_group = kGroupM * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * kGroupM;
+    const int gsize = min(p.tiles_m - first_m, kGroupM);
+    const int r = t - g * per_group;
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+__device__ __forceinline__ int split_begin(const FfmaParams &p, int ks)
+{
+    return static_cast<int>((static_cast<long long>(ks) * p.kblocks) / p.splits);
+}
+
+template <class T>
+__device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                              const FfmaParams &p, uint32_t a_base, uint32_t b_base,
+                                              uint32_t bar_base, volatile int *abort_flag)
+{
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;  // per stage: has a copy outstanding, and its phase parity
+    int seq = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        int tm, tn, ks;
+        decode_unit(p, u, tm, tn, ks);
+        const int kb1 = split_begin(p, ks + 1);
+        for (int kb = split_begin(p, ks); kb < kb1; ++kb) {
+            const uint32_t full = bar_base + 8 * stage;
+            const uint32_t empty = bar_base + 8 * (T::STAGES + stage);
+            if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
+                if (!*abort_flag) {
+                    *abort_flag = 1;
+                    report_status(p.status, kTimeoutCode | kWhereProducerEmpty);
+                }
+                ok = false;
+                break;
+            }
+            const bool skip = (p.inject_skip >= 0 && blockIdx.x == 0 && seq == p.inject_skip);
+            if (!skip) {
+                mbar_arrive_expect_tx(full, T::STAGE_BYTES);
+                tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, kb * T::BK, tm * T::BM);
+                tma_load_2d(b_base + stage * T::B_BYTES, tmB, full, tn * T::BN, kb * T::BK);
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            }
+            ++seq;
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // No copy of ours may still be writing this CTA's shared memory when it exits.
+    for (int s = 0; s < T::STAGES; ++s) {
+        if (issued >> s & 1u) {
+            if (!mbar_wait_bounded(bar_base + 8 * s, issued_parity >> s & 1u, nullptr, p.timeout_ns))
+                report_status(p.status, kTimeoutCode | kWhereDrain);
+        }
+    }
+}
+
+// One BK = 32 slab: 8 chunks of 4 k. Per chunk a thread loads its 8 rows of A
+// (one 128-bit load each: 4 consecutive k) and 4 x 2 128-bit loads of B, then
+// issues 4 * 8 * 4 = 128 FFMA2 (256 FMAs).
+template <class T>
+__device__ __forceinline__ void compute_slab(const float *__restrict__ a_rows,
+                                             const float *__restrict__ b_cols, int r,
+                                             float2 (&acc)[8][4])
+{
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+        // 128-byte swizzle: 16-byte chunk q of row `row` sits at chunk q ^ (row & 7).
+        // This thread's rows have row & 7 == r (even i) or r + 4 (odd i).
+        const int off_even = (kc ^ r) << 2;
+        const int off_odd = ((kc ^ 4) ^ r) << 2;
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a[i] = *reinterpret_cast<const float4 *>(a_rows + i * 4 * T::BK + ((i & 1) ? off_odd : off_even));
+        float4 b[4][2];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            b[kk][0] = *reinterpret_cast<const float4 *>(b_cols + (kc * 4 + kk) * T::BN);
+            b[kk][1] = *reinterpret_cast<const float4 *>(b_cols + (kc * 4 + kk) * T::BN + 32);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float2 b0 = make_float2(b[kk][0].x, b[kk][0].y);
+            const float2 b1 = make_float2(b[kk][0].z, b[kk][0].w);
+            const float2 b2 = make_float2(b[kk][1].x, b[kk][1].y);
+            const float2 b3 = make_float2(b[kk][1].z, b[kk][1].w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                const float2 a2 = make_float2(av, av);
+                acc[i][0] = __ffma2_rn(a2, b0, acc[i][0]);
+                acc[i][1] = __ffma2_rn(a2, b1, acc[i][1]);
+                acc[i][2] = __ffma2_rn(a2, b2, acc[i][2]);
+                acc[i][3] = __ffma2_rn(a2, b3, acc[i][3]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float4 axpby4(float alpha, float4 v, float beta, float4 c)
+{
+    return make_float4(fmaf(alpha, v.x, beta * c.x), fmaf(alpha, v.y, beta * c.y),
+                       fmaf(alpha, v.z, beta * c.z), fmaf(alpha, v.w, beta * c.w));
+}
+
+// C[row, col..col+3] = alpha * v + beta * C (beta == 0: C not read), with
+// per-element predication on the ragged N edge or when C is not 16-byte
+// accessible ("Optimizing Matrix Multiplication in CUDA", 1D thread tiling
+// epilogue; bounds predicates of "SGEMM CUDA kernel (First Half)", Part 2).
+__device__ __forceinline__ void store_c4(const FfmaParams &p, int row, int col, float4 v)
+{
+    float *dst = p.C + static_cast<long long>(row) * p.ldc + col;
+    if (p.vec_c && col + 3 < p.N) {
+        float4 out;
+        if (p.beta != 0.0f)
+            out = axpby4(p.alpha, v, p.beta, *reinterpret_cast<const float4 *>(dst));
+        else
+            out = make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
+        *reinterpret_cast<float4 *>(dst) = out;
+    } else {
+        const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (col + q < p.N) {
+                dst[q] = (p.beta != 0.0f) ? fmaf(p.alpha, e[q], p.beta * dst[q]) : p.alpha * e[q];
+            }
+        }
+    }
+}
+
+template <class T>
+__device__ __forceinline__ void epilogue(const FfmaParams &p, const float2 (&acc)[8][4], int tm, int tn,
+                                         int ks, int wm, int wn, int r, int c)
+{
+    const int row0 = tm * T::BM + wm * T::WM + r;
+    const int col0 = tn * T::BN + wn * T::WN + c * 4;
+    if (p.splits > 1) {
+        // Partial sums to this split's slice; the reduction applies alpha/beta.
+        float *W = p.W + static_cast<long long>(ks) * p.wstride;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = row0 + 4 * i;
+            if (row >= p.M) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int col = col0 + 32 * h;
+                if (col < p.N) {
+                    *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) =
+                        make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                }
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = row0 + 4 * i;
+        if (row >= p.M) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = col0 + 32 * h;
+            if (col < p.N)
+                store_c4(p, row, col,
+                         make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
+        }
+    }
+}
+
+template <class T>
+__global__ void __launch_bounds__(T::THREADS, T::MINB)
+ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const FfmaParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const float *sA = reinterpret_cast<const float *>(smem);
+    const float *sB = reinterpret_cast<const float *>(smem + T::STAGES * T::A_BYTES);
+    unsigned char *bar_ptr = smem + T::STAGES * T::STAGE_BYTES;
+    const uint32_t bar_base = smem_addr(bar_ptr);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_ptr + 2 * T::STAGES * 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(bar_base + 8 * s, 1);                          // full: producer's arrive + bytes
+            mbar_init(bar_base + 8 * (T::STAGES + s), T::CONSUMERS); // empty: one arrive per consumer warp
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == T::CONSUMERS && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    __syncthreads();
+
+    if (warp == T::CONSUMERS) {
+        if (lane == 0)
+            producer_loop<T>(&tmA, &tmB, p, smem_addr(sA), smem_addr(sB), bar_base, abort_flag);
+        return;
+    }
+
+    const int wm = warp % T::WARPS_M;
+    const int wn = warp / T::WARPS_M;
+    const int r = lane >> 3;  // row group: rows wm*32 + r + 4i
+    const int c = lane & 7;   // column group: columns wn*64 + 4c + {0..3} and + 32
+    const float *a_rows_base = sA + (wm * T::WM + r) * T::BK;
+    const float *b_cols_base = sB + wn * T::WN + c * 4;
+
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        int tm, tn, ks;
+        decode_unit(p, u, tm, tn, ks);
+        float2 acc[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+
+        const int kb1 = split_begin(p, ks + 1);
+        for (int kb = split_begin(p, ks); kb < kb1; ++kb) {
+            const uint32_t full = bar_base + 8 * stage;
+            bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) {
+                    *abort_flag = 1;
+                    report_status(p.status, kTimeoutCode | kWhereConsumerFull);
+                }
+                return;
+            }
+            compute_slab<T>(a_rows_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), r, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_base + 8 * (T::STAGES + stage));
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        epilogue<T>(p, acc, tm, tn, ks, wm, wn, r, c);
+    }
+}
+
+using Cfg0 = Tile<128, 128, 5, 1>;
+using Cfg1 = Tile<128, 64, 4, 2>;
+using Cfg2 = Tile<64, 128, 4, 2>;
+using Cfg3 = Tile<64, 64, 4, 3>;
+
+template <class T>
+constexpr bool matches(int i)
+{
+    return sgemm_cfg::kFfmaConfigs[i].bm == T::BM && sgemm_cfg::kFfmaConfigs[i].bn == T::BN &&
+           sgemm_cfg::kFfmaConfigs[i].stages == T::STAGES && sgemm_cfg::kFfmaConfigs[i].ctas_per_sm == T::MINB &&
+           sgemm_cfg::kFfmaConfigs[i].threads == T::THREADS &&
+           sgemm_cfg::kFfmaConfigs[i].smem_bytes == T::SMEM_BYTES;
+}
+static_assert(sgemm_cfg::kNumFfmaConfigs == 4, "one instantiation per table row");
+static_assert(matches<Cfg0>(0) && matches<Cfg1>(1) && matches<Cfg2>(2) && matches<Cfg3>(3),
+              "kernel instantiations must match the tile-config table");
+
+template <class T>
+cudaError_t set_attr()
+{
+    return cudaFuncSetAttribute(ffma_sgemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+}
+
+template <class T>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
+                   cudaStream_t stream)
+{
+    ffma_sgemm_kernel<T><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Split-K reduction: C = alpha * sum_{s=0}^{S-1} W_s + beta * C, slices added
+// in increasing s so the result depends only on (plan, S). One thread per 4
+// consecutive columns of a row.
+__global__ void splitk_reduce_kernel(const float *__restrict__ W, long long ldw, long long wstride, int splits,
+                                     int M, int N, float alpha, float beta, float *__restrict__ C, long long ldc,
+                                     int vec_c)
+{
+    const int n4 = (N + 3) >> 2;
+    const long long total = static_cast<long long>(M) * n4;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int row = static_cast<int>(idx / n4);
+        const int col = static_cast<int>(idx - static_cast<long long>(row) * n4) * 4;
+        const float *w = W + static_cast<long long>(row) * ldw + col;
+        float4 s = __ldg(reinterpret_cast<const float4 *>(w));
+        for (int q = 1; q < splits; ++q) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(w + q * wstride));
+            s.x += t.x;
+            s.y += t.y;
+            s.z += t.z;
+            s.w += t.w;
+        }
+        float *dst = C + static_cast<long long>(row) * ldc + col;
+        if (vec_c && col + 3 < N) {
+            float4 out;
+            if (beta != 0.0f)
+                out = axpby4(alpha, s, beta, *reinterpret_cast<const float4 *>(dst));
+            else
+                out = make_float4(alpha * s.x, alpha * s.y, alpha * s.z, alpha * s.w);
+            *reinterpret_cast<float4 *>(dst) = out;
+        } else {
+            const float e[4] = {s.x, s.y, s.z, s.w};
+            for (int q = 0; q < 4 && col + q < N; ++q)
+                dst[q] = (beta != 0.0f) ? fmaf(alpha, e[q], beta * dst[q]) : alpha * e[q];
+        }
+    }
+}
+
+// C = beta * C for K == 0 or alpha == 0 (beta == 0 writes +0 without reading C).
+__global__ void scale_kernel(int M, int N, float beta, float *__restrict__ C, long long ldc)
+{
+    const long long total = static_cast<long long>(M) * N;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = idx / N;
+        const long long col = idx - row * N;
+        float *dst = C + row * ldc + col;
+        *dst = (beta != 0.0f) ? beta * *dst : 0.0f;
+    }
+}
+
+// dst (rows x cols, row stride ldd) = src (row stride lds): gives an operand a
+// 16-byte-aligned base and row stride so the TMA path can read it.
+__global__ void repack_kernel(const float *__restrict__ src, long long lds, float *__restrict__ dst, long long ldd,
+                              int rows, int cols)
+{
+    const long long total = static_cast<long long>(rows) * cols;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = idx / cols;
+        const long long col = idx - row * cols;
+        dst[row * ldd + col] = __ldg(src + row * lds + col);
+    }
+}
+
+int elementwise_grid(long long work, int threads, int num_sms)
+{
+    const long long blocks = (work + threads - 1) / threads;
+    const long long cap = static_cast<long long>(num_sms) * 8;
+    return static_cast<int>(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+}
+
+}  // namespace
+
+cudaError_t ffma_set_attributes()
+{
+    cudaError_t e;
+    if ((e = set_attr<Cfg0>()) != cudaSuccess) return e;
+    if ((e = set_attr<Cfg1>()) != cudaSuccess) return e;
+    if ((e = set_attr<Cfg2>()) != cudaSuccess) return e;
+    return set_attr<Cfg3>();
+}
+
+cudaError_t launch_ffma(int config, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
+                        cudaStream_t stream)
+{
+    switch (config) {
+    case 0: return launch<Cfg0>(tmA, tmB, p, grid, stream);
+    case 1: return launch<Cfg1>(tmA, tmB, p, grid, stream);
+    case 2: return launch<Cfg2>(tmA, tmB, p, grid, stream);
+    case 3: return launch<Cfg3>(tmA, tmB, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits, int M, int N,
+                                 float alpha, float beta, float *C, long long ldc, int vec_c, int num_sms,
+                                 cudaStream_t stream)
+{
+    const long long work = static_cast<long long>(M) * ((N + 3) / 4);
+    splitk_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(W, ldw, wstride, splits, M, N,
+                                                                                   alpha, beta, C, ldc, vec_c);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms, cudaStream_t stream)
+{
+    scale_kernel<<<elementwise_grid(static_cast<long long>(M) * N, 256, num_sms), 256, 0, stream>>>(M, N, beta, C,
+                                                                                                     ldc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const float *src, long long lds, float *dst, long long ldd, int rows, int cols,
+                          int num_sms, cudaStream_t stream)
+{
+    repack_kernel<<<elementwise_grid(static_cast<long long>(rows) * cols, 256, num_sms), 256, 0, stream>>>(
+        src, lds, dst, ldd, rows, cols);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm_impl

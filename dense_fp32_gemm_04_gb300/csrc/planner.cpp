@@ -1,0 +1,169 @@
+// Host-only planning: argument validation, quick returns, alignment gates,
+// tile-config and split-K choice, workspace sizing. No CUDA calls here, so
+// sgemm_plan() works on a machine without a GPU.
+#include "planner.h"
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+
+namespace sgemm_impl {
+
+namespace {
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Modelled time (seconds) of one FFMA configuration with S splits. Per CTA a
+// 32-deep k-block of a BM x BN tile costs BM*BN*32 FMAs at the SM's FP32 rate
+// shared by the CTAs resident on it; a persistent CTA runs ceil(units/slots)
+// units one after another; split-K adds the partial write + reduce traffic.
+double model_time(const sgemm_cfg::TileConfig &c, int M, int N, int K, int S, int num_sms, bool beta_read)
+{
+    const double fma_per_sm = 128.0 * 1.9e9 * 0.85;  // FMA/s per SM, at an achieved fraction
+    const double hbm = 5.5e12;                        // B/s achieved by the elementwise kernels
+    const long long kb = ceil_div(K, sgemm_cfg::kFfmaBK);
+    const long long tiles = ceil_div(M, c.bm) * ceil_div(N, c.bn);
+    const long long units = tiles * S;
+    const long long slots = static_cast<long long>(num_sms) * c.ctas_per_sm;
+    const long long per_cta = ceil_div(units, slots);
+    const double kb_per_unit = static_cast<double>(ceil_div(kb, S));
+    const double t_kb = static_cast<double>(c.bm) * c.bn * sgemm_cfg::kFfmaBK * c.ctas_per_sm / fma_per_sm * c.rel_cost;
+    double t = static_cast<double>(per_cta) * (kb_per_unit + 1.5) * t_kb + 2.0e-6;
+    if (S > 1) {
+        const double bytes = (2.0 * S + (beta_read ? 2.0 : 1.0)) * 4.0 * M * static_cast<double>(N);
+        t += bytes / hbm + 2.5e-6;
+    }
+    return t;
+}
+
+}  // namespace
+
+int validate(const Problem &q)
+{
+    if (q.M < 0 || q.N < 0 || q.K < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (q.lda < std::max(1, q.K) || q.ldb < std::max(1, q.N) || q.ldc < std::max(1, q.N))
+        return SGEMM_ERR_INVALID_VALUE;
+    if (q.num_sms <= 0) return SGEMM_ERR_INVALID_VALUE;
+    if (q.math_mode != SGEMM_MATH_FP32 && q.math_mode != SGEMM_MATH_TF32) return SGEMM_ERR_INVALID_VALUE;
+    return SGEMM_OK;
+}
+
+void config_as_plan(int index, sgemm_plan_t *out)
+{
+    *out = sgemm_plan_t{};
+    const sgemm_cfg::TileConfig &c = sgemm_cfg::kFfmaConfigs[index];
+    out->kernel = SGEMM_KERNEL_FFMA;
+    out->config = index;
+    out->bm = c.bm;
+    out->bn = c.bn;
+    out->bk = c.bk;
+    out->stages = c.stages;
+    out->threads = c.threads;
+    out->ctas_per_sm = c.ctas_per_sm;
+    out->splits = 1;
+}
+
+int choose_ffma(int M, int N, int K, int num_sms, bool beta_read, int force_config, int force_splits,
+                int *config, int *splits)
+{
+    const int kb = static_cast<int>(ceil_div(K, sgemm_cfg::kFfmaBK));
+    const int max_s = std::max(1, std::min(kb, kMaxSplits));
+    if (force_config >= sgemm_cfg::kNumFfmaConfigs) return SGEMM_ERR_INVALID_VALUE;
+    if (force_splits < 0) return SGEMM_ERR_INVALID_VALUE;
+    double best = INFINITY;
+    int best_c = 0, best_s = 1;
+    for (int ci = 0; ci < sgemm_cfg::kNumFfmaConfigs; ++ci) {
+        if (force_config >= 0 && ci != force_config) continue;
+        const int s_lo = force_splits > 0 ? std::min(force_splits, max_s) : 1;
+        const int s_hi = force_splits > 0 ? s_lo : max_s;
+        for (int s = s_lo; s <= s_hi; ++s) {
+            const double t = model_time(sgemm_cfg::kFfmaConfigs[ci], M, N, K, s, num_sms, beta_read);
+            // Prefer earlier rows and fewer splits unless clearly faster (2 %).
+            if (t < best * 0.98) {
+                best = t;
+                best_c = ci;
+                best_s = s;
+            }
+        }
+    }
+    *config = best_c;
+    *splits = best_s;
+    return SGEMM_OK;
+}
+
+int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
+{
+    const int v = validate(q);
+    if (v != SGEMM_OK) return v;
+    *out = sgemm_plan_t{};
+    out->config = -1;
+    out->math_mode = q.math_mode;
+    out->splits = 1;
+    if (q.M == 0 || q.N == 0) {
+        out->kernel = SGEMM_KERNEL_NONE;
+        return SGEMM_OK;
+    }
+    if (q.K == 0 || q.alpha == 0.0f) {
+        if (q.beta == 1.0f) {
+            out->kernel = SGEMM_KERNEL_NONE;
+        } else {
+            out->kernel = SGEMM_KERNEL_SCALE;
+            out->launches = 1;
+        }
+        return SGEMM_OK;
+    }
+    const bool a_ok = (q.align_flags & 1) && q.lda % 4 == 0;
+    const bool b_ok = (q.align_flags & 2) && q.ldb % 4 == 0;
+    out->repack_a = a_ok ? 0 : 1;
+    out->repack_b = b_ok ? 0 : 1;
+    out->vec_c = ((q.align_flags & 4) && q.ldc % 4 == 0) ? 1 : 0;
+
+    int cfg = 0, S = 1;
+    const int rc = choose_ffma(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f, ov.force_config, ov.force_splits, &cfg, &S);
+    if (rc != SGEMM_OK) return rc;
+    const sgemm_cfg::TileConfig &c = sgemm_cfg::kFfmaConfigs[cfg];
+    config_as_plan(cfg, out);
+    out->math_mode = q.math_mode;
+    out->repack_a = a_ok ? 0 : 1;
+    out->repack_b = b_ok ? 0 : 1;
+    out->vec_c = ((q.align_flags & 4) && q.ldc % 4 == 0) ? 1 : 0;
+    out->splits = S;
+    out->tiles_m = static_cast<int>(ceil_div(q.M, c.bm));
+    out->tiles_n = static_cast<int>(ceil_div(q.N, c.bn));
+    const long long units = static_cast<long long>(out->tiles_m) * out->tiles_n * S;
+    if (units > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
+    out->units = static_cast<int>(units);
+    out->grid = static_cast<int>(std::min<long long>(units, static_cast<long long>(q.num_sms) * c.ctas_per_sm));
+
+    const Workspace w = workspace_layout(q, *out);
+    out->workspace_bytes = w.total;
+    out->launches = 1 + out->repack_a + out->repack_b + (S > 1 ? 1 : 0);
+    return SGEMM_OK;
+}
+
+Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
+{
+    Workspace w{};
+    long long off = 0;
+    if (p.repack_a) {
+        w.lda = round_up(q.K, 4);
+        w.a_off = off;
+        off += round_up(static_cast<long long>(q.M) * w.lda * 4, 256);
+    }
+    if (p.repack_b) {
+        w.ldb = round_up(q.N, 4);
+        w.b_off = off;
+        off += round_up(static_cast<long long>(q.K) * w.ldb * 4, 256);
+    }
+    if (p.splits > 1) {
+        w.ldw = round_up(q.N, 4);
+        w.wstride = static_cast<long long>(q.M) * w.ldw;
+        w.w_off = off;
+        off += round_up(static_cast<long long>(p.splits) * w.wstride * 4, 256);
+    }
+    w.total = off;
+    return w;
+}
+
+}  // namespace sgemm_impl

@@ -1,0 +1,41 @@
+// Host-only planner interface (validation, tile-config / split-K choice,
+// workspace layout). Used by the C ABI; needs no CUDA runtime.
+#pragma once
+
+#include "../../include/sgemm.h"
+#include "tile_table.h"
+
+namespace sgemm_impl {
+
+constexpr int kMaxSplits = 16;
+
+struct Problem {
+    int M, N, K;
+    int lda, ldb, ldc;
+    int align_flags;  // bit 0: A 16-byte aligned, bit 1: B, bit 2: C
+    int num_sms;
+    int math_mode;
+    float alpha, beta;
+};
+
+struct Overrides {
+    int force_config = -1;  // table row, -1 automatic
+    int force_splits = 0;   // 0 automatic
+};
+
+// Offsets (bytes) into the handle's workspace and the strides used there.
+struct Workspace {
+    long long a_off = 0, lda = 0;       // repacked A (M x lda), when plan.repack_a
+    long long b_off = 0, ldb = 0;       // repacked B (K x ldb), when plan.repack_b
+    long long w_off = 0, ldw = 0, wstride = 0;  // split-K partials, when plan.splits > 1
+    long long total = 0;
+};
+
+int validate(const Problem &q);
+int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out);
+Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p);
+void config_as_plan(int index, sgemm_plan_t *out);
+int choose_ffma(int M, int N, int K, int num_sms, bool beta_read, int force_config, int force_splits,
+                int *config, int *splits);
+
+}  // namespace sgemm_impl

@@ -1,0 +1,431 @@
+// C ABI of the GB300 SGEMM library: handle lifetime, argument checks, plan
+// execution (repack -> mainloop -> split-K reduce), host-buffer entry point
+// and status reporting. Declarations and contracts: include/sgemm.h.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sgemm.h"
+#include "planner.h"
+#include "sgemm_internal.h"
+
+using namespace sgemm_impl;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct sgemm_handle_s {
+    int device = 0;
+    int num_sms = 0;
+    int math_mode = SGEMM_MATH_FP32;
+    int *d_status = nullptr;
+    void *workspace = nullptr;
+    size_t ws_bytes = 0;
+    float *stage = nullptr;  // sgemm_run_host device copies of A | B | C
+    size_t stage_bytes = 0;
+    Overrides ov;
+    int inject_skip = -1;
+    int log = 0;
+    long long timeout_ns = 4000000000LL;
+    sgemm_plan_t last{};
+    EncodeTiledFn encode = nullptr;
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA; }
+
+// Bind the handle's device for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+int ensure_workspace(sgemm_handle_t h, size_t bytes)
+{
+    if (bytes <= h->ws_bytes) return SGEMM_OK;
+    if (h->workspace) {
+        // Earlier launches on any stream may still read the old buffer.
+        if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+        cudaFree(h->workspace);
+        h->workspace = nullptr;
+        h->ws_bytes = 0;
+    }
+    const size_t grow = bytes + bytes / 4;
+    if (cudaMalloc(&h->workspace, grow) != cudaSuccess) {
+        cudaGetLastError();
+        h->workspace = nullptr;
+        return SGEMM_ERR_ALLOC;
+    }
+    h->ws_bytes = grow;
+    return SGEMM_OK;
+}
+
+// 2-D FP32 tensor map over a row-major (outer x inner) matrix with row stride ld.
+int make_tmap(sgemm_handle_t h, CUtensorMap *map, const float *base, int inner, int outer, long long ld,
+              int box_inner, int box_outer, CUtensorMapSwizzle swz)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+int check_args(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+               float *C, int ldc)
+{
+    if (h == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    Problem q{M, N, K, lda, ldb, ldc, 0, 1, SGEMM_MATH_FP32, alpha, 0.0f};
+    const int v = validate(q);
+    if (v != SGEMM_OK) return v;
+    if (M > 0 && N > 0) {
+        if (C == nullptr) return SGEMM_ERR_INVALID_VALUE;
+        if (K > 0 && alpha != 0.0f && (A == nullptr || B == nullptr)) return SGEMM_ERR_INVALID_VALUE;
+    }
+    return SGEMM_OK;
+}
+
+void log_plan(const sgemm_plan_t &p, int M, int N, int K)
+{
+    std::fprintf(stderr,
+                 "[sgemm] M=%d N=%d K=%d kernel=%d config=%d tile=%dx%dx%d stages=%d splits=%d units=%d grid=%d "
+                 "repack=(%d,%d) vec_c=%d mode=%d launches=%d ws=%lld\n",
+                 M, N, K, p.kernel, p.config, p.bm, p.bn, p.bk, p.stages, p.splits, p.units, p.grid, p.repack_a,
+                 p.repack_b, p.vec_c, p.math_mode, p.launches, p.workspace_bytes);
+}
+
+int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+               float beta, float *C, int ldc, cudaStream_t stream)
+{
+    const int align = (aligned16(A) ? 1 : 0) | (aligned16(B) ? 2 : 0) | (aligned16(C) ? 4 : 0);
+    Problem q{M, N, K, lda, ldb, ldc, align, h->num_sms, h->math_mode, alpha, beta};
+    sgemm_plan_t plan;
+    int rc = make_plan(q, h->ov, &plan);
+    if (rc != SGEMM_OK) return rc;
+    if (h->log) log_plan(plan, M, N, K);
+    h->last = plan;
+    if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;
+    if (plan.kernel == SGEMM_KERNEL_SCALE)
+        return launch_scale(M, N, beta, C, ldc, h->num_sms, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+
+    const Workspace w = workspace_layout(q, plan);
+    if ((rc = ensure_workspace(h, static_cast<size_t>(w.total))) != SGEMM_OK) return rc;
+    char *ws = static_cast<char *>(h->workspace);
+
+    const float *a_src = A;
+    long long a_ld = lda;
+    const float *b_src = B;
+    long long b_ld = ldb;
+    if (plan.repack_a) {
+        float *dst = reinterpret_cast<float *>(ws + w.a_off);
+        if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        a_src = dst;
+        a_ld = w.lda;
+    }
+    if (plan.repack_b) {
+        float *dst = reinterpret_cast<float *>(ws + w.b_off);
+        if (launch_repack(B, ldb, dst, w.ldb, K, N, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        b_src = dst;
+        b_ld = w.ldb;
+    }
+
+    CUtensorMap tmA, tmB;
+    if ((rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kFfmaBK, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        SGEMM_OK)
+        return rc;
+    if ((rc = make_tmap(h, &tmB, b_src, N, K, b_ld, plan.bn, sgemm_cfg::kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+        SGEMM_OK)
+        return rc;
+
+    FfmaParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.W = plan.splits > 1 ? reinterpret_cast<float *>(ws + w.w_off) : nullptr;
+    p.ldw = w.ldw;
+    p.wstride = w.wstride;
+    p.splits = plan.splits;
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.units = plan.units;
+    p.kblocks = (K + sgemm_cfg::kFfmaBK - 1) / sgemm_cfg::kFfmaBK;
+    p.vec_c = plan.vec_c;
+    p.status = h->d_status;
+    p.timeout_ns = h->timeout_ns;
+    p.inject_skip = h->inject_skip;
+    if (launch_ffma(plan.config, tmA, tmB, p, plan.grid, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (plan.splits > 1) {
+        if (launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
+                                 h->num_sms, stream) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgemm_create(sgemm_handle_t *out)
+{
+    if (out == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_ARCH;
+    }
+    return sgemm_create_for_device(dev, out);
+}
+
+int sgemm_create_for_device(int dev, sgemm_handle_t *out)
+{
+    if (out == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || dev < 0 || dev >= count) {
+        cudaGetLastError();
+        return count > 0 ? SGEMM_ERR_INVALID_VALUE : SGEMM_ERR_ARCH;
+    }
+    DeviceGuard g(dev);
+    if (!g.ok) return SGEMM_ERR_CUDA;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_ARCH;
+    }
+    if (major != 10 || minor != 3) return SGEMM_ERR_ARCH;
+
+    sgemm_handle_t h = new (std::nothrow) sgemm_handle_s();
+    if (h == nullptr) return SGEMM_ERR_ALLOC;
+    h->device = dev;
+    h->num_sms = sms;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+            cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || fn == nullptr) {
+        delete h;
+        return SGEMM_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    if (ffma_set_attributes() != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return SGEMM_ERR_CUDA;
+    }
+    if (cudaMalloc(&h->d_status, 256) != cudaSuccess || cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->d_status) cudaFree(h->d_status);
+        delete h;
+        return SGEMM_ERR_ALLOC;
+    }
+    const char *env = std::getenv("SGEMM_LOG");
+    h->log = (env != nullptr && env[0] == '1') ? 1 : 0;
+    *out = h;
+    return SGEMM_OK;
+}
+
+int sgemm_destroy(sgemm_handle_t h)
+{
+    if (h == nullptr) return SGEMM_OK;
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    if (h->workspace) cudaFree(h->workspace);
+    if (h->stage) cudaFree(h->stage);
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+    return SGEMM_OK;
+}
+
+int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+              float beta, float *C, int ldc, struct CUstream_st *stream)
+{
+    const int v = check_args(h, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (v != SGEMM_OK) return v;
+    DeviceGuard g(h->device);
+    if (!g.ok) return SGEMM_ERR_CUDA;
+    return run_device(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                   int ldb, float beta, float *C, int ldc, struct CUstream_st *stream)
+{
+    const int v = check_args(h, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (v != SGEMM_OK) return v;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    DeviceGuard g(h->device);
+    if (!g.ok) return SGEMM_ERR_CUDA;
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    // Device copies with row strides rounded up to 4 floats keep every
+    // operand on the aligned (TMA, 16-byte) path.
+    const long long dlda = (K + 3) / 4 * 4, dldb = (N + 3) / 4 * 4, dldc = (N + 3) / 4 * 4;
+    const long long a_elems = need_ab ? static_cast<long long>(M) * (dlda > 0 ? dlda : 4) : 0;
+    const long long b_elems = need_ab ? static_cast<long long>(K) * dldb : 0;
+    const long long c_elems = static_cast<long long>(M) * dldc;
+    const size_t bytes = static_cast<size_t>(a_elems + b_elems + c_elems) * 4u + 512u;
+    if (bytes > h->stage_bytes) {
+        if (h->stage) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+            cudaFree(h->stage);
+            h->stage = nullptr;
+            h->stage_bytes = 0;
+        }
+        if (cudaMalloc(&h->stage, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return SGEMM_ERR_ALLOC;
+        }
+        h->stage_bytes = bytes;
+    }
+    float *dA = h->stage;
+    float *dB = dA + (a_elems + 63) / 64 * 64;
+    float *dC = dB + (b_elems + 63) / 64 * 64;
+    cudaStream_t s = stream;
+    if (need_ab) {
+        if (cudaMemcpy2DAsync(dA, dlda * 4, A, static_cast<size_t>(lda) * 4, static_cast<size_t>(K) * 4, M,
+                              cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpy2DAsync(dB, dldb * 4, B, static_cast<size_t>(ldb) * 4, static_cast<size_t>(N) * 4, K,
+                              cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+    }
+    if (beta != 0.0f) {
+        if (cudaMemcpy2DAsync(dC, dldc * 4, C, static_cast<size_t>(ldc) * 4, static_cast<size_t>(N) * 4, M,
+                              cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+    }
+    int rc = run_device(h, M, N, K, alpha, need_ab ? dA : nullptr, static_cast<int>(dlda > 0 ? dlda : 1),
+                        need_ab ? dB : nullptr, static_cast<int>(dldb), beta, dC, static_cast<int>(dldc), s);
+    if (rc != SGEMM_OK) return rc;
+    if (h->last.kernel == SGEMM_KERNEL_NONE) return cuda_status(cudaStreamSynchronize(s));  // beta == 1: C unchanged
+    if (cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 4, dC, dldc * 4, static_cast<size_t>(N) * 4, M,
+                          cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+int sgemm_set_math_mode(sgemm_handle_t h, int mode)
+{
+    if (h == nullptr || (mode != SGEMM_MATH_FP32 && mode != SGEMM_MATH_TF32)) return SGEMM_ERR_INVALID_VALUE;
+    if (mode == SGEMM_MATH_TF32) return SGEMM_ERR_NOT_SUPPORTED;
+    h->math_mode = mode;
+    return SGEMM_OK;
+}
+
+int sgemm_get_math_mode(sgemm_handle_t h, int *mode)
+{
+    if (h == nullptr || mode == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    *mode = h->math_mode;
+    return SGEMM_OK;
+}
+
+int sgemm_set_option(sgemm_handle_t h, int option, long long value)
+{
+    if (h == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    switch (option) {
+    case SGEMM_OPT_FORCE_CONFIG:
+        if (value < -1 || value >= sgemm_cfg::kNumFfmaConfigs) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.force_config = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_FORCE_SPLITS:
+        if (value < 0 || value > kMaxSplits) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.force_splits = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_WAIT_TIMEOUT_NS:
+        if (value < 1000000LL || value > 60000000000LL) return SGEMM_ERR_INVALID_VALUE;
+        h->timeout_ns = value;
+        return SGEMM_OK;
+    case SGEMM_OPT_INJECT_SKIP:
+        if (value < -1 || value > (1LL << 30)) return SGEMM_ERR_INVALID_VALUE;
+        h->inject_skip = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_LOG:
+        h->log = value ? 1 : 0;
+        return SGEMM_OK;
+    default:
+        return SGEMM_ERR_INVALID_VALUE;
+    }
+}
+
+int sgemm_check_device_status(sgemm_handle_t h, struct CUstream_st *stream, int *device_status)
+{
+    if (h == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    DeviceGuard g(h->device);
+    if (!g.ok) return SGEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SGEMM_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (code != 0 && cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (device_status) *device_status = code;
+    return code == 0 ? SGEMM_OK : (code >> 16);
+}
+
+int sgemm_plan(int M, int N, int K, int lda, int ldb, int ldc, int align_flags, int num_sms, int math_mode,
+               sgemm_plan_t *out)
+{
+    if (out == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    Problem q{M, N, K, lda, ldb, ldc, align_flags, num_sms, math_mode, 1.0f, 1.0f};
+    return make_plan(q, Overrides{}, out);
+}
+
+int sgemm_last_plan(sgemm_handle_t h, sgemm_plan_t *out)
+{
+    if (h == nullptr || out == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    *out = h->last;
+    return SGEMM_OK;
+}
+
+int sgemm_config_count(void) { return sgemm_cfg::kNumFfmaConfigs; }
+
+int sgemm_config_info(int index, sgemm_plan_t *out)
+{
+    if (out == nullptr || index < 0 || index >= sgemm_cfg::kNumFfmaConfigs) return SGEMM_ERR_INVALID_VALUE;
+    config_as_plan(index, out);
+    return SGEMM_OK;
+}
+
+const char *sgemm_status_string(int status)
+{
+    switch (status) {
+    case SGEMM_OK: return "SGEMM_OK: success";
+    case SGEMM_ERR_INVALID_VALUE: return "SGEMM_ERR_INVALID_VALUE: invalid dimension, leading dimension, pointer, handle or option";
+    case SGEMM_ERR_ARCH: return "SGEMM_ERR_ARCH: the current device is not an sm_103 (GB300) GPU";
+    case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: device allocation failed";
+    case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: kernel launch failed";
+    case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait ran out";
+    case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA runtime or driver call failed";
+    case SGEMM_ERR_NOT_SUPPORTED: return "SGEMM_ERR_NOT_SUPPORTED: valid request that is not implemented";
+    default: return "unknown sgemm status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Interface between the host side of the library (planner, handle, C ABI in
+// sgemm_api.cpp / planner.cpp) and its kernels (*.cu). Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "tile_table.h"
+
+namespace sgemm_impl {
+
+// Device status codes: (sgemm_status << 16) | where.
+enum : int {
+    kWhereConsumerFull = 1,  // a consumer's wait for a filled stage ran out
+    kWhereProducerEmpty = 2, // the producer's wait for a released stage ran out
+    kWhereDrain = 3,         // waiting for this CTA's own copies in flight ran out
+    kWhereMmaEmpty = 4,      // TF32: the MMA issuer's wait for a filled stage ran out
+    kWhereAccum = 5,         // TF32: the epilogue's wait for the accumulator ran out
+    kWhereTmemAlloc = 6      // TF32: TMEM allocation failed
+};
+
+// Everything the FFMA mainloop needs besides the two tensor maps.
+struct FfmaParams {
+    int M, N, K;
+    float alpha, beta;
+    float *C;
+    long long ldc;
+    float *W;          // split-K partials: slice s at W + s * wstride, row stride ldw
+    long long ldw;
+    long long wstride;
+    int splits;
+    int tiles_m, tiles_n;
+    int units;         // tiles_m * tiles_n * splits
+    int kblocks;       // ceil(K / 32)
+    int vec_c;         // C may be accessed with 16-byte vectors
+    int *status;       // device status word (first error wins)
+    long long timeout_ns;
+    int inject_skip;   // test only: CTA 0's producer never fills its n-th stage (-1 off)
+};
+
+// Plain-launch helpers implemented in the .cu files. All return the CUDA
+// error of the launch (cudaSuccess when it was enqueued).
+cudaError_t ffma_set_attributes();  // opt in to large dynamic shared memory (current device)
+cudaError_t launch_ffma(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const FfmaParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
+                                 int M, int N, float alpha, float beta, float *C, long long ldc,
+                                 int vec_c, int num_sms, cudaStream_t stream);
+cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms,
+                         cudaStream_t stream);
+cudaError_t launch_repack(const float *src, long long lds, float *dst, long long ldd, int rows,
+                          int cols, int num_sms, cudaStream_t stream);
+
+}  // namespace sgemm_impl

@@ -1,0 +1,193 @@
+/*
+ * sgemm.h — single-precision GEMM for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * The operation (all calls below compute it):
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ *   A is M x K, B is K x N, C is M x N, FP32, all three row-major:
+ *   element (i, k) of A is A[i*lda + k], (k, j) of B is B[k*ldb + j],
+ *   (i, j) of C is C[i*ldc + j]. All offsets are computed in 64 bits.
+ *
+ *   Source of the definition: "SGEMM CUDA kernel (First Half)", opening
+ *   definition (S = single precision, GEMM: C = alpha AB + beta C, A is M x K,
+ *   B is K x N) and its Part 1 (row-major offsets row * ncols + col);
+ *   "Optimizing Matrix Multiplication in CUDA", the kernels' argument order
+ *   (M, N, K, alpha, A, B, beta, C) in the global-memory coalescing section.
+ *   Leading dimensions (row strides >= the column count) are this library's
+ *   extension; the pages use packed matrices.
+ *
+ * Conventions where the pages are silent (BLAS practice):
+ *   - M == 0 or N == 0: nothing is touched, SGEMM_OK.
+ *   - K == 0 or alpha == 0: A and B are not read; C = beta * C
+ *     (beta == 1: C untouched; beta == 0: C set to +0 without being read).
+ *   - beta == 0: C is never read, so NaN/Inf already in C does not propagate.
+ *   - C must not overlap A or B.
+ *   - Misaligned pointers or leading dimensions are not an error: the library
+ *     switches to a path that does not need 16-byte alignment.
+ *
+ * Numerics: the default mode (SGEMM_MATH_FP32) performs only IEEE FP32 fused
+ * multiply-adds (round to nearest even); each output is within
+ * (K + 2) * 2^-24 * (|alpha| sum_k |a_ik||b_kj| + |beta||c_ij|) of the exact
+ * result, and is bitwise reproducible for a fixed (shape, alignment, plan).
+ * SGEMM_MATH_TF32 rounds A and B to TF32 on the tensor cores: the same bound
+ * holds with 2^-10 in place of 2^-24.
+ *
+ * Errors: every call returns an sgemm_status value. Launches are asynchronous
+ * on the given stream; a kernel watchdog (bounded waits inside the kernels)
+ * records SGEMM_ERR_TIMEOUT in the handle's device status word, which
+ * sgemm_check_device_status() reads.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* same type as cudaStream_t; NULL means the legacy default stream */
+
+typedef struct sgemm_handle_s *sgemm_handle_t;
+
+typedef enum sgemm_status {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_VALUE = 1, /* bad dimension, leading dimension, pointer, handle or option */
+    SGEMM_ERR_ARCH = 2,          /* current device is not sm_103 (GB300) */
+    SGEMM_ERR_ALLOC = 3,         /* device or pinned allocation failed */
+    SGEMM_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError) */
+    SGEMM_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (see sgemm_check_device_status) */
+    SGEMM_ERR_CUDA = 6,          /* another CUDA runtime/driver call failed */
+    SGEMM_ERR_NOT_SUPPORTED = 7  /* the request is valid but not implemented */
+} sgemm_status_t;
+
+typedef enum sgemm_math_mode {
+    SGEMM_MATH_FP32 = 0, /* default: FP32 FFMA on the CUDA cores, exact-FP32 semantics */
+    SGEMM_MATH_TF32 = 1  /* opt-in: tcgen05 tensor cores with TF32 inputs, FP32 accumulate */
+} sgemm_math_mode_t;
+
+/* Kernels a plan can use (sgemm_plan_t.kernel). */
+typedef enum sgemm_kernel_kind {
+    SGEMM_KERNEL_NONE = 0,  /* quick return, nothing launched */
+    SGEMM_KERNEL_SCALE = 1, /* C = beta * C only (K == 0 or alpha == 0) */
+    SGEMM_KERNEL_FFMA = 2,  /* FP32 FFMA mainloop */
+    SGEMM_KERNEL_TF32 = 3   /* tcgen05 TF32 mainloop */
+} sgemm_kernel_kind_t;
+
+/* What sgemm_run does for one problem (filled by sgemm_plan / sgemm_last_plan). */
+typedef struct sgemm_plan_s {
+    int kernel;              /* sgemm_kernel_kind_t */
+    int config;              /* row of the tile-config table, -1 if none */
+    int bm, bn, bk, stages;  /* CTA tile and pipeline depth */
+    int threads;             /* threads per CTA */
+    int ctas_per_sm;         /* resident CTAs per SM the grid is sized for */
+    int splits;              /* split-K factor S (1 = fused epilogue) */
+    int tiles_m, tiles_n;    /* output tiles */
+    int units;               /* tiles_m * tiles_n * splits work units */
+    int grid;                /* CTAs launched (persistent: min(units, SMs * ctas_per_sm)) */
+    int repack_a, repack_b;  /* operand first copied to a 16-byte-aligned workspace copy */
+    int vec_c;               /* 1: C read/written with 16-byte accesses */
+    int math_mode;           /* sgemm_math_mode_t */
+    int launches;            /* kernels one sgemm_run launches for this plan */
+    long long workspace_bytes; /* device workspace the handle holds for it */
+} sgemm_plan_t;
+
+/* Tuning and test options for sgemm_set_option. */
+typedef enum sgemm_option {
+    SGEMM_OPT_FORCE_CONFIG = 1,   /* table row to use (-1 = automatic, the default) */
+    SGEMM_OPT_FORCE_SPLITS = 2,   /* split-K factor (0 = automatic, the default) */
+    SGEMM_OPT_WAIT_TIMEOUT_NS = 3,/* watchdog limit of every in-kernel wait (default 4e9 ns) */
+    SGEMM_OPT_INJECT_SKIP = 4,    /* TEST ONLY: the producer of CTA 0 never fills its n-th stage
+                                     (-1 = off, the default); the consumers' wait then runs out
+                                     and the run reports SGEMM_ERR_TIMEOUT without faulting */
+    SGEMM_OPT_LOG = 5             /* 1: print the chosen plan of each call to stderr */
+} sgemm_option_t;
+
+/*
+ * Create a handle bound to the current CUDA device.
+ * out: receives the handle (set to NULL on failure).
+ * Returns SGEMM_ERR_ARCH unless the device is compute capability 10.3,
+ * SGEMM_ERR_ALLOC if its small device status word cannot be allocated.
+ * The handle owns a lazily grown device workspace (split-K partials and
+ * aligned operand copies) and, for sgemm_run_host, device staging buffers.
+ * A handle must not be used by two host threads or two streams at once.
+ */
+int sgemm_create(sgemm_handle_t *out);
+
+/* Same as sgemm_create for CUDA device ordinal `device` (the calling thread's
+ * current device is left unchanged). SGEMM_ERR_INVALID_VALUE for an ordinal
+ * that does not exist. */
+int sgemm_create_for_device(int device, sgemm_handle_t *out);
+
+/* Free the handle and everything it owns. NULL is accepted. Waits for the
+ * device to finish work that may still use the workspace. */
+int sgemm_destroy(sgemm_handle_t h);
+
+/*
+ * C = alpha * A * B + beta * C on the device, asynchronously on `stream`.
+ * A, B, C: caller-owned DEVICE pointers (the library never frees them).
+ * Requirements: M, N, K >= 0; lda >= max(1, K); ldb >= max(1, N);
+ * ldc >= max(1, N); A and B non-NULL when M, N > 0 and K > 0 and alpha != 0;
+ * C non-NULL when M, N > 0. Any violation returns SGEMM_ERR_INVALID_VALUE
+ * and touches nothing. SGEMM_ERR_ALLOC if the workspace cannot grow.
+ */
+int sgemm_run(sgemm_handle_t h, int M, int N, int K,
+              float alpha, const float *A, int lda,
+              const float *B, int ldb,
+              float beta, float *C, int ldc,
+              struct CUstream_st *stream);
+
+/*
+ * Same operation with HOST operands: copies A, B (and C when beta != 0) to
+ * handle-owned device buffers on `stream`, runs sgemm_run, copies C back and
+ * synchronizes `stream` before returning. Pinned (page-locked) host memory
+ * gives asynchronous, full-bandwidth copies; pageable memory also works.
+ * Same argument rules as sgemm_run (pointers are host pointers).
+ */
+int sgemm_run_host(sgemm_handle_t h, int M, int N, int K,
+                   float alpha, const float *A, int lda,
+                   const float *B, int ldb,
+                   float beta, float *C, int ldc,
+                   struct CUstream_st *stream);
+
+/* Select SGEMM_MATH_FP32 (default) or SGEMM_MATH_TF32 for later runs. */
+int sgemm_set_math_mode(sgemm_handle_t h, int mode);
+int sgemm_get_math_mode(sgemm_handle_t h, int *mode);
+
+/* Set a tuning/test option (sgemm_option_t). Unknown options or values:
+ * SGEMM_ERR_INVALID_VALUE. */
+int sgemm_set_option(sgemm_handle_t h, int option, long long value);
+
+/*
+ * Synchronize `stream`, then read and clear the handle's device status word.
+ * device_status (may be NULL) receives 0 when no kernel reported a problem,
+ * else a code whose upper 16 bits are an sgemm_status value (SGEMM_ERR_TIMEOUT)
+ * and lower bits say which wait ran out. Returns that sgemm_status value, or
+ * SGEMM_ERR_CUDA if synchronizing failed (e.g. a sticky device error).
+ */
+int sgemm_check_device_status(sgemm_handle_t h, struct CUstream_st *stream, int *device_status);
+
+/*
+ * Host-only planning: what sgemm_run would launch for this problem on a GPU
+ * with `num_sms` SMs. align_flags: bit 0 = A is 16-byte aligned, bit 1 = B,
+ * bit 2 = C. Validates like sgemm_run (pointers are not checked here).
+ * Needs no GPU.
+ */
+int sgemm_plan(int M, int N, int K, int lda, int ldb, int ldc, int align_flags,
+               int num_sms, int math_mode, sgemm_plan_t *out);
+
+/* The plan used by the handle's most recent sgemm_run / sgemm_run_host. */
+int sgemm_last_plan(sgemm_handle_t h, sgemm_plan_t *out);
+
+/* Number of rows in the tile-config table, and row `index` (as a plan whose
+ * problem-dependent fields are zero). Needs no GPU. */
+int sgemm_config_count(void);
+int sgemm_config_info(int index, sgemm_plan_t *out);
+
+/* Static description of a status code. Never NULL. */
+const char *sgemm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

@@ -1,0 +1,113 @@
+"""The C ABI library loads, exports every function include/sgemm.h declares, and plans on the host."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp32_gemm_04_gb300 as sg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sgemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|char|void)\s*\*?\s*(sgemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_core_calls():
+    names = declared_functions()
+    for n in ("sgemm_create", "sgemm_run", "sgemm_destroy", "sgemm_set_math_mode", "sgemm_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and the binding covers them all
+    assert set(declared_functions()) <= set(sg._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for st in range(8):
+        s = sg.status_string(st)
+        assert s and "unknown" not in s
+    assert "unknown" in sg.status_string(99)
+
+
+def test_null_handle_is_rejected(lib):
+    assert lib.sgemm_run(None, 4, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, None) == sg.SGEMM_ERR_INVALID_VALUE
+    assert lib.sgemm_set_option(None, sg.OPT_LOG, 1) == sg.SGEMM_ERR_INVALID_VALUE
+    assert lib.sgemm_destroy(None) == sg.SGEMM_OK
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    st = lib.sgemm_create(ctypes.byref(h))
+    assert st in (sg.SGEMM_ERR_ARCH, sg.SGEMM_ERR_INVALID_VALUE) and not h.value
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, 4, 4, 4), (4, -1, 4, 4, 4, 4), (4, 4, -1, 4, 4, 4),
+    (4, 4, 8, 7, 4, 4),   # lda < K
+    (4, 8, 4, 4, 7, 8),   # ldb < N
+    (4, 8, 4, 4, 8, 7),   # ldc < N
+    (4, 4, 0, 0, 4, 4),   # lda < max(1, K)
+])
+def test_plan_rejects_bad_dimensions(lib, args):
+    M, N, K, lda, ldb, ldc = args
+    p = sg.Plan()
+    assert lib.sgemm_plan(M, N, K, lda, ldb, ldc, 7, 152, 0, ctypes.byref(p)) == sg.SGEMM_ERR_INVALID_VALUE
+
+
+def test_plan_quick_returns(lib):
+    assert sg.plan(0, 5, 5).kernel == sg.KERNEL_NONE
+    assert sg.plan(5, 0, 5).kernel == sg.KERNEL_NONE
+    p = sg.plan(5, 5, 0)
+    assert p.kernel == sg.KERNEL_NONE  # sgemm_plan assumes beta == 1 for the K == 0 case
+    assert p.launches == 0
+
+
+def test_plan_square_4096(lib):
+    p = sg.plan(4096, 4096, 4096, num_sms=152)
+    assert p.kernel == sg.KERNEL_FFMA and p.splits == 1
+    assert p.repack_a == 0 and p.repack_b == 0 and p.vec_c == 1
+    assert p.units == p.tiles_m * p.tiles_n * p.splits
+    assert p.grid <= 152 * p.ctas_per_sm and p.grid == min(p.units, 152 * p.ctas_per_sm)
+    assert p.launches == 1 and p.workspace_bytes == 0
+
+
+def test_plan_ragged_unaligned_repacks(lib):
+    # ld = 1531 / 3001 floats are not multiples of 4: rows are not 16-byte aligned,
+    # so both operands go through the aligned workspace copy and C is scalar.
+    p = sg.plan(2047, 3001, 1531, lda=1531, ldb=3001, ldc=3001)
+    assert p.repack_a == 1 and p.repack_b == 1 and p.vec_c == 0
+    assert p.launches == 3 + (1 if p.splits > 1 else 0)
+    assert p.workspace_bytes >= 4 * (2047 * 1532 + 1531 * 3004)
+
+
+def test_plan_misaligned_pointer_repacks(lib):
+    p = sg.plan(512, 512, 512, align_flags=0b110)
+    assert p.repack_a == 1 and p.repack_b == 0
+
+
+def test_plan_skinny_uses_split_k(lib):
+    for M, N in ((16384, 64), (64, 16384)):
+        p = sg.plan(M, N, 8192, num_sms=152)
+        assert p.kernel == sg.KERNEL_FFMA
+        assert p.splits > 1, p.as_dict()
+        assert p.units >= 152
+        assert p.workspace_bytes >= p.splits * M * N * 4
+
+
+def test_config_table(lib):
+    rows = sg.configs()
+    assert len(rows) >= 1
+    for r in rows:
+        assert r.bm % 32 == 0 and r.bn % 64 == 0 and r.bk == 32
+        assert r.threads == ((r.bm // 32) * (r.bn // 64) + 1) * 32

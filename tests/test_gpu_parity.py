@@ -1,0 +1,214 @@
+"""GPU parity: the library (through its C ABI) against the FP64 oracle.
+
+Bit-exact on integer-valued operands; within
+(K + 2) * 2^-24 * (|alpha| sum |a||b| + |beta||c|) elementwise on real ones.
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_04_gb300 as sg
+import oracle
+from dense_fp32_gemm_04_gb300 import inputs
+from gpu_helpers import check_against_oracle, run_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_gemm_04_gb300 import _build
+
+    _build.build()
+    handle = sg.Sgemm(0)
+    yield handle
+    handle.close()
+
+
+def ops(M, N, K, seed, dist=("int", "int", "int")):
+    return inputs.problem_operands(M=M, N=N, K=K, seed=seed, dist=dist)
+
+
+def test_tiny_shapes_exact(h):
+    """Every M, N, K in 1..9 with integer operands: bit-exact, guards intact."""
+    for M, N, K in itertools.product(range(1, 10), repeat=3):
+        A, B, C = ops(M, N, K, seed=M * 100 + N * 10 + K)
+        got, guards, st = run_gemm(torch, h, A, B, C, 1.5, -0.5)
+        assert st == sg.SGEMM_OK and guards, (M, N, K)
+        check_against_oracle(got, A, B, C, 1.5, -0.5, exact=True)
+
+
+@pytest.mark.parametrize("cfg", range(4))
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_every_config_and_split(h, cfg, splits):
+    """Each tile-config row and split factor, around tile multiples, integer and real operands."""
+    h.set_option(sg.OPT_FORCE_CONFIG, cfg)
+    h.set_option(sg.OPT_FORCE_SPLITS, splits)
+    try:
+        for (M, N, K) in [(63, 65, 33), (129, 127, 95), (200, 300, 257), (256, 128, 224)]:
+            A, B, C = ops(M, N, K, seed=cfg * 10 + splits)
+            got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
+            assert st == sg.SGEMM_OK and guards
+            p = h.last_plan()
+            assert p.config == cfg and p.splits == min(splits, (K + 31) // 32)
+            check_against_oracle(got, A, B, C, 1.5, 0.5, exact=True)
+            Ar, Br, Cr = ops(M, N, K, seed=cfg * 10 + splits + 1, dist=("normal", "uniform", "uniform"))
+            got, guards, st = run_gemm(torch, h, Ar, Br, Cr, -0.75, 1.25)
+            assert st == sg.SGEMM_OK and guards
+            check_against_oracle(got, Ar, Br, Cr, -0.75, 1.25)
+    finally:
+        h.set_option(sg.OPT_FORCE_CONFIG, -1)
+        h.set_option(sg.OPT_FORCE_SPLITS, 0)
+
+
+def test_deterministic(h):
+    A, B, C = ops(300, 260, 700, seed=5, dist=("normal", "normal", "uniform"))
+    r1, _, _ = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+    r2, _, _ = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+    assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
+
+
+def test_leading_dimensions_and_misalignment(h):
+    """Padded leading dimensions keep pad columns untouched; misaligned pointers take the repack path."""
+    M, N, K = 190, 170, 150
+    A, B, C = ops(M, N, K, seed=77)
+    for lds, offs in [((K + 4, N + 8, N + 12), (0, 0, 0)),    # aligned, padded
+                      ((K + 1, N + 3, N + 5), (0, 0, 0)),     # unaligned strides
+                      ((None, None, None), (1, 2, 3)),        # unaligned pointers
+                      ((K + 3, N, N + 1), (2, 0, 1))]:
+        got, guards, st = run_gemm(torch, h, A, B, C, 2.0, -1.0, lds=lds, offsets=offs)
+        assert st == sg.SGEMM_OK and guards, (lds, offs)
+        check_against_oracle(got, A, B, C, 2.0, -1.0, exact=True)
+    p = h.last_plan()
+    assert p.repack_a == 1 and p.vec_c == 0
+
+
+def test_quick_returns(h):
+    M, N, K = 70, 90, 40
+    A, B, C = ops(M, N, K, seed=3, dist=("uniform", "uniform", "uniform"))
+    nanA = np.full_like(A, np.nan)
+    nanB = np.full_like(B, np.nan)
+    # alpha == 0: A, B not read; C = beta * C
+    got, guards, st = run_gemm(torch, h, nanA, nanB, C, 0.0, 0.5)
+    assert st == sg.SGEMM_OK and guards and np.array_equal(got, 0.5 * C)
+    # alpha == 0, beta == 1: C untouched
+    got, guards, st = run_gemm(torch, h, nanA, nanB, C, 0.0, 1.0)
+    assert st == sg.SGEMM_OK and guards and np.array_equal(got, C)
+    # beta == 0: C not read (NaN in C must not appear)
+    nanC = np.full_like(C, np.nan)
+    got, guards, st = run_gemm(torch, h, A, B, nanC, 1.0, 0.0)
+    assert st == sg.SGEMM_OK and guards and np.all(np.isfinite(got))
+    check_against_oracle(got, A, B, None, 1.0, 0.0)
+    # alpha == 0, beta == 0: C = 0 without reading it
+    got, guards, st = run_gemm(torch, h, nanA, nanB, nanC, 0.0, 0.0)
+    assert st == sg.SGEMM_OK and guards and np.all(got == 0)
+    # K == 0
+    A0 = np.zeros((M, 0), np.float32)
+    B0 = np.zeros((0, N), np.float32)
+    got, guards, st = run_gemm(torch, h, A0, B0, C, 1.0, 2.0)
+    assert st == sg.SGEMM_OK and guards and np.array_equal(got, 2.0 * C)
+    # M == 0 / N == 0: nothing touched
+    for (m, n) in ((0, N), (M, 0)):
+        Am = np.zeros((m, K), np.float32)
+        Bn = np.zeros((K, n), np.float32)
+        Cm = np.zeros((m, n), np.float32)
+        got, guards, st = run_gemm(torch, h, Am, Bn, Cm, 1.0, 0.0)
+        assert st == sg.SGEMM_OK and guards
+
+
+def test_invalid_arguments_touch_nothing(h):
+    M, N, K = 16, 16, 16
+    A, B, C = ops(M, N, K, seed=1)
+    bufs = [torch.from_numpy(x).cuda() for x in (A, B, C)]
+    pA, pB, pC = (b.data_ptr() for b in bufs)
+    bad = [(-1, N, K, K, N, N), (M, N, K, K - 1, N, N), (M, N, K, K, N - 1, N), (M, N, K, K, N, N - 1)]
+    for (m, n, k, lda, ldb, ldc) in bad:
+        assert h.run_ptr(m, n, k, 1.0, pA, lda, pB, ldb, 0.0, pC, ldc) == sg.SGEMM_ERR_INVALID_VALUE
+    assert h.run_ptr(M, N, K, 1.0, None, K, pB, N, 0.0, pC, N) == sg.SGEMM_ERR_INVALID_VALUE
+    assert h.run_ptr(M, N, K, 1.0, pA, K, pB, N, 0.0, None, N) == sg.SGEMM_ERR_INVALID_VALUE
+    torch.cuda.synchronize()
+    assert np.array_equal(bufs[2].cpu().numpy(), C)
+
+
+def test_non_default_stream(h):
+    A, B, C = ops(333, 222, 111, seed=8)
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        h.run(dA, dB, dC, 1.0, 1.0, stream=s)
+    s.synchronize()
+    check_against_oracle(dC.cpu().numpy(), A, B, C, 1.0, 1.0, exact=True)
+
+
+def test_run_host(h):
+    """Host-operand entry point (the e2e path): padded host strides, pinned and pageable."""
+    M, N, K = 257, 131, 513
+    A, B, C = ops(M, N, K, seed=21, dist=("normal", "normal", "uniform"))
+    Ab = inputs.with_ld(A, K + 3)
+    Cb = inputs.with_ld(C, N + 1)
+    out = Cb.copy()
+    h.run_host(Ab[:, :K], B, out[:, :N], 1.5, 0.5)
+    check_against_oracle(out[:, :N], A, B, C, 1.5, 0.5)
+    assert np.isnan(out[:, N:]).all()
+    pinned = [torch.from_numpy(x).pin_memory() for x in (A, B, C)]
+    h.run_host(pinned[0], pinned[1], pinned[2], 1.5, 0.5)
+    check_against_oracle(pinned[2].numpy(), A, B, C, 1.5, 0.5)
+
+
+# ---- the benchmark problems ------------------------------------------------
+
+def _problem(name):
+    p = inputs.PROBLEMS[name]
+    A, B, C = inputs.problem_operands(name)
+    return p, A, B, C
+
+
+def test_square256(h):
+    p, A, B, C = _problem("square256")
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    check_against_oracle(got, A, B, C, p["alpha"], p["beta"])
+
+
+@pytest.mark.parametrize("name", ["square4096", "square4096_int"])
+def test_square4096(h, name):
+    p, A, B, C = _problem(name)
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    rows = sample_rows(p["M"])
+    check_against_oracle(got, A, B, C, p["alpha"], p["beta"], rows=rows, exact=name.endswith("_int"))
+
+
+@pytest.mark.parametrize("name", ["ragged", "ragged_int"])
+def test_ragged(h, name):
+    p, A, B, C = _problem(name)
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    plan = h.last_plan()
+    assert plan.repack_a and plan.repack_b and not plan.vec_c
+    check_against_oracle(got, A, B, C, p["alpha"], p["beta"], exact=name.endswith("_int"))
+
+
+@pytest.mark.parametrize("n", [512, 1024, 2048, 8192, 16384])
+def test_sweep(h, n):
+    p, A, B, C = _problem(f"sweep{n}")
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    rows = None if n <= 2048 else sample_rows(n, n_random=16 if n > 8192 else 48)
+    check_against_oracle(got, A, B, C, p["alpha"], p["beta"], rows=rows)
+
+
+@pytest.mark.parametrize("name", ["skinny_tall", "skinny_wide"])
+def test_skinny(h, name):
+    p, A, B, C = _problem(name)
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    assert h.last_plan().splits > 1
+    rows = sample_rows(p["M"]) if p["M"] > 4096 else None
+    check_against_oracle(got, A, B, C, p["alpha"], p["beta"], rows=rows)
