@@ -77,7 +77,10 @@ _SIGNATURES = {
     "sgemm_config_count": ([], _I),
     "sgemm_config_info": ([_I, ctypes.POINTER(Plan)], _I),
     "sgemm_status_string": ([_I], ctypes.c_char_p),
+    "sgemm_run_splitk_static": ([_I, _I, _I, _F, _P, _I, _P, _I, _F, _P, _I, _I, _P, _P], _I),
 }
+
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def library():
@@ -116,6 +119,22 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, align_flags=7, num_sms=152, math
     _check(library().sgemm_plan(M, N, K, lda, ldb, ldc, align_flags, num_sms, math_mode, ctypes.byref(p)),
            "sgemm_plan")
     return p
+
+
+def run_splitk_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, splits, device_status=None, stream=None) -> int:
+    """Split-K SGEMM that allocates nothing (static 32 MiB scratch); raw device pointers.
+
+    For callers that cannot call cudaMalloc. Returns the C-ABI status (no
+    exception). ``stream`` is a torch stream, a raw handle or None (current
+    torch stream).
+    """
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return library().sgemm_run_splitk_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, splits,
+                                             device_status, s)
 
 
 def configs():

@@ -149,6 +149,45 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K,
                    float beta, float *C, int ldc,
                    struct CUstream_st *stream);
 
+/*
+ * Split-K SGEMM that allocates no device memory. The pages have no
+ * counterpart to this call; it exists for callers that cannot call cudaMalloc:
+ * code running inside another runtime's memory pool, which must not grow
+ * device memory behind that pool's back, and latency-sensitive loops that
+ * cannot afford the device-wide synchronization cudaMalloc / cudaFree imply.
+ *
+ * Computes the same C = alpha * A * B + beta * C as sgemm_run (same argument
+ * rules, DEVICE pointers, asynchronous on `stream`), always with the split-K
+ * kernels: `splits` in 1..16 K slices (clamped to ceil(K / 32)) whose partial
+ * sums go to a static scratch array, then a reduction in slice order. No
+ * handle is needed.
+ *
+ * Scratch: a file-scope static device array of SGEMM_STATIC_SCRATCH_BYTES
+ * (32 MiB), held by every GPU that loads this library until process exit.
+ * It must fit splits * M * roundup(N, 4) floats of partials, plus aligned
+ * copies of A (M * roundup(K, 4)) and/or B (K * roundup(N, 4)) when an operand
+ * is not 16-byte aligned or its leading dimension is not a multiple of 4;
+ * otherwise the call returns SGEMM_ERR_NOT_SUPPORTED and launches nothing.
+ * All calls on a device share the array and it keeps the last call's
+ * contents: calls that overlap on the GPU (e.g. on two unordered streams)
+ * race on it.
+ *
+ * device_status: optional caller-owned device int that receives the
+ * kernels' watchdog code (see sgemm_check_device_status); it is set to 0 on
+ * `stream` at the start of the call. NULL uses an internal static word.
+ *
+ * The first call on a device performs a one-time set-up with that device
+ * current (looks up the array's device address, sets kernel attributes);
+ * make that first call before any stream capture.
+ */
+#define SGEMM_STATIC_SCRATCH_BYTES (32u << 20)
+int sgemm_run_splitk_static(int M, int N, int K,
+                            float alpha, const float *A, int lda,
+                            const float *B, int ldb,
+                            float beta, float *C, int ldc,
+                            int splits, int *device_status,
+                            struct CUstream_st *stream);
+
 /* Select SGEMM_MATH_FP32 (default) or SGEMM_MATH_TF32 for later runs. */
 int sgemm_set_math_mode(sgemm_handle_t h, int mode);
 int sgemm_get_math_mode(sgemm_handle_t h, int *mode);
