@@ -118,6 +118,28 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     out->repack_a = a_ok ? 0 : 1;
     out->repack_b = b_ok ? 0 : 1;
     out->vec_c = ((q.align_flags & 4) && q.ldc % 4 == 0) ? 1 : 0;
+    if (q.math_mode == SGEMM_MATH_TF32) {
+        // B always goes through the workspace: transposed to K-major (N x roundup(K, 4)).
+        if (q.K > 65535LL * 32) return SGEMM_ERR_NOT_SUPPORTED;
+        out->kernel = SGEMM_KERNEL_TF32;
+        out->bm = sgemm_cfg::kTf32BM;
+        out->bn = sgemm_cfg::kTf32BN;
+        out->bk = sgemm_cfg::kTf32BK;
+        out->stages = sgemm_cfg::kTf32Stages;
+        out->threads = sgemm_cfg::kTf32Threads;
+        out->ctas_per_sm = 1;
+        out->splits = 1;
+        out->repack_b = 1;
+        out->tiles_m = static_cast<int>(ceil_div(q.M, out->bm));
+        out->tiles_n = static_cast<int>(ceil_div(q.N, out->bn));
+        const long long units = static_cast<long long>(out->tiles_m) * out->tiles_n;
+        if (units > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
+        out->units = static_cast<int>(units);
+        out->grid = static_cast<int>(std::min<long long>(units, q.num_sms));
+        out->workspace_bytes = workspace_layout(q, *out).total;
+        out->launches = 1 + out->repack_a + 1;
+        return SGEMM_OK;
+    }
 
     int cfg = 0, S = 1;
     const int rc = choose_ffma(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f, ov.force_config, ov.force_splits, &cfg, &S);
@@ -151,7 +173,12 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
         w.a_off = off;
         off += round_up(static_cast<long long>(q.M) * w.lda * 4, 256);
     }
-    if (p.repack_b) {
+    if (p.kernel == SGEMM_KERNEL_TF32) {
+        // B^T, K-major: N rows of roundup(K, 4) floats.
+        w.ldb = round_up(q.K, 4);
+        w.b_off = off;
+        off += round_up(static_cast<long long>(q.N) * w.ldb * 4, 256);
+    } else if (p.repack_b) {
         w.ldb = round_up(q.N, 4);
         w.b_off = off;
         off += round_up(static_cast<long long>(q.K) * w.ldb * 4, 256);

@@ -118,6 +118,47 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
                  p.repack_b, p.vec_c, p.math_mode, p.launches, p.workspace_bytes);
 }
 
+// TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop.
+int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int M, int N, int K, float alpha,
+             const float *A, int lda, const float *B, int ldb, float beta, float *C, int ldc, cudaStream_t stream)
+{
+    char *ws = static_cast<char *>(h->workspace);
+    const float *a_src = A;
+    long long a_ld = lda;
+    if (plan.repack_a) {
+        float *dst = reinterpret_cast<float *>(ws + w.a_off);
+        if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        a_src = dst;
+        a_ld = w.lda;
+    }
+    float *bt = reinterpret_cast<float *>(ws + w.b_off);
+    if (launch_transpose(B, ldb, bt, w.ldb, K, N, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    CUtensorMap tmA, tmBt;
+    int rc;
+    if ((rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kTf32BK, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        SGEMM_OK)
+        return rc;
+    if ((rc = make_tmap(h, &tmBt, bt, K, N, w.ldb, sgemm_cfg::kTf32BK, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        SGEMM_OK)
+        return rc;
+    Tf32Params p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.units = plan.units;
+    p.kblocks = (K + sgemm_cfg::kTf32BK - 1) / sgemm_cfg::kTf32BK;
+    p.vec_c = plan.vec_c;
+    p.status = h->d_status;
+    p.timeout_ns = h->timeout_ns;
+    return launch_tf32(tmA, tmBt, p, plan.grid, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
                float beta, float *C, int ldc, cudaStream_t stream)
 {
@@ -140,6 +181,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     long long a_ld = lda;
     const float *b_src = B;
     long long b_ld = ldb;
+    if (plan.kernel == SGEMM_KERNEL_TF32) return run_tf32(h, plan, w, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
     if (plan.repack_a) {
         float *dst = reinterpret_cast<float *>(ws + w.a_off);
         if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -239,7 +281,7 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
         return SGEMM_ERR_CUDA;
     }
     h->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (ffma_set_attributes() != cudaSuccess) {
+    if (ffma_set_attributes() != cudaSuccess || tf32_set_attributes() != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return SGEMM_ERR_CUDA;
@@ -336,7 +378,6 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
 int sgemm_set_math_mode(sgemm_handle_t h, int mode)
 {
     if (h == nullptr || (mode != SGEMM_MATH_FP32 && mode != SGEMM_MATH_TF32)) return SGEMM_ERR_INVALID_VALUE;
-    if (mode == SGEMM_MATH_TF32) return SGEMM_ERR_NOT_SUPPORTED;
     h->math_mode = mode;
     return SGEMM_OK;
 }

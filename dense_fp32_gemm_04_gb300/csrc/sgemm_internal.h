@@ -39,6 +39,21 @@ struct FfmaParams {
     int inject_skip;   // test only: CTA 0's producer never fills its n-th stage (-1 off)
 };
 
+// Everything the TF32 tcgen05 mainloop needs besides the two tensor maps
+// (A: M x K, and B^T: N x K, both K-major).
+struct Tf32Params {
+    int M, N, K;
+    float alpha, beta;
+    float *C;
+    long long ldc;
+    int tiles_m, tiles_n;
+    int units;         // tiles_m * tiles_n
+    int kblocks;       // ceil(K / 32)
+    int vec_c;
+    int *status;
+    long long timeout_ns;
+};
+
 // Plain-launch helpers implemented in the .cu files. All return the CUDA
 // error of the launch (cudaSuccess when it was enqueued).
 cudaError_t ffma_set_attributes();  // opt in to large dynamic shared memory (current device)
@@ -49,6 +64,11 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
                                  int vec_c, int num_sms, cudaStream_t stream);
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms,
                          cudaStream_t stream);
+cudaError_t tf32_set_attributes();
+cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
+                        cudaStream_t stream);
+cudaError_t launch_transpose(const float *B, long long ldb, float *BT, long long ldbt, int K, int N,
+                             cudaStream_t stream);
 cudaError_t launch_repack(const float *src, long long lds, float *dst, long long ldd, int rows,
                           int cols, int num_sms, cudaStream_t stream);
 

@@ -46,4 +46,12 @@ constexpr TileConfig kFfmaConfigs[] = {
 };
 constexpr int kNumFfmaConfigs = sizeof(kFfmaConfigs) / sizeof(kFfmaConfigs[0]);
 
+// The flagged TF32 tensor-core mode: one CTA per SM computes 128 x 256 tiles
+// (tcgen05.mma M = 128, N = 256) from 32-deep K slabs in a 4-stage ring.
+constexpr int kTf32BM = 128, kTf32BN = 256, kTf32BK = 32, kTf32Stages = 4, kTf32Threads = 192;
+constexpr int tf32_smem_bytes()
+{
+    return 1024 + kTf32Stages * (kTf32BM + kTf32BN) * kTf32BK * 4 + 256;
+}
+
 }  // namespace sgemm_cfg

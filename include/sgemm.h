@@ -96,7 +96,7 @@ typedef enum sgemm_option {
     SGEMM_OPT_FORCE_CONFIG = 1,   /* table row to use (-1 = automatic, the default) */
     SGEMM_OPT_FORCE_SPLITS = 2,   /* split-K factor (0 = automatic, the default) */
     SGEMM_OPT_WAIT_TIMEOUT_NS = 3,/* watchdog limit of every in-kernel wait (default 4e9 ns) */
-    SGEMM_OPT_INJECT_SKIP = 4,    /* TEST ONLY: the producer of CTA 0 never fills its n-th stage
+    SGEMM_OPT_INJECT_SKIP = 4,    /* TEST ONLY: CTA 0 never issues the copy of its n-th k-slab
                                      (-1 = off, the default); the consumers' wait then runs out
                                      and the run reports SGEMM_ERR_TIMEOUT without faulting */
     SGEMM_OPT_LOG = 5             /* 1: print the chosen plan of each call to stderr */

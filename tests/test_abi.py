@@ -110,4 +110,4 @@ def test_config_table(lib):
     assert len(rows) >= 1
     for r in rows:
         assert r.bm % 32 == 0 and r.bn % 64 == 0 and r.bk == 32
-        assert r.threads == ((r.bm // 32) * (r.bn // 64) + 1) * 32
+        assert r.threads == ((r.bm // 32) * (r.bn // 64) + 1) * 32  # warp tiles + the TMA producer warp

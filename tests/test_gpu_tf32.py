@@ -1,0 +1,116 @@
+"""GPU parity of the flagged TF32 tensor-core mode (SGEMM_MATH_TF32).
+
+Bounds: the stated TF32 bound (K + 2) * 2^-10 * (|alpha| sum |a||b| + |beta||c|)
+is very loose at large K, so every case is also held to a tighter one that
+follows the same rounding argument more closely: each operand is rounded to
+TF32 (relative error below 2^-10, so a product is off by below 2^-9 + 2^-20),
+then K products are summed in FP32 (depth K + 2 with alpha/beta):
+|err| <= (2^-9 + 2^-20 + (K + 2) * 2^-24) * magnitude. A wrong descriptor or
+layout would fail the tight bound by orders of magnitude. Integer operands in
+{-2..2} are exact in TF32, so those runs must be bit-exact.
+"""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_04_gb300 as sg
+import oracle
+from dense_fp32_gemm_04_gb300 import inputs
+from gpu_helpers import run_gemm, sample_rows
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_gemm_04_gb300 import _build
+
+    _build.build()
+    handle = sg.Sgemm(0)
+    handle.set_math_mode(sg.MATH_TF32)
+    yield handle
+    handle.close()
+
+
+def _check(got, A, B, C, alpha, beta, rows=None, exact=False):
+    K = A.shape[1]
+    ref, mag = oracle.sgemm_f64(A, B, C, alpha, beta, rows=rows)
+    g = (got if rows is None else got[rows]).astype(np.float64)
+    assert np.all(np.isfinite(g))
+    err = np.abs(g - ref)
+    assert np.all(err <= oracle.bound(K, mag, oracle.U_TF32)), "outside the TF32 bound"
+    tight = (2.0**-9 + 2.0**-20 + (K + 2) * 2.0**-24) * mag
+    bad = err > tight
+    assert not bad.any(), f"{int(bad.sum())} elements outside the tight TF32 bound, worst ratio {float(np.max(err / np.maximum(tight, 1e-300))):.3g}"
+    if exact:
+        assert oracle.exact(got if rows is None else got[rows], ref)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (128, 256, 32), (129, 257, 33), (256, 256, 256), (300, 500, 200),
+                                   (77, 1000, 517)])
+def test_integer_exact(h, shape):
+    M, N, K = shape
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=M + N + K, dist=("int", "int", "int"))
+    got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
+    assert st == sg.SGEMM_OK and guards
+    plan = h.last_plan()
+    assert plan.kernel == sg.KERNEL_TF32
+    assert h.check_device_status() == (sg.SGEMM_OK, 0)
+    _check(got, A, B, C, 1.5, 0.5, exact=True)
+
+
+def test_real_square(h):
+    A, B, C = inputs.problem_operands(M=512, N=512, K=512, seed=5, dist=("uniform", "uniform", "uniform"))
+    got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
+    assert st == sg.SGEMM_OK and guards
+    _check(got, A, B, C, 1.5, 0.5)
+
+
+def test_ragged_problem(h):
+    p = inputs.PROBLEMS["ragged"]
+    A, B, C = inputs.problem_operands("ragged")
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    assert h.last_plan().repack_a == 1
+    _check(got, A, B, C, p["alpha"], p["beta"])
+
+
+def test_unaligned_and_padded(h):
+    M, N, K = 190, 300, 130
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=6, dist=("int", "int", "int"))
+    for lds, offs in [((K + 4, N + 8, N + 4), (0, 0, 0)), ((K + 1, N + 3, N + 1), (1, 2, 3))]:
+        got, guards, st = run_gemm(torch, h, A, B, C, 1.0, -1.0, lds=lds, offsets=offs)
+        assert st == sg.SGEMM_OK and guards
+        _check(got, A, B, C, 1.0, -1.0, exact=True)
+
+
+@pytest.mark.parametrize("name", ["square4096", "square4096_int"])
+def test_square4096(h, name):
+    p = inputs.PROBLEMS[name]
+    A, B, C = inputs.problem_operands(name)
+    got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
+    assert st == sg.SGEMM_OK and guards
+    assert h.check_device_status() == (sg.SGEMM_OK, 0)
+    _check(got, A, B, C, p["alpha"], p["beta"], rows=sample_rows(p["M"]), exact=name.endswith("_int"))
+
+
+def test_deterministic(h):
+    A, B, C = inputs.problem_operands(M=384, N=512, K=640, seed=7, dist=("normal", "normal", "uniform"))
+    r1, _, _ = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+    r2, _, _ = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+    assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
+
+
+def test_mode_switch_back_to_fp32(h):
+    A, B, C = inputs.problem_operands(M=200, N=200, K=300, seed=8, dist=("normal", "normal", "uniform"))
+    h.set_math_mode(sg.MATH_FP32)
+    try:
+        got, _, st = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+        assert st == sg.SGEMM_OK and h.last_plan().kernel == sg.KERNEL_FFMA
+        ref, mag = oracle.sgemm_f64(A, B, C, 1.0, 1.0)
+        assert oracle.check(got, ref, mag, 300)[0]
+    finally:
+        h.set_math_mode(sg.MATH_TF32)
