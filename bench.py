@@ -43,6 +43,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--tf32-steps", type=int, default=50, help="calls timed in the flagged TF32 mode (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
@@ -390,7 +391,8 @@ def run_ours(args, world):
     e2e_t = world.max(time.perf_counter() - t0)
     e2e_value = flops * e2e_steps * world.size / e2e_t / 1e12
 
-    tf32 = measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, world.local_rank)
+    tf32 = (measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, world.local_rank, args.tf32_steps)
+            if args.tf32_steps > 0 else None)
 
     clocks = sampler.summary(t_wall0, t_wall1)
     nsm = props.multi_processor_count
@@ -400,7 +402,9 @@ def run_ours(args, world):
     peak = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if peak else None, "traffic": recorded_traffic(),
-                "kernel": "ffma_sgemm_kernel (plan config %d, %dx%d tile)" % (plan.config, plan.bm, plan.bn),
+                "kernel": ("ffma_sgemm_kernel (plan config %d, %dx%d tile)" % (plan.config, plan.bm, plan.bn)) +
+                          (" + tail_reduce_kernel (timed together per call: a lower bound for the mainloop)"
+                           if plan.tail_splits > 1 else ""),
                 "peak_basis": f"{nsm} SMs x 128 FP32 FMA/clk x 2 FLOP x median SM clock under load "
                               f"({sm_mhz} MHz, nvidia-smi during the timed region)",
                 "frac_at_max_clock": (achieved / (nsm * 256 * clocks["sm_max_mhz"] * 1e-6)) if clocks else None}

@@ -64,25 +64,49 @@ struct Tile {
     static_assert(A_BYTES % 1024 == 0, "A stages must keep the 1024-byte swizzle alignment");
 };
 
-// Work unit u -> (tile row tm, tile column tn, K split ks). Splits of a tile
-// are adjacent; tiles run in groups of kGroupM tile rows, column by column,
-// so concurrently running CTAs share B columns and A rows in L2.
-__device__ __forceinline__ void decode_unit(const FfmaParams &p, int u, int &tm, int &tn, int &ks)
+// Tile index t -> (tile row, tile column): tiles run in groups of kGroupM
+// tile rows, column by column, so concurrently running CTAs share B columns
+// and A rows in L2.
+__device__ __forceinline__ void decode_tile(int tiles_m, int tiles_n, int t, int &tm, int &tn)
 {
-    ks = u % p.splits;
-    const int t = u / p.splits;
-    const int per_group = kGroupM * p.tiles_n;
+    const int per_group = kGroupM * tiles_n;
     const int g = t / per_group;
     const int first_m = g * kGroupM;
-    const int gsize = min(p.tiles_m - first_m, kGroupM);
+    const int gsize = min(tiles_m - first_m, kGroupM);
     const int r = t - g * per_group;
     tm = first_m + r % gsize;
     tn = r / gsize;
 }
 
-__device__ __forceinline__ int split_begin(const FfmaParams &p, int ks)
+// Work unit u -> (tile row tm, tile column tn, K slice ks of nsplit). Slices
+// of a tile are adjacent units. In tail-split mode the first n_full units are
+// whole tiles and the rest are tail_splits slices of the remaining tiles.
+__device__ __forceinline__ void decode_unit(const FfmaParams &p, int u, int &t, int &tm, int &tn, int &ks,
+                                            int &nsplit)
 {
-    return static_cast<int>((static_cast<long long>(ks) * p.kblocks) / p.splits);
+    if (p.tail_splits > 1) {
+        if (u < p.n_full) {
+            t = u;
+            ks = 0;
+            nsplit = 1;
+        } else {
+            const int v = u - p.n_full;
+            t = p.n_full + v / p.tail_splits;
+            ks = v % p.tail_splits;
+            nsplit = p.tail_splits;
+        }
+    } else {
+        ks = u % p.splits;
+        t = u / p.splits;
+        nsplit = p.splits;
+    }
+    decode_tile(p.tiles_m, p.tiles_n, t, tm, tn);
+}
+
+// First k-block of slice ks of nsplit (balanced integer split of kblocks).
+__device__ __forceinline__ int split_begin(const FfmaParams &p, int ks, int nsplit)
+{
+    return static_cast<int>((static_cast<long long>(ks) * p.kblocks) / nsplit);
 }
 
 template <class T>
@@ -96,10 +120,10 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
     int seq = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-        int tm, tn, ks;
-        decode_unit(p, u, tm, tn, ks);
-        const int kb1 = split_begin(p, ks + 1);
-        for (int kb = split_begin(p, ks); kb < kb1; ++kb) {
+        int t, tm, tn, ks, ns;
+        decode_unit(p, u, t, tm, tn, ks, ns);
+        const int kb1 = split_begin(p, ks + 1, ns);
+        for (int kb = split_begin(p, ks, ns); kb < kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             const uint32_t empty = bar_base + 8 * (T::STAGES + stage);
             if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -209,11 +233,27 @@ __device__ __forceinline__ void store_c4(const FfmaParams &p, int row, int col, 
 }
 
 template <class T>
-__device__ __forceinline__ void epilogue(const FfmaParams &p, const float2 (&acc)[8][4], int tm, int tn,
-                                         int ks, int wm, int wn, int r, int c)
+__device__ __forceinline__ void epilogue(const FfmaParams &p, const float2 (&acc)[8][4], int tile, int tm,
+                                         int tn, int ks, int nsplit, int wm, int wn, int r, int c)
 {
     const int row0 = tm * T::BM + wm * T::WM + r;
     const int col0 = tn * T::BN + wn * T::WN + c * 4;
+    if (p.tail_splits > 1 && nsplit > 1) {
+        // Tail-split slice: the whole partial tile, tile-packed (rows beyond M
+        // or columns beyond N hold sums of the copy engine's zero fill).
+        float *W = p.W + (static_cast<long long>(tile - p.n_full) * p.tail_splits + ks) * (T::BM * T::BN);
+        const int lr0 = wm * T::WM + r;
+        const int lc0 = wn * T::WN + c * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                *reinterpret_cast<float4 *>(W + (lr0 + 4 * i) * T::BN + lc0 + 32 * h) =
+                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+            }
+        }
+        return;
+    }
     if (p.splits > 1) {
         // Partial sums to this split's slice; the reduction applies alpha/beta.
         float *W = p.W + static_cast<long long>(ks) * p.wstride;
@@ -294,15 +334,16 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         int tm, tn, ks;
-        decode_unit(p, u, tm, tn, ks);
+        int t, ns;
+        decode_unit(p, u, t, tm, tn, ks, ns);
         float2 acc[8][4];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
-        const int kb1 = split_begin(p, ks + 1);
-        for (int kb = split_begin(p, ks); kb < kb1; ++kb) {
+        const int kb1 = split_begin(p, ks + 1, ns);
+        for (int kb = split_begin(p, ks, ns); kb < kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
@@ -321,7 +362,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 phase ^= 1u;
             }
         }
-        epilogue<T>(p, acc, tm, tn, ks, wm, wn, r, c);
+        epilogue<T>(p, acc, t, tm, tn, ks, ns, wm, wn, r, c);
     }
 }
 
@@ -395,6 +436,37 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, long long ldw,
     }
 }
 
+// Tail-split reduction: for every tail tile, C = alpha * sum_s P_s + beta * C
+// with its tail_splits partial tiles added in slice order. One thread per 4
+// consecutive columns of a tile row.
+__global__ void tail_reduce_kernel(const FfmaParams p, int bm, int bn)
+{
+    const int n_tail = p.tiles_m * p.tiles_n - p.n_full;
+    const int q4 = bn / 4;
+    const long long per_tile = static_cast<long long>(bm) * q4;
+    const long long total = per_tile * n_tail;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int q = static_cast<int>(idx / per_tile);
+        const int e = static_cast<int>(idx - static_cast<long long>(q) * per_tile);
+        const int lr = e / q4, lc = (e - lr * q4) * 4;
+        int tm, tn;
+        decode_tile(p.tiles_m, p.tiles_n, p.n_full + q, tm, tn);
+        const int row = tm * bm + lr, col = tn * bn + lc;
+        if (row >= p.M || col >= p.N) continue;
+        const float *w = p.W + static_cast<long long>(q) * p.tail_splits * bm * bn + lr * bn + lc;
+        float4 s = *reinterpret_cast<const float4 *>(w);
+        for (int k = 1; k < p.tail_splits; ++k) {
+            const float4 t = *reinterpret_cast<const float4 *>(w + static_cast<long long>(k) * bm * bn);
+            s.x += t.x;
+            s.y += t.y;
+            s.z += t.z;
+            s.w += t.w;
+        }
+        store_c4(p, row, col, s);
+    }
+}
+
 // C = beta * C for K == 0 or alpha == 0 (beta == 0 writes +0 without reading C).
 __global__ void scale_kernel(int M, int N, float beta, float *__restrict__ C, long long ldc)
 {
@@ -459,6 +531,13 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
     const long long work = static_cast<long long>(M) * ((N + 3) / 4);
     splitk_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(W, ldw, wstride, splits, M, N,
                                                                                    alpha, beta, C, ldc, vec_c);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)
+{
+    const long long work = static_cast<long long>(p.tiles_m * p.tiles_n - p.n_full) * bm * (bn / 4);
+    tail_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(p, bm, bn);
     return cudaGetLastError();
 }
 

@@ -27,7 +27,7 @@ struct Overrides {
 struct Workspace {
     long long a_off = 0, lda = 0;       // repacked A (M x lda), when plan.repack_a
     long long b_off = 0, ldb = 0;       // repacked B (K x ldb), when plan.repack_b
-    long long w_off = 0, ldw = 0, wstride = 0;  // split-K partials, when plan.splits > 1
+    long long w_off = 0, ldw = 0, wstride = 0;  // split-K partials (plan.splits > 1) or tail partials
     long long total = 0;
 };
 

@@ -113,9 +113,9 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
 {
     std::fprintf(stderr,
                  "[sgemm] M=%d N=%d K=%d kernel=%d config=%d tile=%dx%dx%d stages=%d splits=%d units=%d grid=%d "
-                 "repack=(%d,%d) vec_c=%d mode=%d launches=%d ws=%lld\n",
+                 "repack=(%d,%d) vec_c=%d mode=%d launches=%d ws=%lld tail=%dx%d\n",
                  M, N, K, p.kernel, p.config, p.bm, p.bn, p.bk, p.stages, p.splits, p.units, p.grid, p.repack_a,
-                 p.repack_b, p.vec_c, p.math_mode, p.launches, p.workspace_bytes);
+                 p.repack_b, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.tail_tiles, p.tail_splits);
 }
 
 // TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop.
@@ -223,7 +223,14 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
     p.inject_skip = h->inject_skip;
+    if (plan.tail_splits > 1) {
+        p.W = reinterpret_cast<float *>(ws + w.w_off);
+        p.n_full = plan.tiles_m * plan.tiles_n - plan.tail_tiles;
+        p.tail_splits = plan.tail_splits;
+    }
     if (launch_ffma(plan.config, tmA, tmB, p, plan.grid, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (plan.tail_splits > 1 && launch_tail_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1) {
         if (launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
                                  h->num_sms, stream) != cudaSuccess)

@@ -37,6 +37,12 @@ struct FfmaParams {
     int *status;       // device status word (first error wins)
     long long timeout_ns;
     int inject_skip;   // test only: CTA 0's producer never fills its n-th stage (-1 off)
+    // Tail split (wave quantisation): when tail_splits > 1, units [0, n_full)
+    // are whole tiles written straight to C, and each remaining tile is split
+    // into tail_splits K slices whose partial tiles go, tile-packed, to
+    // W + ((tile - n_full) * tail_splits + slice) * BM * BN. `splits` is then 1.
+    int n_full;
+    int tail_splits;
 };
 
 // Everything the TF32 tcgen05 mainloop needs besides the two tensor maps
@@ -62,6 +68,7 @@ cudaError_t launch_ffma(int config, const CUtensorMap &tmA, const CUtensorMap &t
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
                                  int vec_c, int num_sms, cudaStream_t stream);
+cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms,
                          cudaStream_t stream);
 cudaError_t tf32_set_attributes();

@@ -89,6 +89,9 @@ typedef struct sgemm_plan_s {
     int math_mode;           /* sgemm_math_mode_t */
     int launches;            /* kernels one sgemm_run launches for this plan */
     long long workspace_bytes; /* device workspace the handle holds for it */
+    int tail_tiles;          /* tiles of the last, partial round of the persistent grid that are
+                                split along K to even out the waves (0 = none) */
+    int tail_splits;         /* K slices per tail tile (their partials are reduced in order) */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */

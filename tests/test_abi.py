@@ -77,9 +77,21 @@ def test_plan_square_4096(lib):
     p = sg.plan(4096, 4096, 4096, num_sms=152)
     assert p.kernel == sg.KERNEL_FFMA and p.splits == 1
     assert p.repack_a == 0 and p.repack_b == 0 and p.vec_c == 1
-    assert p.units == p.tiles_m * p.tiles_n * p.splits
-    assert p.grid <= 152 * p.ctas_per_sm and p.grid == min(p.units, 152 * p.ctas_per_sm)
-    assert p.launches == 1 and p.workspace_bytes == 0
+    assert p.grid <= 152 * p.ctas_per_sm
+    # 1024 tiles on 152 CTAs: 6 whole rounds, then the 112 remaining tiles are
+    # split along K so the last round is shared by every CTA
+    tiles = p.tiles_m * p.tiles_n
+    slots = 152 * p.ctas_per_sm
+    assert p.tail_tiles == tiles - (tiles // slots) * slots == 112
+    assert p.tail_splits > 1
+    assert p.units == tiles - p.tail_tiles + p.tail_tiles * p.tail_splits
+    assert p.launches == 2 and p.workspace_bytes >= p.tail_tiles * p.tail_splits * p.bm * p.bn * 4
+
+
+def test_plan_full_rounds_have_no_tail(lib):
+    # 8192^3: 4096 tiles -> 26.9 rounds, the last one 94 % full: not worth splitting
+    p = sg.plan(8192, 8192, 8192, num_sms=152)
+    assert p.tail_tiles == 0 and p.units == p.tiles_m * p.tiles_n and p.launches == 1
 
 
 def test_plan_ragged_unaligned_repacks(lib):

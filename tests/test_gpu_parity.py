@@ -212,3 +212,22 @@ def test_skinny(h, name):
     assert h.last_plan().splits > 1
     rows = sample_rows(p["M"]) if p["M"] > 4096 else None
     check_against_oracle(got, A, B, C, p["alpha"], p["beta"], rows=rows)
+
+
+@pytest.mark.parametrize("shape", [(1000, 2500, 513), (1999, 3001, 1031), (1500, 4095, 2050)])
+def test_tail_split(h, shape):
+    """Shapes whose last round is split along K (tail split): exact on integers, bound on reals."""
+    M, N, K = shape
+    A, B, C = ops(M, N, K, seed=M + N, dist=("int", "int", "int"))
+    got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
+    assert st == sg.SGEMM_OK and guards
+    plan = h.last_plan()
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert plan.tail_splits > 1 and plan.tail_tiles > 0, plan.as_dict()
+    check_against_oracle(got, A, B, C, 1.5, 0.5, exact=True)
+    Ar, Br, Cr = ops(M, N, K, seed=M + N + 1, dist=("normal", "uniform", "uniform"))
+    got, guards, st = run_gemm(torch, h, Ar, Br, Cr, -1.0, 0.25)
+    assert st == sg.SGEMM_OK and guards
+    check_against_oracle(got, Ar, Br, Cr, -1.0, 0.25)
+    r2, _, _ = run_gemm(torch, h, Ar, Br, Cr, -1.0, 0.25)
+    assert np.array_equal(got.view(np.uint32), r2.view(np.uint32))
