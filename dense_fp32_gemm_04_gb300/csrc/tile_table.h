@@ -39,10 +39,12 @@ constexpr TileConfig make_ffma(int bm, int bn, int stages, int ctas, float cost)
 
 // Row order is part of the ABI of sgemm_config_info / SGEMM_OPT_FORCE_CONFIG.
 constexpr TileConfig kFfmaConfigs[] = {
-    make_ffma(128, 128, 5, 1, 1.00f),  // 0: large squares
-    make_ffma(128, 64, 4, 2, 1.05f),   // 1: N <= 64, or more tiles for mid sizes
-    make_ffma(64, 128, 4, 2, 1.05f),   // 2: M <= 64
-    make_ffma(64, 64, 4, 3, 1.20f),    // 3: small problems
+    // rel_cost: time per FMA relative to row 0, measured on large squares
+    // (4096^3 .. 16384^3, one split) by dense_fp32_gemm_04_gb300/tune.py.
+    make_ffma(128, 128, 5, 1, 1.000f),  // 0: large squares
+    make_ffma(128, 64, 4, 2, 1.055f),   // 1: N <= 64, or more tiles for mid sizes
+    make_ffma(64, 128, 4, 2, 1.055f),   // 2: M <= 64
+    make_ffma(64, 64, 4, 3, 1.430f),    // 3: tiny problems (1.5 consumer warps per scheduler)
 };
 constexpr int kNumFfmaConfigs = sizeof(kFfmaConfigs) / sizeof(kFfmaConfigs[0]);
 
