@@ -34,7 +34,15 @@ struct sgemm_handle_s {
     long long timeout_ns = 4000000000LL;
     sgemm_plan_t last{};
     EncodeTiledFn encode = nullptr;
+    // sgemm_run_host pipeline: copy-in and copy-out streams and their events.
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_end = nullptr;
+    cudaEvent_t ev_in[8] = {}, ev_done[8] = {};
 };
+
+namespace {
+constexpr int kMaxHostPanels = 8;
+}
 
 namespace {
 
@@ -157,6 +165,38 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
     return launch_tf32(tmA, tmBt, p, plan.grid, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+// Streams and events of the host-buffer pipeline, created on first use.
+int ensure_host_pipeline(sgemm_handle_t h)
+{
+    if (h->h2d != nullptr) return SGEMM_OK;
+    bool ok = cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_b, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_end, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kMaxHostPanels; ++i)
+        ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
+// Row panels for sgemm_run_host: enough that copies of later panels overlap the
+// compute of earlier ones, few enough that each panel still fills the GPU for
+// about two rounds of 128 x 128 tiles.
+int host_panels(sgemm_handle_t h, int M, int N, int K)
+{
+    if (static_cast<double>(M) * N * K < 1.0e9 || M < 256) return 1;
+    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
+    long long p = tiles / (2LL * h->num_sms);
+    if (p > 4) p = 4;
+    if (p > M / 128) p = M / 128;
+    return p < 1 ? 1 : static_cast<int>(p);
 }
 
 int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
@@ -312,6 +352,14 @@ int sgemm_destroy(sgemm_handle_t h)
     cudaDeviceSynchronize();
     if (h->workspace) cudaFree(h->workspace);
     if (h->stage) cudaFree(h->stage);
+    if (h->h2d) cudaStreamDestroy(h->h2d);
+    if (h->d2h) cudaStreamDestroy(h->d2h);
+    for (cudaEvent_t e : {h->ev_start, h->ev_b, h->ev_end})
+        if (e) cudaEventDestroy(e);
+    for (int i = 0; i < kMaxHostPanels; ++i) {
+        if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_done[i]) cudaEventDestroy(h->ev_done[i]);
+    }
     if (h->d_status) cudaFree(h->d_status);
     delete h;
     return SGEMM_OK;
@@ -359,27 +407,65 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     float *dA = h->stage;
     float *dB = dA + (a_elems + 63) / 64 * 64;
     float *dC = dB + (b_elems + 63) / 64 * 64;
-    cudaStream_t s = stream;
-    if (need_ab) {
-        if (cudaMemcpy2DAsync(dA, dlda * 4, A, static_cast<size_t>(lda) * 4, static_cast<size_t>(K) * 4, M,
-                              cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpy2DAsync(dB, dldb * 4, B, static_cast<size_t>(ldb) * 4, static_cast<size_t>(N) * 4, K,
-                              cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return SGEMM_ERR_CUDA;
-    }
-    if (beta != 0.0f) {
-        if (cudaMemcpy2DAsync(dC, dldc * 4, C, static_cast<size_t>(ldc) * 4, static_cast<size_t>(N) * 4, M,
-                              cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return SGEMM_ERR_CUDA;
-    }
-    int rc = run_device(h, M, N, K, alpha, need_ab ? dA : nullptr, static_cast<int>(dlda > 0 ? dlda : 1),
-                        need_ab ? dB : nullptr, static_cast<int>(dldb), beta, dC, static_cast<int>(dldc), s);
+    int rc = ensure_host_pipeline(h);
     if (rc != SGEMM_OK) return rc;
-    if (h->last.kernel == SGEMM_KERNEL_NONE) return cuda_status(cudaStreamSynchronize(s));  // beta == 1: C unchanged
-    if (cudaMemcpy2DAsync(C, static_cast<size_t>(ldc) * 4, dC, dldc * 4, static_cast<size_t>(N) * 4, M,
-                          cudaMemcpyDeviceToHost, s) != cudaSuccess)
+
+    // Pipeline over row panels of A and C: B and panel 0 go in first on the
+    // copy-in stream; panel p computes on `stream` once its rows are in, while
+    // panel p + 1 is copied in and panel p - 1 is copied out on the copy-out
+    // stream. Every panel is an ordinary device call on the staged copies.
+    cudaStream_t s = stream;
+    const int P = host_panels(h, M, N, K);
+    const int rows_per = ((M + P - 1) / P + 127) / 128 * 128;
+    const bool copy_c_in = beta != 0.0f;
+    bool ok = cudaEventRecord(h->ev_start, s) == cudaSuccess && cudaStreamWaitEvent(h->h2d, h->ev_start, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(h->d2h, h->ev_start, 0) == cudaSuccess;
+    if (ok && need_ab)
+        ok = cudaMemcpy2DAsync(dB, dldb * 4, B, static_cast<size_t>(ldb) * 4, static_cast<size_t>(N) * 4, K,
+                               cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+    ok = ok && cudaEventRecord(h->ev_b, h->h2d) == cudaSuccess && cudaStreamWaitEvent(s, h->ev_b, 0) == cudaSuccess;
+    int panels = 0;
+    bool c_changed = true;
+    for (int p = 0; ok && p < P; ++p) {
+        const int r0 = p * rows_per;
+        if (r0 >= M) break;
+        const int mp = (M - r0 < rows_per) ? (M - r0) : rows_per;
+        const float *hA = A + static_cast<long long>(r0) * lda;
+        float *hC = C + static_cast<long long>(r0) * ldc;
+        float *pA = dA + static_cast<long long>(r0) * dlda;
+        float *pC = dC + static_cast<long long>(r0) * dldc;
+        if (need_ab)
+            ok = cudaMemcpy2DAsync(pA, dlda * 4, hA, static_cast<size_t>(lda) * 4, static_cast<size_t>(K) * 4, mp,
+                                   cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+        if (ok && copy_c_in)
+            ok = cudaMemcpy2DAsync(pC, dldc * 4, hC, static_cast<size_t>(ldc) * 4, static_cast<size_t>(N) * 4, mp,
+                                   cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+        ok = ok && cudaEventRecord(h->ev_in[p], h->h2d) == cudaSuccess && cudaStreamWaitEvent(s, h->ev_in[p], 0) == cudaSuccess;
+        if (!ok) break;
+        rc = run_device(h, mp, N, K, alpha, need_ab ? pA : nullptr, static_cast<int>(dlda > 0 ? dlda : 1),
+                        need_ab ? dB : nullptr, static_cast<int>(dldb), beta, pC, static_cast<int>(dldc), s);
+        if (rc != SGEMM_OK) break;
+        c_changed = h->last.kernel != SGEMM_KERNEL_NONE;  // alpha == 0 / K == 0 with beta == 1: C unchanged
+        ok = cudaEventRecord(h->ev_done[p], s) == cudaSuccess && cudaStreamWaitEvent(h->d2h, h->ev_done[p], 0) == cudaSuccess;
+        if (ok && c_changed)
+            ok = cudaMemcpy2DAsync(hC, static_cast<size_t>(ldc) * 4, pC, dldc * 4, static_cast<size_t>(N) * 4, mp,
+                                   cudaMemcpyDeviceToHost, h->d2h) == cudaSuccess;
+        ++panels;
+    }
+    // Join the copy streams back into `stream` and wait: on success and on
+    // failure alike no copy into the caller's host buffers is left in flight.
+    const bool joined = cudaEventRecord(h->ev_end, h->d2h) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, h->ev_end, 0) == cudaSuccess;
+    const cudaError_t e1 = cudaStreamSynchronize(h->h2d);
+    const cudaError_t e2 = cudaStreamSynchronize(h->d2h);
+    const cudaError_t e3 = cudaStreamSynchronize(s);
+    if (rc != SGEMM_OK) return rc;
+    if (!ok || !joined || e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+        cudaGetLastError();
         return SGEMM_ERR_CUDA;
-    return cuda_status(cudaStreamSynchronize(s));
+    }
+    (void)panels;
+    return SGEMM_OK;
 }
 
 int sgemm_set_math_mode(sgemm_handle_t h, int mode)
