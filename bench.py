@@ -285,6 +285,26 @@ def measured_bf16_peak():
         return 1900.0, "fallback"
 
 
+def measure_min2(torch, sg, h, dA, dB, dC, M, N, K, alpha, beta, stream, ms_per_call, steps=20):
+    """Cost of also returning C's two smallest elements (sgemm_run_min2) over a plain call."""
+    C = dC.clone()
+    for _ in range(3):
+        h.run_min2(dA, dB, C, alpha, beta, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        h.run_min2(dA, dB, C, alpha, beta, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    extra = max(ms - ms_per_call, 1e-6)
+    return {"ms_per_call": ms, "extra_ms_over_sgemm_run": ms - ms_per_call,
+            "reduction_gbs": 4.0 * M * N / (extra * 1e-3) / 1e9,
+            "note": "two smallest elements of C with positions; the extra pass reads C once (HBM-bound)"}
+
+
 def measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, device, steps=50):
     """Time the flagged TF32 tensor-core mode on the same operands (outside the FP32 timed region)."""
     h = sg.Sgemm(device)
@@ -391,6 +411,7 @@ def run_ours(args, world):
     e2e_t = world.max(time.perf_counter() - t0)
     e2e_value = flops * e2e_steps * world.size / e2e_t / 1e12
 
+    min2 = measure_min2(torch, sg, h, dA, dB, dC, M, N, K, alpha, beta, stream, ms_per_call=elapsed / args.steps * 1e3)
     tf32 = (measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, world.local_rank, args.tf32_steps)
             if args.tf32_steps > 0 else None)
 
@@ -425,6 +446,7 @@ def run_ours(args, world):
         "gpu_launches": plan.launches * args.steps,
         "clocks": clocks,
         "tf32_mode": tf32,
+        "min2": min2,
     }
     if world.rank == 0 and world.size == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds, A, B, C)

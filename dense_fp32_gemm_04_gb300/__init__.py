@@ -79,6 +79,7 @@ _SIGNATURES = {
     "sgemm_config_info": ([_I, ctypes.POINTER(Plan)], _I),
     "sgemm_status_string": ([_I], ctypes.c_char_p),
     "sgemm_run_splitk_static": ([_I, _I, _I, _F, _P, _I, _P, _I, _F, _P, _I, _I, _P, _P], _I),
+    "sgemm_run_min2": ([_P, _I, _I, _I, _F, _P, _I, _P, _I, _F, _P, _I, _P, _P, _P], _I),
 }
 
 STATIC_SCRATCH_BYTES = 32 << 20
@@ -210,6 +211,24 @@ class Sgemm:
         _check(library().sgemm_run(self._h, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, self._stream(stream)),
                "sgemm_run")
         return C
+
+    def run_min2(self, A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+        """C = alpha * A @ B + beta * C in place, plus the two smallest elements of C.
+
+        Returns device tensors ``(vals[2], ij[4])`` = values and {row0, col0, row1, col1}.
+        """
+        import torch
+
+        M, K = A.shape
+        N = B.shape[1]
+        pa, lda = _matrix_arg(A, M, K, "A")
+        pb, ldb = _matrix_arg(B, K, N, "B")
+        pc, ldc = _matrix_arg(C, M, N, "C")
+        vals = torch.empty(2, dtype=torch.float32, device=C.device)
+        ij = torch.empty(4, dtype=torch.int32, device=C.device)
+        _check(library().sgemm_run_min2(self._h, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, vals.data_ptr(),
+                                        ij.data_ptr(), self._stream(stream)), "sgemm_run_min2")
+        return vals, ij
 
     def run_ptr(self, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
         """Direct C-ABI call with raw device pointers; returns the status (no exception)."""

@@ -38,6 +38,7 @@ struct sgemm_handle_s {
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_end = nullptr;
     cudaEvent_t ev_in[8] = {}, ev_done[8] = {};
+    void *min2_cand = nullptr;  // sgemm_run_min2 per-block candidates
 };
 
 namespace {
@@ -352,6 +353,7 @@ int sgemm_destroy(sgemm_handle_t h)
     cudaDeviceSynchronize();
     if (h->workspace) cudaFree(h->workspace);
     if (h->stage) cudaFree(h->stage);
+    if (h->min2_cand) cudaFree(h->min2_cand);
     if (h->h2d) cudaStreamDestroy(h->h2d);
     if (h->d2h) cudaStreamDestroy(h->d2h);
     for (cudaEvent_t e : {h->ev_start, h->ev_b, h->ev_end})
@@ -466,6 +468,27 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     }
     (void)panels;
     return SGEMM_OK;
+}
+
+int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                   int ldb, float beta, float *C, int ldc, float *min_vals, int *min_ij, struct CUstream_st *stream)
+{
+    const int v = check_args(h, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+    if (v != SGEMM_OK) return v;
+    if (min_vals == nullptr || min_ij == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    DeviceGuard g(h->device);
+    if (!g.ok) return SGEMM_ERR_CUDA;
+    int rc = run_device(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+    if (rc != SGEMM_OK) return rc;
+    const int blocks = 2 * h->num_sms;
+    if (h->min2_cand == nullptr && cudaMalloc(&h->min2_cand, min2_candidate_bytes(blocks)) != cudaSuccess) {
+        cudaGetLastError();
+        h->min2_cand = nullptr;
+        return SGEMM_ERR_ALLOC;
+    }
+    return launch_min2(C, ldc, M, N, h->min2_cand, blocks, min_vals, min_ij, stream) == cudaSuccess
+               ? SGEMM_OK
+               : SGEMM_ERR_LAUNCH;
 }
 
 int sgemm_set_math_mode(sgemm_handle_t h, int mode)

@@ -69,6 +69,9 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
                                  int vec_c, int num_sms, cudaStream_t stream);
 cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
+size_t min2_candidate_bytes(int blocks);
+cudaError_t launch_min2(const float *C, long long ldc, int M, int N, void *cand, int blocks, float *vals, int *ij,
+                        cudaStream_t stream);
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms,
                          cudaStream_t stream);
 cudaError_t tf32_set_attributes();

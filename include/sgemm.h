@@ -191,6 +191,24 @@ int sgemm_run_splitk_static(int M, int N, int K,
                             int splits, int *device_status,
                             struct CUstream_st *stream);
 
+/*
+ * sgemm_run, then the two smallest elements of the resulting C and their
+ * positions ("SGEMM CUDA kernel (First Half)", Additionally Required: the two
+ * minimums of the product C and their 2D indices, found in parallel).
+ * Elements are ordered by (value, row-major position i * N + j): equal values
+ * rank by position, so the answer is unique; NaN ranks as +infinity.
+ * min_vals: DEVICE array of 2 floats (smallest first). min_ij: DEVICE array of
+ * 4 ints {row0, col0, row1, col1}. Missing entries (M * N < 2) are +inf with
+ * row = col = -1. Asynchronous on `stream` like sgemm_run; same argument rules,
+ * plus min_vals and min_ij must be non-NULL.
+ */
+int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K,
+                   float alpha, const float *A, int lda,
+                   const float *B, int ldb,
+                   float beta, float *C, int ldc,
+                   float *min_vals, int *min_ij,
+                   struct CUstream_st *stream);
+
 /* Select SGEMM_MATH_FP32 (default) or SGEMM_MATH_TF32 for later runs. */
 int sgemm_set_math_mode(sgemm_handle_t h, int mode);
 int sgemm_get_math_mode(sgemm_handle_t h, int *mode);

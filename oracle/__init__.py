@@ -156,6 +156,33 @@ def sgemm_f32_ijk(*args, **kwargs):
     return _default().sgemm_f32_ijk(*args, **kwargs)
 
 
+def min2(values):
+    """The two smallest entries of a matrix and their (row, column).
+
+    The pages' follow-up task ("SGEMM CUDA kernel (First Half)", Additionally
+    Required: the two minimums of the product C and their 2D indices), taken as
+    a total order on (value, row-major position): equal values are ordered by
+    the smaller row-major index. Returns ``(vals, rows, cols)`` of length 2; a
+    matrix with one element reports (+inf, -1, -1) second.
+    """
+    v = np.asarray(values, dtype=np.float64)
+    M, N = v.shape
+    flat = v.reshape(-1)
+    order = np.lexsort((np.arange(flat.size), flat))  # by value, then position
+    vals, rows, cols = [], [], []
+    for t in range(2):
+        if t < flat.size:
+            e = int(order[t])
+            vals.append(float(flat[e]))
+            rows.append(e // N)
+            cols.append(e % N)
+        else:
+            vals.append(float("inf"))
+            rows.append(-1)
+            cols.append(-1)
+    return vals, rows, cols
+
+
 def bound(K: int, mag, u: float = U_FP32):
     """Elementwise error bound (K + 2) * u * mag."""
     return (K + 2) * u * mag

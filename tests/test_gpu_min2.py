@@ -1,0 +1,94 @@
+"""sgemm_run_min2: C and its two smallest elements with their (row, column).
+
+Integer operands: C is exact, so values and positions must equal the oracle's
+two minimums of the exact product (ties ranked by row-major position).
+Real operands: the reported pair must be the two smallest elements of the
+GPU's own C (the definition applied to that C) and lie within the FP32 bound of
+the oracle's values at those positions.
+"""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_04_gb300 as sg
+import oracle
+from dense_fp32_gemm_04_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_gemm_04_gb300 import _build
+
+    _build.build()
+    handle = sg.Sgemm(0)
+    yield handle
+    handle.close()
+
+
+def _run(h, A, B, C, alpha, beta):
+    dA, dB, dC = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (A, B, C))
+    vals, ij = h.run_min2(dA, dB, dC, alpha, beta)
+    torch.cuda.synchronize()
+    assert h.check_device_status() == (sg.SGEMM_OK, 0)
+    return dC.cpu().numpy(), vals.cpu().numpy(), ij.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 5), (1, 37, 9), (64, 64, 64), (300, 200, 100), (1000, 2500, 513),
+                                   (2047, 3001, 1531), (16384, 64, 512)])
+def test_integer_exact(h, shape):
+    M, N, K = shape
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=M + 3 * N, dist=("int", "int", "int"))
+    got, vals, ij = _run(h, A, B, C, 1.0, 1.0)
+    ref, _ = oracle.sgemm_f64(A, B, C, 1.0, 1.0, with_mag=False)
+    assert oracle.exact(got, ref)
+    rv, rr, rc = oracle.min2(ref)
+    assert list(vals.astype(np.float64)) == rv
+    assert list(ij) == [rr[0], rc[0], rr[1], rc[1]]
+
+
+@pytest.mark.parametrize("name", ["square256", "ragged", "skinny_wide"])
+def test_real(h, name):
+    p = inputs.PROBLEMS[name]
+    A, B, C = inputs.problem_operands(name)
+    got, vals, ij = _run(h, A, B, C, p["alpha"], p["beta"])
+    # the definition applied to the GPU's own C
+    gv, gr, gc = oracle.min2(got)
+    assert list(vals.astype(np.float64)) == gv and list(ij) == [gr[0], gc[0], gr[1], gc[1]]
+    # and those elements are within the FP32 bound of the exact product
+    rows = np.array([gr[0], gr[1]])
+    ref, mag = oracle.sgemm_f64(A, B, C, p["alpha"], p["beta"], rows=rows)
+    for t in range(2):
+        e = abs(float(vals[t]) - ref[t, gc[t]])
+        assert e <= oracle.bound(p["K"], mag[t, gc[t]])
+    # the true (FP64) minimum is within two bounds of the reported one
+    full, fmag = oracle.sgemm_f64(A, B, C, p["alpha"], p["beta"], with_mag=True)
+    tv, _, _ = oracle.min2(full)
+    assert abs(tv[0] - float(vals[0])) <= 2 * oracle.bound(p["K"], fmag.max())
+
+
+def test_empty_and_degenerate(h):
+    A = np.zeros((0, 4), np.float32)
+    B = np.ones((4, 3), np.float32)
+    C = np.zeros((0, 3), np.float32)
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
+    vals, ij = h.run_min2(dA, dB, dC, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert np.all(np.isinf(vals.cpu().numpy())) and list(ij.cpu().numpy()) == [-1, -1, -1, -1]
+    # a single element: second entry is +inf at (-1, -1)
+    A = np.full((1, 3), 2.0, np.float32)
+    B = np.full((3, 1), -1.0, np.float32)
+    got, vals, ij = _run(h, A, B, np.zeros((1, 1), np.float32), 1.0, 0.0)
+    assert vals[0] == -6.0 and np.isinf(vals[1]) and list(ij) == [0, 0, -1, -1]
+
+
+def test_deterministic_under_ties(h):
+    # all-equal product: every element ties, the first two positions win
+    A = np.ones((300, 17), np.float32)
+    B = np.ones((17, 500), np.float32)
+    got, vals, ij = _run(h, A, B, np.zeros((300, 500), np.float32), 1.0, 0.0)
+    assert list(vals) == [17.0, 17.0] and list(ij) == [0, 0, 0, 1]

@@ -73,3 +73,29 @@ def test_empty_shapes():
     C = inputs.matrix(1, 2, 4, 3, "uniform")
     out, mag = oracle.sgemm_f64(A, B, C, 1.0, 2.0)
     assert np.array_equal(out, 2.0 * C.astype(np.float64))
+
+
+def _min2_brute(v):
+    """Sort every (value, row-major position) pair: the definition, by brute force."""
+    M, N = v.shape
+    pairs = sorted((float(v[i, j]), i * N + j) for i in range(M) for j in range(N))
+    out = pairs[:2] + [(float("inf"), None)] * (2 - len(pairs[:2]))
+    vals = [p[0] for p in out]
+    rows = [p[1] // N if p[1] is not None else -1 for p in out]
+    cols = [p[1] % N if p[1] is not None else -1 for p in out]
+    return vals, rows, cols
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 7), (5, 1), (3, 4), (9, 13), (16, 16)])
+def test_min2_matches_brute_force(shape):
+    M, N = shape
+    for seed in range(5):
+        v = inputs.matrix(seed, 0, M, N, "int")  # many ties
+        assert oracle.min2(v) == _min2_brute(v)
+        w = inputs.matrix(seed, 1, M, N, "normal")
+        assert oracle.min2(w) == _min2_brute(w)
+
+
+def test_min2_ties_take_the_first_position():
+    v = np.array([[3.0, -1.0, 2.0], [-1.0, 0.0, -1.0]], dtype=np.float32)
+    assert oracle.min2(v) == ([-1.0, -1.0], [0, 1], [1, 0])
