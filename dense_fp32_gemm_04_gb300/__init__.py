@@ -80,6 +80,7 @@ _SIGNATURES = {
     "sgemm_status_string": ([_I], ctypes.c_char_p),
     "sgemm_run_splitk_static": ([_I, _I, _I, _F, _P, _I, _P, _I, _F, _P, _I, _I, _P, _P], _I),
     "sgemm_run_min2": ([_P, _I, _I, _I, _F, _P, _I, _P, _I, _F, _P, _I, _P, _P, _P], _I),
+    "sgemm_ladder_run": ([_I, _I, _I, _I, _F, _P, _P, _F, _P, _P], _I),
 }
 
 STATIC_SCRATCH_BYTES = 32 << 20
@@ -137,6 +138,21 @@ def run_splitk_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, splits, devi
     s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
     return library().sgemm_run_splitk_static(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, splits,
                                              device_status, s)
+
+
+def ladder_run(rung, A, B, C, alpha=1.0, beta=0.0, stream=None) -> int:
+    """One rung of the pages' kernel ladder (context kernels) on packed torch CUDA tensors; returns the status."""
+    import torch
+
+    M, K = A.shape
+    N = B.shape[1]
+    for t, r, c, name in ((A, M, K, "A"), (B, K, N, "B"), (C, M, N, "C")):
+        if not t.is_contiguous() or tuple(t.shape) != (r, c) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a packed {r} x {c} float32 CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return library().sgemm_ladder_run(rung, M, N, K, alpha, A.data_ptr(), B.data_ptr(), beta, C.data_ptr(), s)
 
 
 def configs():

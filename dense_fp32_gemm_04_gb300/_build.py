@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libsgemm_gb300.so")
 OBJ_DIR = os.path.join(ROOT, "_build", "obj")
 
-SOURCES = ["ffma_kernels.cu", "tf32_kernels.cu", "min2_kernels.cu", "planner.cpp", "sgemm_api.cpp", "static_scratch.cu"]
+SOURCES = ["ffma_kernels.cu", "tf32_kernels.cu", "min2_kernels.cu", "ladder_kernels.cu", "planner.cpp", "sgemm_api.cpp", "static_scratch.cu"]
 HEADERS = ["device_ptx.cuh", "sgemm_internal.h", "tile_table.h", "planner.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -37,8 +37,9 @@ def _flags(extra=()):
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "sgemm.h"),
-                                                                 os.path.abspath(__file__)]
+    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", h)
+                                                                 for h in ("sgemm.h", "sgemm_ladder.h")]
+    files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 
 

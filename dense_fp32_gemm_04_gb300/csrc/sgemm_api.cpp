@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/sgemm.h"
+#include "../../include/sgemm_ladder.h"
 #include "planner.h"
 #include "sgemm_internal.h"
 
@@ -489,6 +490,22 @@ int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     return launch_min2(C, ldc, M, N, h->min2_cand, blocks, min_vals, min_ij, stream) == cudaSuccess
                ? SGEMM_OK
                : SGEMM_ERR_LAUNCH;
+}
+
+int sgemm_ladder_run(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta, float *C,
+                     struct CUstream_st *stream)
+{
+    if (rung < 1 || rung > 7 || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return SGEMM_ERR_INVALID_VALUE;
+    if (M > (1 << 21)) return SGEMM_ERR_NOT_SUPPORTED;
+    if (rung >= 6 && (K % 4 != 0 || N % 4 != 0 || !aligned16(A) || !aligned16(B))) return SGEMM_ERR_NOT_SUPPORTED;
+    const cudaError_t e = launch_ladder(rung, M, N, K, alpha, A, B, beta, C, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
 }
 
 int sgemm_set_math_mode(sgemm_handle_t h, int mode)

@@ -69,6 +69,8 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
                                  int vec_c, int num_sms, cudaStream_t stream);
 cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
+cudaError_t launch_ladder(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta,
+                          float *C, cudaStream_t stream);
 size_t min2_candidate_bytes(int blocks);
 cudaError_t launch_min2(const float *C, long long ldc, int M, int N, void *cand, int blocks, float *vals, int *ij,
                         cudaStream_t stream);
