@@ -123,3 +123,48 @@ def test_config_table(lib):
     for r in rows:
         assert r.bm % 32 == 0 and r.bn % 64 == 0 and r.bk == 32
         assert r.threads == ((r.bm // 32) * (r.bn // 64) + 1) * 32  # warp tiles + the TMA producer warp
+
+
+def test_plan_invariants_random_shapes(lib):
+    """Host planner invariants over many seeded random problems and SM counts."""
+    import numpy as np
+
+    rng = np.random.default_rng(1234)
+    for _ in range(400):
+        M, N, K = (int(x) for x in rng.integers(1, 20000, 3))
+        if rng.random() < 0.3:
+            M = int(rng.integers(1, 300))
+        if rng.random() < 0.3:
+            N = int(rng.integers(1, 300))
+        sms = int(rng.choice([1, 8, 132, 148, 152, 160]))
+        lda, ldb, ldc = K + int(rng.integers(0, 5)), N + int(rng.integers(0, 5)), N + int(rng.integers(0, 5))
+        align = int(rng.integers(0, 8))
+        p = sg.plan(M, N, K, lda=lda, ldb=ldb, ldc=ldc, align_flags=align, num_sms=sms)
+        assert p.kernel == sg.KERNEL_FFMA
+        tiles = p.tiles_m * p.tiles_n
+        assert p.tiles_m == -(-M // p.bm) and p.tiles_n == -(-N // p.bn)
+        kb = -(-K // 32)
+        assert 1 <= p.splits <= min(kb, 16)
+        slots = sms * p.ctas_per_sm
+        if p.tail_splits > 1:
+            assert p.splits == 1 and 0 < p.tail_tiles < slots
+            assert (tiles - p.tail_tiles) % slots == 0
+            assert p.units == tiles - p.tail_tiles + p.tail_tiles * p.tail_splits
+            assert p.workspace_bytes >= p.tail_tiles * p.tail_splits * p.bm * p.bn * 4
+        else:
+            assert p.tail_tiles == 0 and p.units == tiles * p.splits
+            if p.splits > 1:
+                assert p.workspace_bytes >= p.splits * M * (-(-N // 4) * 4) * 4
+        assert 1 <= p.grid <= min(p.units, slots)
+        assert p.repack_a == (0 if (align & 1 and lda % 4 == 0) else 1)
+        assert p.repack_b == (0 if (align & 2 and ldb % 4 == 0) else 1)
+        assert p.vec_c == (1 if (align & 4 and ldc % 4 == 0) else 0)
+        extra = 1 if (p.splits > 1 or p.tail_splits > 1) else 0
+        assert p.launches == 1 + p.repack_a + p.repack_b + extra
+
+
+def test_tf32_plan(lib):
+    p = sg.plan(4096, 4096, 4096, math_mode=sg.MATH_TF32)
+    assert p.kernel == sg.KERNEL_TF32 and (p.bm, p.bn, p.bk) == (128, 256, 32)
+    assert p.repack_b == 1 and p.launches == 2 and p.units == 32 * 16 and p.grid == 152
+    assert p.workspace_bytes >= 4096 * 4096 * 4  # B transposed to K-major
