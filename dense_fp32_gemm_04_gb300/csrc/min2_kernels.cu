@@ -6,12 +6,14 @@
 // Order: (value, row-major position i * N + j), so equal values rank by
 // position and the answer is unique; NaN ranks as +infinity. Pass 1: every
 // block keeps a running top-2 over rows of C (grid-stride over rows, threads
-// stride over columns, coalesced), merges it across the warp with shuffles and
-// across warps in shared memory, and writes one candidate pair. Pass 2: one
-// block merges all candidate pairs. The result does not depend on scheduling.
+// stride over columns, coalesced, with 16-byte loads when C allows), merges it
+// across the warp with shuffles and across warps in shared memory, and writes
+// one candidate pair. Pass 2: one block merges all candidate pairs. The result
+// does not depend on scheduling.
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstdint>
 
 #include "sgemm_internal.h"
 
@@ -79,6 +81,7 @@ __device__ Top2 block_reduce(Top2 t)
     return t;
 }
 
+template <bool VEC>
 __global__ void __launch_bounds__(kThreads) min2_pass1(const float *__restrict__ C, long long ldc, int M, int N,
                                                        Top2 *__restrict__ cand)
 {
@@ -86,7 +89,20 @@ __global__ void __launch_bounds__(kThreads) min2_pass1(const float *__restrict__
     for (int row = blockIdx.x; row < M; row += gridDim.x) {
         const float *crow = C + static_cast<long long>(row) * ldc;
         const long long base = static_cast<long long>(row) * N;
-        for (int col = threadIdx.x; col < N; col += kThreads) push(t, crow[col], base + col);
+        if (VEC) {
+            // 16-byte loads of 4 consecutive columns (C 16-byte aligned, ldc % 4 == 0)
+            const int n4 = N & ~3;
+            for (int col = 4 * threadIdx.x; col < n4; col += 4 * kThreads) {
+                const float4 v = *reinterpret_cast<const float4 *>(crow + col);
+                push(t, v.x, base + col);
+                push(t, v.y, base + col + 1);
+                push(t, v.z, base + col + 2);
+                push(t, v.w, base + col + 3);
+            }
+            for (int col = n4 + threadIdx.x; col < N; col += kThreads) push(t, crow[col], base + col);
+        } else {
+            for (int col = threadIdx.x; col < N; col += kThreads) push(t, crow[col], base + col);
+        }
     }
     t = block_reduce(t);
     if (threadIdx.x == 0) cand[blockIdx.x] = t;
@@ -116,7 +132,11 @@ cudaError_t launch_min2(const float *C, long long ldc, int M, int N, void *cand,
                         cudaStream_t stream)
 {
     const int g = M < blocks ? (M > 0 ? M : 1) : blocks;
-    min2_pass1<<<g, kThreads, 0, stream>>>(C, ldc, M, N, static_cast<Top2 *>(cand));
+    const bool vec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0;
+    if (vec)
+        min2_pass1<true><<<g, kThreads, 0, stream>>>(C, ldc, M, N, static_cast<Top2 *>(cand));
+    else
+        min2_pass1<false><<<g, kThreads, 0, stream>>>(C, ldc, M, N, static_cast<Top2 *>(cand));
     min2_pass2<<<1, kThreads, 0, stream>>>(static_cast<const Top2 *>(cand), g, N, vals, ij);
     return cudaGetLastError();
 }

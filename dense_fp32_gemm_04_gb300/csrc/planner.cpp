@@ -150,7 +150,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     out->vec_c = ((q.align_flags & 4) && q.ldc % 4 == 0) ? 1 : 0;
     if (q.math_mode == SGEMM_MATH_TF32) {
         // B always goes through the workspace: transposed to K-major (N x roundup(K, 4)).
-        if (q.K > 65535LL * 32) return SGEMM_ERR_NOT_SUPPORTED;
+        if (q.K > 65535LL * 64) return SGEMM_ERR_NOT_SUPPORTED;
         out->kernel = SGEMM_KERNEL_TF32;
         out->bm = sgemm_cfg::kTf32BM;
         out->bn = sgemm_cfg::kTf32BN;

@@ -481,7 +481,7 @@ int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     if (!g.ok) return SGEMM_ERR_CUDA;
     int rc = run_device(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
     if (rc != SGEMM_OK) return rc;
-    const int blocks = 2 * h->num_sms;
+    const int blocks = 8 * h->num_sms;
     if (h->min2_cand == nullptr && cudaMalloc(&h->min2_cand, min2_candidate_bytes(blocks)) != cudaSuccess) {
         cudaGetLastError();
         h->min2_cand = nullptr;
