@@ -247,3 +247,30 @@ def test_run_host_pipelined_panels(h):
     pinned = [torch.from_numpy(x).pin_memory() for x in (A, B, C)]
     h.run_host(pinned[0], pinned[1], pinned[2], 1.5, 0.5)
     check_against_oracle(pinned[2].numpy(), A, B, C, 1.5, 0.5, exact=True)
+
+
+def test_offsets_beyond_2_31_elements(h):
+    """C with 2.6e9 elements (row offsets past 2^31): the tail rows are still exact.
+
+    Integer A and B, beta = 0 (C never read, allocated uninitialised on the device).
+    Every output below row 53687 has an offset under 2^31; the checked rows are the
+    first ones and rows far past that point.
+    """
+    M, N, K = 65536, 40000, 64
+    free, _ = torch.cuda.mem_get_info()
+    if free < 16 * 2**30:
+        pytest.skip("needs 16 GiB of free device memory")
+    A = inputs.matrix(51, 0, M, K, "int")
+    B = inputs.matrix(51, 1, K, N, "int")
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    h.run(dA, dB, dC, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert h.check_device_status() == (sg.SGEMM_OK, 0)
+    rows = np.array([0, 1, 53686, 53687, 53688, 60000, M - 2, M - 1])
+    got = dC[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref, _ = oracle.sgemm_f64(A, B, None, 1.0, 0.0, rows=rows, with_mag=False)
+    assert oracle.exact(got, ref)
+    del dC
+    torch.cuda.empty_cache()
