@@ -38,6 +38,7 @@ OPT_FORCE_SPLITS = 2
 OPT_WAIT_TIMEOUT_NS = 3
 OPT_INJECT_SKIP = 4
 OPT_LOG = 5
+OPT_SKEW_NS = 6
 
 
 class Plan(ctypes.Structure):

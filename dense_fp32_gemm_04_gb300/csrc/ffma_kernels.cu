@@ -134,6 +134,7 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
                 ok = false;
                 break;
             }
+            if (p.skew_ns > 0) __nanosleep(static_cast<unsigned>(p.skew_ns));
             const bool skip = (p.inject_skip >= 0 && blockIdx.x == 0 && seq == p.inject_skip);
             if (!skip) {
                 mbar_arrive_expect_tx(full, T::STAGE_BYTES);
@@ -355,6 +356,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 return;
             }
             compute_slab<T>(a_rows_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), r, acc);
+            if (p.skew_ns < 0) __nanosleep(static_cast<unsigned>(-p.skew_ns));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_base + 8 * (T::STAGES + stage));
             if (++stage == T::STAGES) {

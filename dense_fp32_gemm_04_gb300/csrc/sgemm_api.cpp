@@ -31,6 +31,7 @@ struct sgemm_handle_s {
     size_t stage_bytes = 0;
     Overrides ov;
     int inject_skip = -1;
+    int skew_ns = 0;
     int log = 0;
     long long timeout_ns = 4000000000LL;
     sgemm_plan_t last{};
@@ -265,6 +266,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
     p.inject_skip = h->inject_skip;
+    p.skew_ns = h->skew_ns;
     if (plan.tail_splits > 1) {
         p.W = reinterpret_cast<float *>(ws + w.w_off);
         p.n_full = plan.tiles_m * plan.tiles_n - plan.tail_tiles;
@@ -343,6 +345,15 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
     }
     const char *env = std::getenv("SGEMM_LOG");
     h->log = (env != nullptr && env[0] == '1') ? 1 : 0;
+    // Tuning overrides for the planner (same ranges as sgemm_set_option).
+    if (const char *fc = std::getenv("SGEMM_FORCE_CONFIG")) {
+        const long v = std::strtol(fc, nullptr, 10);
+        if (v >= -1 && v < sgemm_cfg::kNumFfmaConfigs) h->ov.force_config = static_cast<int>(v);
+    }
+    if (const char *fs = std::getenv("SGEMM_FORCE_SPLITS")) {
+        const long v = std::strtol(fs, nullptr, 10);
+        if (v >= 0 && v <= kMaxSplits) h->ov.force_splits = static_cast<int>(v);
+    }
     *out = h;
     return SGEMM_OK;
 }
@@ -544,6 +555,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
         return SGEMM_OK;
     case SGEMM_OPT_LOG:
         h->log = value ? 1 : 0;
+        return SGEMM_OK;
+    case SGEMM_OPT_SKEW_NS:
+        if (value < -100000 || value > 100000) return SGEMM_ERR_INVALID_VALUE;
+        h->skew_ns = static_cast<int>(value);
         return SGEMM_OK;
     default:
         return SGEMM_ERR_INVALID_VALUE;

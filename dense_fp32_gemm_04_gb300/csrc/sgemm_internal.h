@@ -43,6 +43,9 @@ struct FfmaParams {
     // W + ((tile - n_full) * tail_splits + slice) * BM * BN. `splits` is then 1.
     int n_full;
     int tail_splits;
+    // Test only (race detection): > 0 delays the producer by this many ns before
+    // every fill, < 0 delays every consumer warp before it releases a slab.
+    int skew_ns;
 };
 
 // Everything the TF32 tcgen05 mainloop needs besides the two tensor maps

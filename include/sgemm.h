@@ -102,7 +102,10 @@ typedef enum sgemm_option {
     SGEMM_OPT_INJECT_SKIP = 4,    /* TEST ONLY: CTA 0 never issues the copy of its n-th k-slab
                                      (-1 = off, the default); the consumers' wait then runs out
                                      and the run reports SGEMM_ERR_TIMEOUT without faulting */
-    SGEMM_OPT_LOG = 5             /* 1: print the chosen plan of each call to stderr */
+    SGEMM_OPT_LOG = 5,            /* 1: print the chosen plan of each call to stderr */
+    SGEMM_OPT_SKEW_NS = 6         /* TEST ONLY (race detection): > 0 delays the FP32 kernel's copy
+                                     issue by this many ns per k-slab, < 0 delays every compute warp
+                                     before it releases a slab; |value| <= 100000, 0 = off */
 } sgemm_option_t;
 
 /*
@@ -113,6 +116,8 @@ typedef enum sgemm_option {
  * The handle owns a lazily grown device workspace (split-K partials and
  * aligned operand copies) and, for sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
+ * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
+ * SGEMM_FORCE_SPLITS=<S> preset the planner overrides of sgemm_set_option.
  */
 int sgemm_create(sgemm_handle_t *out);
 

@@ -274,3 +274,29 @@ def test_offsets_beyond_2_31_elements(h):
     assert oracle.exact(got, ref)
     del dC
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("skew", [3000, -3000])
+def test_timing_skew_is_race_free(h, skew):
+    """A slow producer (skew > 0) or slow consumers (skew < 0) change only timing:
+    results stay bitwise identical (a race on the shared-memory ring would show here)."""
+    cases = [((1999, 3001, 1031), dict()), ((700, 900, 1500), dict(config=1, splits=3)),
+             ((300, 260, 777), dict(config=3, splits=1))]
+    for (M, N, K), force in cases:
+        A, B, C = ops(M, N, K, seed=M + skew, dist=("normal", "uniform", "uniform"))
+        if force:
+            h.set_option(sg.OPT_FORCE_CONFIG, force["config"])
+            h.set_option(sg.OPT_FORCE_SPLITS, force["splits"])
+        try:
+            ref_run, _, st = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+            assert st == sg.SGEMM_OK
+            h.set_option(sg.OPT_SKEW_NS, skew)
+            skewed, guards, st = run_gemm(torch, h, A, B, C, 1.0, 1.0)
+            assert st == sg.SGEMM_OK and guards
+            assert h.check_device_status() == (sg.SGEMM_OK, 0)
+        finally:
+            h.set_option(sg.OPT_SKEW_NS, 0)
+            h.set_option(sg.OPT_FORCE_CONFIG, -1)
+            h.set_option(sg.OPT_FORCE_SPLITS, 0)
+        assert np.array_equal(ref_run.view(np.uint32), skewed.view(np.uint32)), (M, N, K, skew)
+        check_against_oracle(skewed, A, B, C, 1.0, 1.0)
