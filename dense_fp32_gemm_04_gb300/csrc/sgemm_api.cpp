@@ -3,8 +3,6 @@
 // and status reporting. Declarations and contracts: include/sgemm.h.
 #include <cstdio>
 #include <cstdlib>
-#include <cstring>
-#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
