@@ -3,6 +3,7 @@
 // and status reporting. Declarations and contracts: include/sgemm.h.
 #include <cstdio>
 #include <cstdlib>
+#include <new>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
