@@ -45,6 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--tf32-steps", type=int, default=50, help="calls timed in the flagged TF32 mode (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the other configured problem sizes")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
 
@@ -204,8 +205,8 @@ def problem(name):
     return p
 
 
-def cpu_oracle_sample(name, seconds, A=None, B=None, C=None):
-    """Time the FP64 oracle on rows of the workload for about ``seconds`` (all host threads)."""
+def cpu_oracle_sample(name, seconds, A=None, B=None, C=None, nthreads=0):
+    """Time the FP64 oracle on rows of the workload for about ``seconds`` (``nthreads`` 0: all host threads)."""
     import numpy as np
 
     import oracle
@@ -215,22 +216,48 @@ def cpu_oracle_sample(name, seconds, A=None, B=None, C=None):
     if A is None:
         A, B, C = inputs.problem_operands(name)
     M, N, K = p["M"], p["N"], p["K"]
-    threads = oracle.max_threads()
-    rows_done, elapsed, r = 0, 0.0, 4
-    while elapsed < seconds and rows_done < M:
-        rows = np.arange(rows_done, min(M, rows_done + r))
+    threads = nthreads or oracle.max_threads()
+    rows_done, elapsed, r, lo = 0, 0.0, 1, 0
+    while elapsed < seconds:
+        rows = np.arange(lo, min(M, lo + r))
         t = time.perf_counter()
-        oracle.sgemm_f64(A, B, C, p["alpha"], p["beta"], rows=rows, with_mag=False)
+        oracle.sgemm_f64(A, B, C, p["alpha"], p["beta"], rows=rows, with_mag=False, nthreads=nthreads)
         dt = time.perf_counter() - t
         elapsed += dt
         rows_done += len(rows)
+        lo = (lo + len(rows)) % M  # small problems are repeated until the budget is spent
         # grow the batch toward the remaining budget
         per_row = dt / len(rows)
-        r = max(1, min(M - rows_done, int((seconds - elapsed) / max(per_row, 1e-9)) + 1, 4 * r))
+        r = max(1, min(M, int((seconds - elapsed) / max(per_row, 1e-9)) + 1, 4 * r))
     flops = 2.0 * rows_done * N * K
     return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows_done} of {M} rows of C for M=N=K={K} ({rows_done}x{N}x{K} MACs, FP64 accumulate, "
-                      f"i-k-j loop, {threads} threads), {elapsed:.1f} s"}
+            "sample": f"{rows_done} rows (C has {M}) for {shape_text(M, N, K)} ({rows_done}x{N}x{K} MACs, FP64 "
+                      f"accumulate, i-k-j loop, {threads} threads), {elapsed:.1f} s"}
+
+
+def cpu_oracle_configs(seconds_each, C2=None):
+    """The oracle's GFLOP/s at 1 thread and at all host threads on the 256^3, 4096^3, ragged and skinny problems."""
+    import oracle
+
+    out = []
+    for name in ("square256", "square4096", "ragged", "skinny_tall"):
+        ops = C2 if (name == "square4096" and C2 is not None) else (None, None, None)
+        for nt in (1, oracle.max_threads()):
+            d = cpu_oracle_sample(name, seconds_each, *ops, nthreads=nt)
+            out.append({"problem": name, "threads": nt, "gflops": d["value"] * 1e3, "sample": d["sample"]})
+    return out
+
+
+def workload_text(p):
+    dist = {"uniform": "uniform[-1,1)", "normal": "N(0,1)", "int": "int{-2..2}", "zero": "0"}
+    da, db, dc = (dist[d] for d in p["dist"])
+    ops = f"A,B,C {da}" if da == db == dc else f"A {da}, B {db}, C {dc}"
+    return (f"sgemm {shape_text(p['M'], p['N'], p['K'])} alpha={p['alpha']} beta={p['beta']} {ops} "
+            f"seed {p['seed']}")
+
+
+def shape_text(M, N, K):
+    return f"M=N=K={K}" if M == N == K else f"M={M} N={N} K={K}"
 
 
 # ---------------------------------------------------------------- reference arm
@@ -266,7 +293,7 @@ def run_reference(args, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"sgemm M=N=K={K} alpha={p['alpha']} beta={p['beta']} uniform[-1,1) seed {p['seed']}",
+        "config": {"workload": workload_text(p),
                    "step": f"{rows_per_step} rows of C per step (bounded sample of the workload)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} of {M} rows of C per step, FP64 i-k-j oracle, {threads} threads"},
@@ -333,6 +360,87 @@ def measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, device, st
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "peak_basis": f"{basis} bf16 {bf16} TFLOP/s x 1.1/2.25 (nominal tf32:bf16 dense ratio)"}}
+
+
+CONFIG_PROBLEMS = ["square256", "sweep512", "sweep1024", "sweep2048", "sweep8192", "sweep16384", "ragged",
+                   "skinny_tall", "skinny_wide"]
+
+
+def measure_configs(torch, sg, h, dev, stream, hbm_gbs, min_seconds=1.0):
+    """TFLOP/s, % of the FFMA peak and algorithmic HBM GB/s of every other configured problem.
+
+    Seeded operands of each problem; 5 warm-up calls, then at least 20 timed calls and at
+    least ``min_seconds`` of them; L2 is flushed (a 256 MiB write) before every timed call
+    and only the call itself sits between its CUDA events (median and min reported).
+    Outside the headline timed region.
+    """
+    from dense_fp32_gemm_04_gb300 import inputs
+
+    flush = torch.empty(64 * 2**20, dtype=torch.float32, device=dev)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "")) or None
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or "0"))
+    rows = []
+    sampler.start()
+    t0 = time.time()
+    for name in CONFIG_PROBLEMS:
+        q = inputs.PROBLEMS[name]
+        M, N, K, alpha, beta = q["M"], q["N"], q["K"], q["alpha"], q["beta"]
+        A, B, C = inputs.problem_operands(name)
+        dA, dB, dC = (torch.from_numpy(x).to(dev) for x in (A, B, C))
+        del A, B, C
+        flops = gemm_flops(M, N, K)
+        for _ in range(5):
+            h.run(dA, dB, dC, alpha, beta, stream=stream)
+        times = []
+        while len(times) < 20 or sum(times) < min_seconds * 1e3:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+            for e0, e1 in ev:
+                flush.fill_(1.0)
+                e0.record(stream)
+                h.run(dA, dB, dC, alpha, beta, stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            times += [e0.elapsed_time(e1) for e0, e1 in ev]
+        st, _ = h.check_device_status()
+        plan = h.last_plan()
+        ms = statistics.median(times)
+        bytes_alg = 4.0 * (M * K + K * N + M * N * (2 if beta != 0 else 1))
+        rows.append({"problem": name, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta, "calls": len(times),
+                     "ms_median": ms, "ms_min": min(times), "tflops": flops / (ms * 1e-3) / 1e12,
+                     "tflops_best": flops / (min(times) * 1e-3) / 1e12, "hbm_gbs": bytes_alg / (ms * 1e-3) / 1e9,
+                     "flop_per_byte": flops / bytes_alg, "status": st,
+                     "plan": {"config": plan.config, "splits": plan.splits, "tail_tiles": plan.tail_tiles,
+                              "tail_splits": plan.tail_splits, "launches": plan.launches}})
+        del dA, dB, dC
+    t1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    sm_mhz = clocks["sm_mhz"] if clocks else None
+    peak = nsm * 256 * sm_mhz * 1e-6 if sm_mhz else None
+    ridge = (peak * 1e3 / hbm_gbs) if (peak and hbm_gbs) else None
+    peak_max = nsm * 256 * clocks["sm_max_mhz"] * 1e-6 if clocks else None
+    for r in rows:
+        r["pct_ffma_peak"] = 100.0 * r["tflops"] / peak if peak else None
+        r["pct_ffma_peak_at_max_clock"] = 100.0 * r["tflops"] / peak_max if peak_max else None
+        r["pct_hbm"] = 100.0 * r["hbm_gbs"] / hbm_gbs if hbm_gbs else None
+        r["bound"] = ("alu" if r["flop_per_byte"] >= ridge else "hbm") if ridge else None
+    del flush
+    torch.cuda.empty_cache()
+    return {"problems": rows, "clocks": clocks, "ffma_peak_tflops": peak, "ffma_peak_tflops_at_max_clock": peak_max,
+            "hbm_peak_gbs": hbm_gbs,
+            "ridge_flop_per_byte": ridge,
+            "note": "per-call CUDA events, L2 flushed before each call, rates from the median call; peak at the "
+                    "median SM clock sampled here; hbm_gbs = algorithmic bytes (A, B, C written, C read when "
+                    "beta != 0) / time"}
+
+
+def measured_hbm_gbs():
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+    except (OSError, KeyError, ValueError):
+        return 6800.0
 
 
 # ---------------------------------------------------------------- our arm
@@ -412,6 +520,8 @@ def run_ours(args, world):
     e2e_value = flops * e2e_steps * world.size / e2e_t / 1e12
 
     min2 = measure_min2(torch, sg, h, dA, dB, dC, M, N, K, alpha, beta, stream, ms_per_call=elapsed / args.steps * 1e3)
+    configs = (measure_configs(torch, sg, h, dev, stream, measured_hbm_gbs())
+               if world.size == 1 and not args.no_configs else None)
     tf32 = (measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, world.local_rank, args.tf32_steps)
             if args.tf32_steps > 0 else None)
 
@@ -434,7 +544,7 @@ def run_ours(args, world):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world.size, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"sgemm M=N=K={K} alpha={alpha} beta={beta} A,B,C uniform[-1,1) seed {p['seed']}",
+        "config": {"workload": workload_text(p),
                    "M": M, "N": N, "K": K, "layout": "row-major",
                    "l2": f"no flush: operands {operand_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB",
                    "parallelism": f"replicas x{world.size}", "plan": plan.as_dict(),
@@ -447,9 +557,13 @@ def run_ours(args, world):
         "clocks": clocks,
         "tf32_mode": tf32,
         "min2": min2,
+        "configs": configs,
     }
     if world.rank == 0 and world.size == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds, A, B, C)
+        if not args.no_configs:
+            line["cpu_baseline"]["configs"] = cpu_oracle_configs(min(2.0, args.cpu_seconds / 4),
+                                                                 (A, B, C) if args.workload == "square4096" else None)
     if world.rank == 0:
         print(json.dumps(line), flush=True)
     h.close()

@@ -43,10 +43,8 @@ struct sgemm_handle_s {
 };
 
 namespace {
-constexpr int kMaxHostPanels = 8;
-}
 
-namespace {
+constexpr int kMaxHostPanels = 8;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

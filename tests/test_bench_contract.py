@@ -48,3 +48,9 @@ def test_our_arm_line():
     assert d["gpu_launches"] == d["config"]["plan"]["launches"] * 20
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["tf32_mode"]["status"] == 0 and d["tf32_mode"]["roofline"]["bound"] == "tensor"
+    probs = d["configs"]["problems"]
+    assert [r["problem"] for r in probs] == ["square256", "sweep512", "sweep1024", "sweep2048", "sweep8192",
+                                             "sweep16384", "ragged", "skinny_tall", "skinny_wide"]
+    for r in probs:
+        assert r["status"] == 0 and r["calls"] >= 20 and r["tflops"] > 0 and r["bound"] == "alu"
+    assert {c["problem"] for c in d["cpu_baseline"]["configs"]} == {"square256", "square4096", "ragged", "skinny_tall"}
