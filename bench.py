@@ -533,9 +533,11 @@ def run_ours(args, world):
     peak = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if peak else None, "traffic": recorded_traffic(),
-                "kernel": ("ffma_sgemm_kernel (plan config %d, %dx%d tile)" % (plan.config, plan.bm, plan.bn)) +
-                          (" + tail_reduce_kernel (timed together per call: a lower bound for the mainloop)"
-                           if plan.tail_splits > 1 else ""),
+                "kernel": ("ffma_sgemm_kernel (plan config %d, %dx%d tile, A %s)" %
+                           (plan.config, plan.bm, plan.bn, "transposed first" if plan.transpose_a else "as given")) +
+                          (" + transpose_kernel (A^T)" if plan.transpose_a else "") +
+                          (" + tail_reduce_kernel" if plan.tail_splits > 1 else "") +
+                          (" (timed together per call: a lower bound for the mainloop)" if plan.launches > 1 else ""),
                 "peak_basis": f"{nsm} SMs x 128 FP32 FMA/clk x 2 FLOP x median SM clock under load "
                               f"({sm_mhz} MHz, nvidia-smi during the timed region)",
                 "frac_at_max_clock": (achieved / (nsm * 256 * clocks["sm_max_mhz"] * 1e-6)) if clocks else None}

@@ -17,24 +17,37 @@
 //    zero-filled by the copy engine, which is the pages' zero-fill
 //    predication ("SGEMM CUDA kernel (First Half)", Part 5 load_ast) done in
 //    hardware.
-//  * Bank conflicts: the pages transpose A in shared memory so a thread's TM
-//    values of A are contiguous (same page, Part 5). Here A stays K-major as
-//    the copy engine writes it, and a thread instead takes its 8 rows 4 apart
-//    (rows r, r+4, ..., r+28 of its warp tile) and reads 4 consecutive k of
-//    one row per 128-bit load. The four row groups of a warp then read four
-//    consecutive rows, which the 128-byte swizzle places in four distinct
-//    bank quads: every 128-bit shared load is conflict-free without a
-//    transposing copy.
+//  * A layout and bank conflicts: the pages transpose A in shared memory so a
+//    thread's TM values of A are contiguous (same page, Part 5). Here the
+//    transposition happens once per call, in global memory: transpose_kernel
+//    writes A^T (K x M, M contiguous) into the handle's workspace and the copy
+//    engine stages As[k][m] slabs of it exactly like B. A thread owns rows
+//    4r..4r+3 and 16+4r..16+4r+3 of its warp tile and columns 4c..4c+3 and
+//    32+4c..32+4c+3; per k it reads two 128-bit words of A and two of B.
+//    The 8 lanes sharing r read the same A word (a broadcast) and the 8 lanes
+//    sharing c read 8 consecutive B words, so every 128-bit shared load is
+//    conflict-free. When transposing A costs more than it saves (N small
+//    against M * K), A stays K-major as the caller gave it: a thread then
+//    takes rows r, r+4, ..., r+28 and reads 4 consecutive k of one row per
+//    128-bit load, and the 128-byte swizzle of the A slab puts the four row
+//    groups of a warp in four distinct bank quads.
 //  * Arithmetic: packed FFMA2 (two FP32 fused multiply-adds per instruction,
 //    round-to-nearest-even, sm_100+) halves the issue slots the 64 FMAs of a
-//    k-step need, leaving room for the loads. Each output is still one chain
-//    of IEEE FP32 FMAs in ascending k.
+//    k-step need. With A^T the packed operand is a pair of A values along M
+//    and the B value is broadcast, (a_m, a_m+1) * (b_n, b_n); the FMA pipe
+//    sustains about 10 % more of this form than of (a_m, a_m) * (b_n, b_n+1),
+//    which the K-major layout has to use because its two A values of a pair
+//    would sit in different 128-bit loads. Either way each output is one chain
+//    of IEEE FP32 FMAs in ascending k, so both layouts give identical bits.
 //  * Persistent grid: CTAs loop over (tile, split) work units in a grouped
 //    order; the producer keeps prefetching across unit boundaries.
 //  * Watchdog: every mbarrier wait is bounded; on expiry the CTA records
 //    SGEMM_ERR_TIMEOUT in the status word, waits (bounded) for its own copies
 //    in flight and returns — it never traps or spins forever.
 #include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
 
 #include "device_ptx.cuh"
 #include "sgemm_internal.h"
@@ -109,7 +122,7 @@ __device__ __forceinline__ int split_begin(const FfmaParams &p, int ks, int nspl
     return static_cast<int>((static_cast<long long>(ks) * p.kblocks) / nsplit);
 }
 
-template <class T>
+template <class T, bool AT>
 __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                               const FfmaParams &p, uint32_t a_base, uint32_t b_base,
                                               uint32_t bar_base, volatile int *abort_flag)
@@ -138,7 +151,10 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
             const bool skip = (p.inject_skip >= 0 && blockIdx.x == 0 && seq == p.inject_skip);
             if (!skip) {
                 mbar_arrive_expect_tx(full, T::STAGE_BYTES);
-                tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, kb * T::BK, tm * T::BM);
+                if (AT)  // A^T slab: BK rows of k, BM consecutive m
+                    tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, tm * T::BM, kb * T::BK);
+                else  // A slab: BM rows of m, BK consecutive k (128-byte swizzle)
+                    tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, kb * T::BK, tm * T::BM);
                 tma_load_2d(b_base + stage * T::B_BYTES, tmB, full, tn * T::BN, kb * T::BK);
                 issued |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -159,11 +175,70 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
     }
 }
 
-// One BK = 32 slab: 8 chunks of 4 k. Per chunk a thread loads its 8 rows of A
-// (one 128-bit load each: 4 consecutive k) and 4 x 2 128-bit loads of B, then
-// issues 4 * 8 * 4 = 128 FFMA2 (256 FMAs).
+// Register accumulator of a thread's 8 x 8 outputs as 32 FFMA2 pairs: with A^T,
+// acc[ip][j] = rows (2ip, 2ip+1) of column j; with K-major A, acc[i][jp] =
+// row i, columns (2jp, 2jp+1).
+template <bool AT>
+using Acc = std::conditional_t<AT, float2[4][8], float2[8][4]>;
+
+// Local row (within the warp tile) of a thread's output row i = 0..7.
+template <bool AT>
+__device__ __forceinline__ int out_row(int r, int i)
+{
+    return AT ? 4 * r + (i & 3) + 16 * (i >> 2) : r + 4 * i;
+}
+
+// Outputs of row i, columns 4c..4c+3 (h = 0) or 32+4c..32+4c+3 (h = 1).
+__device__ __forceinline__ float4 out4(const float2 (&acc)[4][8], int i, int h)
+{
+    const int ip = i >> 1;
+    if (i & 1) return make_float4(acc[ip][4 * h].y, acc[ip][4 * h + 1].y, acc[ip][4 * h + 2].y, acc[ip][4 * h + 3].y);
+    return make_float4(acc[ip][4 * h].x, acc[ip][4 * h + 1].x, acc[ip][4 * h + 2].x, acc[ip][4 * h + 3].x);
+}
+__device__ __forceinline__ float4 out4(const float2 (&acc)[8][4], int i, int h)
+{
+    return make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+}
+
+// One BK = 32 slab of A^T and B: 8 chunks of 4 k. Per k a thread loads two
+// 128-bit words of A^T (its rows 4r.. and 16+4r..) and two of B (its columns
+// 4c.. and 32+4c..), then issues 4 x 8 FFMA2 (a_m, a_m+1) * (b_n, b_n).
 template <class T>
-__device__ __forceinline__ void compute_slab(const float *__restrict__ a_rows,
+__device__ __forceinline__ void compute_slab_mmajor(const float *__restrict__ a_cols,
+                                                    const float *__restrict__ b_cols, float2 (&acc)[4][8])
+{
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+        float4 a[4][2], b[4][2];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            a[kk][0] = *reinterpret_cast<const float4 *>(a_cols + (kc * 4 + kk) * T::BM);
+            a[kk][1] = *reinterpret_cast<const float4 *>(a_cols + (kc * 4 + kk) * T::BM + 16);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            b[kk][0] = *reinterpret_cast<const float4 *>(b_cols + (kc * 4 + kk) * T::BN);
+            b[kk][1] = *reinterpret_cast<const float4 *>(b_cols + (kc * 4 + kk) * T::BN + 32);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float2 ap[4] = {make_float2(a[kk][0].x, a[kk][0].y), make_float2(a[kk][0].z, a[kk][0].w),
+                                  make_float2(a[kk][1].x, a[kk][1].y), make_float2(a[kk][1].z, a[kk][1].w)};
+            const float bv[8] = {b[kk][0].x, b[kk][0].y, b[kk][0].z, b[kk][0].w,
+                                 b[kk][1].x, b[kk][1].y, b[kk][1].z, b[kk][1].w};
+#pragma unroll
+            for (int ip = 0; ip < 4; ++ip)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[ip][j] = __ffma2_rn(ap[ip], make_float2(bv[j], bv[j]), acc[ip][j]);
+        }
+    }
+}
+
+// One BK = 32 slab of K-major A and B: 8 chunks of 4 k. Per chunk a thread
+// loads its 8 rows of A (one 128-bit load each: 4 consecutive k) and 4 x 2
+// 128-bit loads of B, then issues 4 * 8 * 4 = 128 FFMA2 (a_m, a_m) * (b_n, b_n+1).
+template <class T>
+__device__ __forceinline__ void compute_slab_kmajor(const float *__restrict__ a_rows,
                                              const float *__restrict__ b_cols, int r,
                                              float2 (&acc)[8][4])
 {
@@ -233,24 +308,24 @@ __device__ __forceinline__ void store_c4(const FfmaParams &p, int row, int col, 
     }
 }
 
-template <class T>
-__device__ __forceinline__ void epilogue(const FfmaParams &p, const float2 (&acc)[8][4], int tile, int tm,
-                                         int tn, int ks, int nsplit, int wm, int wn, int r, int c)
+template <class T, bool AT>
+__device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc, int tile, int tm, int tn, int ks,
+                                         int nsplit, int wm, int wn, int r, int c)
 {
-    const int row0 = tm * T::BM + wm * T::WM + r;
+    const int row0 = tm * T::BM + wm * T::WM;
     const int col0 = tn * T::BN + wn * T::WN + c * 4;
     if (p.tail_splits > 1 && nsplit > 1) {
         // Tail-split slice: the whole partial tile, tile-packed (rows beyond M
         // or columns beyond N hold sums of the copy engine's zero fill).
         float *W = p.W + (static_cast<long long>(tile - p.n_full) * p.tail_splits + ks) * (T::BM * T::BN);
-        const int lr0 = wm * T::WM + r;
+        const int lr0 = wm * T::WM;
         const int lc0 = wn * T::WN + c * 4;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                *reinterpret_cast<float4 *>(W + (lr0 + 4 * i) * T::BN + lc0 + 32 * h) =
-                    make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                *reinterpret_cast<float4 *>(W + (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h) =
+                    out4(acc, i, h);
             }
         }
         return;
@@ -260,14 +335,13 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const float2 (&acc
         float *W = p.W + static_cast<long long>(ks) * p.wstride;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int row = row0 + 4 * i;
-            if (row >= p.M) break;
+            const int row = row0 + out_row<AT>(r, i);
+            if (row >= p.M) break;  // rows increase with i
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int col = col0 + 32 * h;
                 if (col < p.N) {
-                    *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) =
-                        make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y);
+                    *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) = out4(acc, i, h);
                 }
             }
         }
@@ -275,19 +349,17 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const float2 (&acc
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int row = row0 + 4 * i;
+        const int row = row0 + out_row<AT>(r, i);
         if (row >= p.M) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = col0 + 32 * h;
-            if (col < p.N)
-                store_c4(p, row, col,
-                         make_float4(acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y));
+            if (col < p.N) store_c4(p, row, col, out4(acc, i, h));
         }
     }
 }
 
-template <class T>
+template <class T, bool AT>
 __global__ void __launch_bounds__(T::THREADS, T::MINB)
 ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const FfmaParams p)
@@ -320,15 +392,15 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == T::CONSUMERS) {
         if (lane == 0)
-            producer_loop<T>(&tmA, &tmB, p, smem_addr(sA), smem_addr(sB), bar_base, abort_flag);
+            producer_loop<T, AT>(&tmA, &tmB, p, smem_addr(sA), smem_addr(sB), bar_base, abort_flag);
         return;
     }
 
     const int wm = warp % T::WARPS_M;
     const int wn = warp / T::WARPS_M;
-    const int r = lane >> 3;  // row group: rows wm*32 + r + 4i
+    const int r = lane >> 3;  // row group: rows wm*32 + out_row(r, i)
     const int c = lane & 7;   // column group: columns wn*64 + 4c + {0..3} and + 32
-    const float *a_rows_base = sA + (wm * T::WM + r) * T::BK;
+    const float *a_base = AT ? sA + wm * T::WM + 4 * r : sA + (wm * T::WM + r) * T::BK;
     const float *b_cols_base = sB + wn * T::WN + c * 4;
 
     int stage = 0;
@@ -337,11 +409,12 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int tm, tn, ks;
         int t, ns;
         decode_unit(p, u, t, tm, tn, ks, ns);
-        float2 acc[8][4];
+        Acc<AT> acc;
+        constexpr int kRows = AT ? 4 : 8;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < kRows; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+            for (int j = 0; j < 32 / kRows; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
         const int kb1 = split_begin(p, ks + 1, ns);
         for (int kb = split_begin(p, ks, ns); kb < kb1; ++kb) {
@@ -355,7 +428,11 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 return;
             }
-            compute_slab<T>(a_rows_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), r, acc);
+            if constexpr (AT)
+                compute_slab_mmajor<T>(a_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), acc);
+            else
+                compute_slab_kmajor<T>(a_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), r,
+                                       acc);
             if (p.skew_ns < 0) __nanosleep(static_cast<unsigned>(-p.skew_ns));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_base + 8 * (T::STAGES + stage));
@@ -364,7 +441,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 phase ^= 1u;
             }
         }
-        epilogue<T>(p, acc, t, tm, tn, ks, ns, wm, wn, r, c);
+        epilogue<T, AT>(p, acc, t, tm, tn, ks, ns, wm, wn, r, c);
     }
 }
 
@@ -388,14 +465,21 @@ static_assert(matches<Cfg0>(0) && matches<Cfg1>(1) && matches<Cfg2>(2) && matche
 template <class T>
 cudaError_t set_attr()
 {
-    return cudaFuncSetAttribute(ffma_sgemm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(ffma_sgemm_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(ffma_sgemm_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                T::SMEM_BYTES);
 }
 
 template <class T>
-cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
+cudaError_t launch(bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
                    cudaStream_t stream)
 {
-    ffma_sgemm_kernel<T><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    if (a_mmajor)
+        ffma_sgemm_kernel<T, true><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    else
+        ffma_sgemm_kernel<T, false><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
 }
 
@@ -496,6 +580,55 @@ __global__ void repack_kernel(const float *__restrict__ src, long long lds, floa
     }
 }
 
+// XT (cols x ldxt) = X^T for X (rows x cols, row stride ldx) through 64 x 64
+// tiles in shared memory, so both the reads of X rows and the writes of XT rows
+// are coalesced; interior tiles move 16 bytes per thread access when X allows
+// it (VEC: X 16-byte aligned and ldx % 4 == 0; ldxt is always a multiple of 4).
+// Grid-stride over tile rows, so any row count fits the grid's y limit. Gives
+// the FFMA mainloop A^T and the TF32 mainloop B^T.
+template <bool VEC>
+__global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ X, long long ldx,
+                                                        float *__restrict__ XT, long long ldxt, int rows, int cols)
+{
+    __shared__ float tile[64][65];
+    const int c0 = blockIdx.x * 64;
+    const int t = threadIdx.x;
+    for (long long r0l = blockIdx.y * 64LL; r0l < rows; r0l += gridDim.y * 64LL) {
+        const int r0 = static_cast<int>(r0l);
+        const bool interior = VEC && r0 + 64 <= rows && c0 + 64 <= cols;
+        if (interior) {
+            const int c = (t % 16) * 4;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int r = t / 16 + 16 * q;
+                const float4 v = *reinterpret_cast<const float4 *>(X + static_cast<long long>(r0 + r) * ldx + c0 + c);
+                tile[r][c] = v.x;
+                tile[r][c + 1] = v.y;
+                tile[r][c + 2] = v.z;
+                tile[r][c + 3] = v.w;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = t / 16 + 16 * q;
+                *reinterpret_cast<float4 *>(XT + static_cast<long long>(c0 + n) * ldxt + r0 + c) =
+                    make_float4(tile[c][n], tile[c + 1][n], tile[c + 2][n], tile[c + 3][n]);
+            }
+        } else {
+            for (int e = t; e < 64 * 64; e += 256) {
+                const int r = e / 64, c = e % 64;
+                if (r0 + r < rows && c0 + c < cols) tile[r][c] = X[static_cast<long long>(r0 + r) * ldx + c0 + c];
+            }
+            __syncthreads();
+            for (int e = t; e < 64 * 64; e += 256) {
+                const int n = e / 64, k = e % 64;
+                if (c0 + n < cols && r0 + k < rows) XT[static_cast<long long>(c0 + n) * ldxt + r0 + k] = tile[k][n];
+            }
+        }
+        __syncthreads();  // the tile is reused by the next row block
+    }
+}
+
 int elementwise_grid(long long work, int threads, int num_sms)
 {
     const long long blocks = (work + threads - 1) / threads;
@@ -514,14 +647,14 @@ cudaError_t ffma_set_attributes()
     return set_attr<Cfg3>();
 }
 
-cudaError_t launch_ffma(int config, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
-                        cudaStream_t stream)
+cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const FfmaParams &p, int grid, cudaStream_t stream)
 {
     switch (config) {
-    case 0: return launch<Cfg0>(tmA, tmB, p, grid, stream);
-    case 1: return launch<Cfg1>(tmA, tmB, p, grid, stream);
-    case 2: return launch<Cfg2>(tmA, tmB, p, grid, stream);
-    case 3: return launch<Cfg3>(tmA, tmB, p, grid, stream);
+    case 0: return launch<Cfg0>(a_mmajor, tmA, tmB, p, grid, stream);
+    case 1: return launch<Cfg1>(a_mmajor, tmA, tmB, p, grid, stream);
+    case 2: return launch<Cfg2>(a_mmajor, tmA, tmB, p, grid, stream);
+    case 3: return launch<Cfg3>(a_mmajor, tmA, tmB, p, grid, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -555,6 +688,18 @@ cudaError_t launch_repack(const float *src, long long lds, float *dst, long long
 {
     repack_kernel<<<elementwise_grid(static_cast<long long>(rows) * cols, 256, num_sms), 256, 0, stream>>>(
         src, lds, dst, ldd, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const float *X, long long ldx, float *XT, long long ldxt, int rows, int cols,
+                             cudaStream_t stream)
+{
+    const int gy = (rows + 63) / 64;
+    const dim3 grid((cols + 63) / 64, gy < 65535 ? gy : 65535);
+    if ((reinterpret_cast<uintptr_t>(X) & 15u) == 0 && ldx % 4 == 0 && ldxt % 4 == 0)
+        transpose_kernel<true><<<grid, 256, 0, stream>>>(X, ldx, XT, ldxt, rows, cols);
+    else
+        transpose_kernel<false><<<grid, 256, 0, stream>>>(X, ldx, XT, ldxt, rows, cols);
     return cudaGetLastError();
 }
 

@@ -67,6 +67,17 @@ int choose_tail(const sgemm_cfg::TileConfig &c, int M, int N, int K, int num_sms
     return best;
 }
 
+// Transposing A first pays when its copy (read + write of A, one more launch)
+// costs less than the ~10 % the A^T mainloop saves (measured 9-10 % at
+// 2048^3 .. 8192^3; kAtGain keeps a margin).
+bool transpose_pays(const Problem &q, double t_main)
+{
+    constexpr double kAtGain = 0.07;
+    const double hbm = 5.5e12;
+    const double t_copy = 8.0 * static_cast<double>(q.M) * q.K / hbm + 2.5e-6;
+    return t_copy < kAtGain * t_main;
+}
+
 }  // namespace
 
 int validate(const Problem &q)
@@ -202,9 +213,17 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         }
     }
 
+    // A^T: the mainloop's FFMA2 form with A pairs along M runs ~10 % faster;
+    // transposing A costs one read and one write of A.
+    if (ov.force_transpose_a >= 0)
+        out->transpose_a = ov.force_transpose_a;
+    else
+        out->transpose_a = transpose_pays(q, model_time(c, q.M, q.N, q.K, S, q.num_sms, q.beta != 0.0f)) ? 1 : 0;
+    if (out->transpose_a) out->repack_a = 0;  // the transposed copy is aligned whatever A was
+
     const Workspace w = workspace_layout(q, *out);
     out->workspace_bytes = w.total;
-    out->launches = 1 + out->repack_a + out->repack_b + (S > 1 || out->tail_splits > 1 ? 1 : 0);
+    out->launches = 1 + out->transpose_a + out->repack_a + out->repack_b + (S > 1 || out->tail_splits > 1 ? 1 : 0);
     return SGEMM_OK;
 }
 
@@ -212,7 +231,11 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
 {
     Workspace w{};
     long long off = 0;
-    if (p.repack_a) {
+    if (p.transpose_a) {
+        w.lda = round_up(q.M, 4);
+        w.a_off = off;
+        off += round_up(static_cast<long long>(q.K) * w.lda * 4, 256);
+    } else if (p.repack_a) {
         w.lda = round_up(q.K, 4);
         w.a_off = off;
         off += round_up(static_cast<long long>(q.M) * w.lda * 4, 256);

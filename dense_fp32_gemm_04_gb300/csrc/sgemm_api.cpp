@@ -121,9 +121,10 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
 {
     std::fprintf(stderr,
                  "[sgemm] M=%d N=%d K=%d kernel=%d config=%d tile=%dx%dx%d stages=%d splits=%d units=%d grid=%d "
-                 "repack=(%d,%d) vec_c=%d mode=%d launches=%d ws=%lld tail=%dx%d\n",
+                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld tail=%dx%d\n",
                  M, N, K, p.kernel, p.config, p.bm, p.bn, p.bk, p.stages, p.splits, p.units, p.grid, p.repack_a,
-                 p.repack_b, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.tail_tiles, p.tail_splits);
+                 p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.tail_tiles,
+                 p.tail_splits);
 }
 
 // TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop.
@@ -222,7 +223,12 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     const float *b_src = B;
     long long b_ld = ldb;
     if (plan.kernel == SGEMM_KERNEL_TF32) return run_tf32(h, plan, w, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
-    if (plan.repack_a) {
+    if (plan.transpose_a) {
+        float *dst = reinterpret_cast<float *>(ws + w.a_off);
+        if (launch_transpose(A, lda, dst, w.lda, M, K, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        a_src = dst;
+        a_ld = w.lda;
+    } else if (plan.repack_a) {
         float *dst = reinterpret_cast<float *>(ws + w.a_off);
         if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_src = dst;
@@ -236,9 +242,11 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     }
 
     CUtensorMap tmA, tmB;
-    if ((rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kFfmaBK, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-        SGEMM_OK)
-        return rc;
+    if (plan.transpose_a)  // A^T: K rows of M, boxes of 32 k x BM m
+        rc = make_tmap(h, &tmA, a_src, M, K, a_ld, plan.bm, sgemm_cfg::kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else  // A: M rows of K, boxes of BM m x 32 k, 128-byte swizzle
+        rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kFfmaBK, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != SGEMM_OK) return rc;
     if ((rc = make_tmap(h, &tmB, b_src, N, K, b_ld, plan.bn, sgemm_cfg::kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
         SGEMM_OK)
         return rc;
@@ -269,7 +277,8 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         p.n_full = plan.tiles_m * plan.tiles_n - plan.tail_tiles;
         p.tail_splits = plan.tail_splits;
     }
-    if (launch_ffma(plan.config, tmA, tmB, p, plan.grid, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (launch_ffma(plan.config, plan.transpose_a != 0, tmA, tmB, p, plan.grid, stream) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     if (plan.tail_splits > 1 && launch_tail_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1) {
@@ -350,6 +359,10 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
     if (const char *fs = std::getenv("SGEMM_FORCE_SPLITS")) {
         const long v = std::strtol(fs, nullptr, 10);
         if (v >= 0 && v <= kMaxSplits) h->ov.force_splits = static_cast<int>(v);
+    }
+    if (const char *ft = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
+        const long v = std::strtol(ft, nullptr, 10);
+        if (v >= -1 && v <= 1) h->ov.force_transpose_a = static_cast<int>(v);
     }
     *out = h;
     return SGEMM_OK;
@@ -556,6 +569,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
     case SGEMM_OPT_SKEW_NS:
         if (value < -100000 || value > 100000) return SGEMM_ERR_INVALID_VALUE;
         h->skew_ns = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_FORCE_TRANSPOSE_A:
+        if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.force_transpose_a = static_cast<int>(value);
         return SGEMM_OK;
     default:
         return SGEMM_ERR_INVALID_VALUE;

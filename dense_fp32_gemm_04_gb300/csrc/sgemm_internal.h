@@ -66,7 +66,8 @@ struct Tf32Params {
 // Plain-launch helpers implemented in the .cu files. All return the CUDA
 // error of the launch (cudaSuccess when it was enqueued).
 cudaError_t ffma_set_attributes();  // opt in to large dynamic shared memory (current device)
-cudaError_t launch_ffma(int config, const CUtensorMap &tmA, const CUtensorMap &tmB,
+// a_mmajor: tmA maps A^T (K rows of M, M contiguous) instead of A (M rows of K).
+cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const FfmaParams &p, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
@@ -82,7 +83,8 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int 
 cudaError_t tf32_set_attributes();
 cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
                         cudaStream_t stream);
-cudaError_t launch_transpose(const float *B, long long ldb, float *BT, long long ldbt, int K, int N,
+// XT (cols x ldxt) = X^T for X (rows x cols, row stride ldx); ldxt % 4 == 0.
+cudaError_t launch_transpose(const float *X, long long ldx, float *XT, long long ldxt, int rows, int cols,
                              cudaStream_t stream);
 cudaError_t launch_repack(const float *src, long long lds, float *dst, long long ldd, int rows,
                           int cols, int num_sms, cudaStream_t stream);

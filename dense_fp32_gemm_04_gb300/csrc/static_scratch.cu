@@ -148,6 +148,7 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
 
     Overrides ov;
     ov.force_splits = splits;
+    ov.force_transpose_a = 0;  // the scratch array holds split-K partials only
     sgemm_plan_t plan;
     if ((rc = sgemm_impl::make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
     if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;
@@ -208,7 +209,8 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
     p.status = status;
     p.timeout_ns = kTimeoutNs;
     p.inject_skip = -1;
-    if (sgemm_impl::launch_ffma(plan.config, tmA, tmB, p, plan.grid, st) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (sgemm_impl::launch_ffma(plan.config, false, tmA, tmB, p, plan.grid, st) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1 &&
         sgemm_impl::launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
                                          s->num_sms, st) != cudaSuccess)

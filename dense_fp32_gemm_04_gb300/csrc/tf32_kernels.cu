@@ -16,7 +16,7 @@
 //               stores.
 // Both operands must be K-major for this instruction form: A (row-major M x K)
 // already is; B (row-major K x N) is first transposed into the handle's
-// workspace by transpose_kernel.
+// workspace (transpose_kernel, ffma_kernels.cu).
 //
 // All waits are bounded; on expiry the CTA records SGEMM_ERR_TIMEOUT, lets its
 // copies and MMAs in flight finish (bounded), frees its TMEM and returns.
@@ -258,49 +258,6 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
-// BT (N x ldbt) = B^T for B (K x N, row stride ldb) through 64 x 64 tiles in
-// shared memory, so both the reads of B rows and the writes of BT rows are
-// coalesced; interior tiles move 16 bytes per thread access when B allows it
-// (VEC: B 16-byte aligned and ldb % 4 == 0; ldbt is always a multiple of 4).
-template <bool VEC>
-__global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ B, long long ldb,
-                                                        float *__restrict__ BT, long long ldbt, int K, int N)
-{
-    __shared__ float tile[64][65];
-    const int n0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
-    const int t = threadIdx.x;
-    const bool interior = VEC && k0 + 64 <= K && n0 + 64 <= N;
-    if (interior) {
-        const int c = (t % 16) * 4;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int r = t / 16 + 16 * q;
-            const float4 v = *reinterpret_cast<const float4 *>(B + static_cast<long long>(k0 + r) * ldb + n0 + c);
-            tile[r][c] = v.x;
-            tile[r][c + 1] = v.y;
-            tile[r][c + 2] = v.z;
-            tile[r][c + 3] = v.w;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int n = t / 16 + 16 * q;
-            *reinterpret_cast<float4 *>(BT + static_cast<long long>(n0 + n) * ldbt + k0 + c) =
-                make_float4(tile[c][n], tile[c + 1][n], tile[c + 2][n], tile[c + 3][n]);
-        }
-    } else {
-        for (int e = t; e < 64 * 64; e += 256) {
-            const int r = e / 64, c = e % 64;
-            if (k0 + r < K && n0 + c < N) tile[r][c] = B[static_cast<long long>(k0 + r) * ldb + n0 + c];
-        }
-        __syncthreads();
-        for (int e = t; e < 64 * 64; e += 256) {
-            const int n = e / 64, k = e % 64;
-            if (n0 + n < N && k0 + k < K) BT[static_cast<long long>(n0 + n) * ldbt + k0 + k] = tile[k][n];
-        }
-    }
-}
-
 }  // namespace
 
 cudaError_t tf32_set_attributes()
@@ -313,17 +270,6 @@ cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const T
                         cudaStream_t stream)
 {
     tf32_sgemm_kernel<<<grid, THREADS, sgemm_cfg::tf32_smem_bytes(), stream>>>(tmA, tmBt, p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose(const float *B, long long ldb, float *BT, long long ldbt, int K, int N,
-                             cudaStream_t stream)
-{
-    const dim3 grid((N + 63) / 64, (K + 63) / 64);
-    if ((reinterpret_cast<uintptr_t>(B) & 15u) == 0 && ldb % 4 == 0 && ldbt % 4 == 0)
-        transpose_kernel<true><<<grid, 256, 0, stream>>>(B, ldb, BT, ldbt, K, N);
-    else
-        transpose_kernel<false><<<grid, 256, 0, stream>>>(B, ldb, BT, ldbt, K, N);
     return cudaGetLastError();
 }
 

@@ -92,6 +92,8 @@ typedef struct sgemm_plan_s {
     int tail_tiles;          /* tiles of the last, partial round of the persistent grid that are
                                 split along K to even out the waves (0 = none) */
     int tail_splits;         /* K slices per tail tile (their partials are reduced in order) */
+    int transpose_a;         /* 1: A is first transposed into the workspace (K x M, M contiguous)
+                                and the FP32 mainloop reads A^T; 0: it reads A as given */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */
@@ -103,9 +105,11 @@ typedef enum sgemm_option {
                                      (-1 = off, the default); the consumers' wait then runs out
                                      and the run reports SGEMM_ERR_TIMEOUT without faulting */
     SGEMM_OPT_LOG = 5,            /* 1: print the chosen plan of each call to stderr */
-    SGEMM_OPT_SKEW_NS = 6         /* TEST ONLY (race detection): > 0 delays the FP32 kernel's copy
+    SGEMM_OPT_SKEW_NS = 6,        /* TEST ONLY (race detection): > 0 delays the FP32 kernel's copy
                                      issue by this many ns per k-slab, < 0 delays every compute warp
                                      before it releases a slab; |value| <= 100000, 0 = off */
+    SGEMM_OPT_FORCE_TRANSPOSE_A = 7 /* FP32 path: -1 = automatic (the default), 0 = read A as given,
+                                     1 = always transpose A first (same results either way) */
 } sgemm_option_t;
 
 /*
@@ -117,7 +121,8 @@ typedef enum sgemm_option {
  * aligned operand copies) and, for sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
- * SGEMM_FORCE_SPLITS=<S> preset the planner overrides of sgemm_set_option.
+ * SGEMM_FORCE_SPLITS=<S> and SGEMM_FORCE_TRANSPOSE_A=<-1|0|1> preset the
+ * planner overrides of sgemm_set_option.
  */
 int sgemm_create(sgemm_handle_t *out);
 

@@ -85,27 +85,34 @@ def test_plan_square_4096(lib):
     assert p.tail_tiles == tiles - (tiles // slots) * slots == 112
     assert p.tail_splits > 1
     assert p.units == tiles - p.tail_tiles + p.tail_tiles * p.tail_splits
-    assert p.launches == 2 and p.workspace_bytes >= p.tail_tiles * p.tail_splits * p.bm * p.bn * 4
+    # A is transposed first (A^T mainloop): transpose + mainloop + tail reduce
+    assert p.transpose_a == 1 and p.launches == 3
+    assert p.workspace_bytes >= p.tail_tiles * p.tail_splits * p.bm * p.bn * 4 + 4096 * 4096 * 4
 
 
 def test_plan_full_rounds_have_no_tail(lib):
     # 8192^3: 4096 tiles -> 26.9 rounds, the last one 94 % full: not worth splitting
     p = sg.plan(8192, 8192, 8192, num_sms=152)
-    assert p.tail_tiles == 0 and p.units == p.tiles_m * p.tiles_n and p.launches == 1
+    assert p.tail_tiles == 0 and p.units == p.tiles_m * p.tiles_n
+    assert p.transpose_a == 1 and p.launches == 2
 
 
 def test_plan_ragged_unaligned_repacks(lib):
-    # ld = 1531 / 3001 floats are not multiples of 4: rows are not 16-byte aligned,
-    # so both operands go through the aligned workspace copy and C is scalar.
+    # ld = 1531 / 3001 floats are not multiples of 4: rows are not 16-byte aligned.
+    # A is transposed into the workspace (which aligns it too), B goes through the
+    # aligned workspace copy, and C is accessed with scalar loads and stores.
     p = sg.plan(2047, 3001, 1531, lda=1531, ldb=3001, ldc=3001)
-    assert p.repack_a == 1 and p.repack_b == 1 and p.vec_c == 0
+    assert p.transpose_a == 1 and p.repack_a == 0 and p.repack_b == 1 and p.vec_c == 0
     assert p.launches == 3 + (1 if (p.splits > 1 or p.tail_splits > 1) else 0)
-    assert p.workspace_bytes >= 4 * (2047 * 1532 + 1531 * 3004)
+    assert p.workspace_bytes >= 4 * (1531 * 2048 + 1531 * 3004)
+    # Without the transposition (small N) an unaligned A is repacked instead.
+    q = sg.plan(20000, 16, 1531, lda=1531, ldb=16, ldc=16)
+    assert q.transpose_a == 0 and q.repack_a == 1 and q.repack_b == 0
 
 
 def test_plan_misaligned_pointer_repacks(lib):
     p = sg.plan(512, 512, 512, align_flags=0b110)
-    assert p.repack_a == 1 and p.repack_b == 0
+    assert p.transpose_a == 0 and p.repack_a == 1 and p.repack_b == 0
 
 
 def test_plan_skinny_uses_split_k(lib):
@@ -115,6 +122,8 @@ def test_plan_skinny_uses_split_k(lib):
         assert p.splits > 1, p.as_dict()
         assert p.units >= 152
         assert p.workspace_bytes >= p.splits * M * N * 4
+        # transposing a 16384 x 8192 A costs more than it saves; a 64 x 8192 A is cheap
+        assert p.transpose_a == (1 if M == 64 else 0)
 
 
 def test_config_table(lib):
@@ -156,15 +165,19 @@ def test_plan_invariants_random_shapes(lib):
             if p.splits > 1:
                 assert p.workspace_bytes >= p.splits * M * (-(-N // 4) * 4) * 4
         assert 1 <= p.grid <= min(p.units, slots)
-        assert p.repack_a == (0 if (align & 1 and lda % 4 == 0) else 1)
+        assert p.transpose_a in (0, 1)
+        assert p.repack_a == (0 if (p.transpose_a or (align & 1 and lda % 4 == 0)) else 1)
         assert p.repack_b == (0 if (align & 2 and ldb % 4 == 0) else 1)
         assert p.vec_c == (1 if (align & 4 and ldc % 4 == 0) else 0)
+        if p.transpose_a:
+            assert p.workspace_bytes >= K * (-(-M // 4) * 4) * 4
         extra = 1 if (p.splits > 1 or p.tail_splits > 1) else 0
-        assert p.launches == 1 + p.repack_a + p.repack_b + extra
+        assert p.launches == 1 + p.transpose_a + p.repack_a + p.repack_b + extra
 
 
 def test_tf32_plan(lib):
     p = sg.plan(4096, 4096, 4096, math_mode=sg.MATH_TF32)
     assert p.kernel == sg.KERNEL_TF32 and (p.bm, p.bn, p.bk) == (128, 256, 32)
     assert p.repack_b == 1 and p.launches == 2 and p.units == 32 * 16 and p.grid == 152
+    assert p.transpose_a == 0
     assert p.workspace_bytes >= 4096 * 4096 * 4  # B transposed to K-major

@@ -43,27 +43,52 @@ def test_tiny_shapes_exact(h):
         check_against_oracle(got, A, B, C, 1.5, -0.5, exact=True)
 
 
+def force(h, config=-1, splits=0, transpose_a=-1):
+    h.set_option(sg.OPT_FORCE_CONFIG, config)
+    h.set_option(sg.OPT_FORCE_SPLITS, splits)
+    h.set_option(sg.OPT_FORCE_TRANSPOSE_A, transpose_a)
+
+
 @pytest.mark.parametrize("cfg", range(4))
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_every_config_and_split(h, cfg, splits):
-    """Each tile-config row and split factor, around tile multiples, integer and real operands."""
-    h.set_option(sg.OPT_FORCE_CONFIG, cfg)
-    h.set_option(sg.OPT_FORCE_SPLITS, splits)
+@pytest.mark.parametrize("ta", [0, 1])
+def test_every_config_and_split(h, cfg, splits, ta):
+    """Each tile-config row, split factor and A layout (as given / transposed first),
+    around tile multiples, integer and real operands."""
+    force(h, cfg, splits, ta)
     try:
         for (M, N, K) in [(63, 65, 33), (129, 127, 95), (200, 300, 257), (256, 128, 224)]:
             A, B, C = ops(M, N, K, seed=cfg * 10 + splits)
             got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
             assert st == sg.SGEMM_OK and guards
             p = h.last_plan()
-            assert p.config == cfg and p.splits == min(splits, (K + 31) // 32)
+            assert p.config == cfg and p.splits == min(splits, (K + 31) // 32) and p.transpose_a == ta
             check_against_oracle(got, A, B, C, 1.5, 0.5, exact=True)
             Ar, Br, Cr = ops(M, N, K, seed=cfg * 10 + splits + 1, dist=("normal", "uniform", "uniform"))
             got, guards, st = run_gemm(torch, h, Ar, Br, Cr, -0.75, 1.25)
             assert st == sg.SGEMM_OK and guards
             check_against_oracle(got, Ar, Br, Cr, -0.75, 1.25)
     finally:
-        h.set_option(sg.OPT_FORCE_CONFIG, -1)
-        h.set_option(sg.OPT_FORCE_SPLITS, 0)
+        force(h)
+
+
+@pytest.mark.parametrize("cfg", range(4))
+def test_a_layouts_give_identical_bits(h, cfg):
+    """Both A layouts evaluate every output as the same FMA chain in ascending k:
+    the results must agree bit for bit (real operands, every split path)."""
+    for (M, N, K), splits in [((300, 260, 777), 1), ((129, 200, 500), 3), ((1000, 2500, 513), 0)]:
+        A, B, C = ops(M, N, K, seed=cfg + M, dist=("normal", "normal", "uniform"))
+        outs = []
+        for ta in (0, 1):
+            force(h, cfg, splits, ta)
+            try:
+                got, guards, st = run_gemm(torch, h, A, B, C, 1.25, -0.5)
+                assert st == sg.SGEMM_OK and guards and h.last_plan().transpose_a == ta
+            finally:
+                force(h)
+            outs.append(got)
+        assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32)), (cfg, M, N, K)
+        check_against_oracle(outs[1], A, B, C, 1.25, -0.5)
 
 
 def test_deterministic(h):
@@ -73,19 +98,25 @@ def test_deterministic(h):
     assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
 
 
-def test_leading_dimensions_and_misalignment(h):
-    """Padded leading dimensions keep pad columns untouched; misaligned pointers take the repack path."""
+@pytest.mark.parametrize("ta", [0, 1])
+def test_leading_dimensions_and_misalignment(h, ta):
+    """Padded leading dimensions keep pad columns untouched; misaligned pointers take
+    the repack path (A as given) or the transposition (A transposed first)."""
     M, N, K = 190, 170, 150
     A, B, C = ops(M, N, K, seed=77)
-    for lds, offs in [((K + 4, N + 8, N + 12), (0, 0, 0)),    # aligned, padded
-                      ((K + 1, N + 3, N + 5), (0, 0, 0)),     # unaligned strides
-                      ((None, None, None), (1, 2, 3)),        # unaligned pointers
-                      ((K + 3, N, N + 1), (2, 0, 1))]:
-        got, guards, st = run_gemm(torch, h, A, B, C, 2.0, -1.0, lds=lds, offsets=offs)
-        assert st == sg.SGEMM_OK and guards, (lds, offs)
-        check_against_oracle(got, A, B, C, 2.0, -1.0, exact=True)
-    p = h.last_plan()
-    assert p.repack_a == 1 and p.vec_c == 0
+    force(h, transpose_a=ta)
+    try:
+        for lds, offs in [((K + 4, N + 8, N + 12), (0, 0, 0)),    # aligned, padded
+                          ((K + 1, N + 3, N + 5), (0, 0, 0)),     # unaligned strides
+                          ((None, None, None), (1, 2, 3)),        # unaligned pointers
+                          ((K + 3, N, N + 1), (2, 0, 1))]:
+            got, guards, st = run_gemm(torch, h, A, B, C, 2.0, -1.0, lds=lds, offsets=offs)
+            assert st == sg.SGEMM_OK and guards, (lds, offs)
+            check_against_oracle(got, A, B, C, 2.0, -1.0, exact=True)
+        p = h.last_plan()
+    finally:
+        force(h)
+    assert p.transpose_a == ta and p.repack_a == 1 - ta and p.vec_c == 0
 
 
 def test_quick_returns(h):
@@ -191,7 +222,9 @@ def test_ragged(h, name):
     got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
     assert st == sg.SGEMM_OK and guards
     plan = h.last_plan()
-    assert plan.repack_a and plan.repack_b and not plan.vec_c
+    # lda, ldb, ldc are not multiples of 4: A reaches the mainloop transposed (or
+    # repacked), B through the aligned copy, C through scalar accesses
+    assert (plan.transpose_a or plan.repack_a) and plan.repack_b and not plan.vec_c
     check_against_oracle(got, A, B, C, p["alpha"], p["beta"], exact=name.endswith("_int"))
 
 
@@ -215,8 +248,18 @@ def test_skinny(h, name):
 
 
 @pytest.mark.parametrize("shape", [(1000, 2500, 513), (1999, 3001, 1031), (1500, 4095, 2050)])
-def test_tail_split(h, shape):
+@pytest.mark.parametrize("ta", [0, 1])
+def test_tail_split(h, shape, ta):
     """Shapes whose last round is split along K (tail split): exact on integers, bound on reals."""
+    h.set_option(sg.OPT_FORCE_TRANSPOSE_A, ta)
+    try:
+        _tail_split_case(h, shape)
+        assert h.last_plan().transpose_a == ta
+    finally:
+        h.set_option(sg.OPT_FORCE_TRANSPOSE_A, -1)
+
+
+def _tail_split_case(h, shape):
     M, N, K = shape
     A, B, C = ops(M, N, K, seed=M + N, dist=("int", "int", "int"))
     got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
@@ -280,13 +323,13 @@ def test_offsets_beyond_2_31_elements(h):
 def test_timing_skew_is_race_free(h, skew):
     """A slow producer (skew > 0) or slow consumers (skew < 0) change only timing:
     results stay bitwise identical (a race on the shared-memory ring would show here)."""
-    cases = [((1999, 3001, 1031), dict()), ((700, 900, 1500), dict(config=1, splits=3)),
-             ((300, 260, 777), dict(config=3, splits=1))]
-    for (M, N, K), force in cases:
+    cases = [((1999, 3001, 1031), dict()), ((700, 900, 1500), dict(config=1, splits=3, transpose_a=0)),
+             ((700, 900, 1500), dict(config=1, splits=3, transpose_a=1)),
+             ((300, 260, 777), dict(config=3, splits=1, transpose_a=0)),
+             ((300, 260, 777), dict(config=3, splits=1, transpose_a=1))]
+    for (M, N, K), forced in cases:
         A, B, C = ops(M, N, K, seed=M + skew, dist=("normal", "uniform", "uniform"))
-        if force:
-            h.set_option(sg.OPT_FORCE_CONFIG, force["config"])
-            h.set_option(sg.OPT_FORCE_SPLITS, force["splits"])
+        force(h, **forced)
         try:
             ref_run, _, st = run_gemm(torch, h, A, B, C, 1.0, 1.0)
             assert st == sg.SGEMM_OK
@@ -296,7 +339,6 @@ def test_timing_skew_is_race_free(h, skew):
             assert h.check_device_status() == (sg.SGEMM_OK, 0)
         finally:
             h.set_option(sg.OPT_SKEW_NS, 0)
-            h.set_option(sg.OPT_FORCE_CONFIG, -1)
-            h.set_option(sg.OPT_FORCE_SPLITS, 0)
+            force(h)
         assert np.array_equal(ref_run.view(np.uint32), skewed.view(np.uint32)), (M, N, K, skew)
         check_against_oracle(skewed, A, B, C, 1.0, 1.0)
