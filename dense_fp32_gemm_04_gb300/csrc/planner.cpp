@@ -78,6 +78,38 @@ bool transpose_pays(const Problem &q, double t_main)
     return t_copy < kAtGain * t_main;
 }
 
+// Tail split of the TF32 mode (one 128 x 256 tile per SM per round): the last,
+// partial round's tiles are cut into St K slices (St <= 8, at least one 32-deep
+// block each) when the modelled time saved exceeds the partial-tile reduction.
+// Rates: the mainloop's measured ~650 TFLOP/s, ~5.5 TB/s for the reduction.
+int choose_tail_tf32(int M, int N, int K, int num_sms, bool beta_read)
+{
+    const double flops_per_sm = 650e12 / 152.0;
+    const double hbm = 5.5e12;
+    const long long kb = ceil_div(K, sgemm_cfg::kTf32BK);
+    const long long tiles = ceil_div(M, sgemm_cfg::kTf32BM) * ceil_div(N, sgemm_cfg::kTf32BN);
+    const long long slots = num_sms;
+    const long long rounds = ceil_div(tiles, slots);
+    const long long rem = tiles - (rounds - 1) * slots;
+    if (rem >= slots) return 0;
+    const double tile_elems = static_cast<double>(sgemm_cfg::kTf32BM) * sgemm_cfg::kTf32BN;
+    const double t_kb = tile_elems * sgemm_cfg::kTf32BK * 2.0 / flops_per_sm;
+    const double t_last = (static_cast<double>(kb) + 1.5) * t_kb;
+    double best_gain = 0.01 * static_cast<double>(rounds) * t_last;
+    int best = 0;
+    for (int st = 2; st <= 8 && st <= kb; ++st) {
+        const double t_tail = static_cast<double>(ceil_div(rem * st, slots)) *
+                              (static_cast<double>(ceil_div(kb, st)) + 1.5) * t_kb;
+        const double bytes = (2.0 * st + (beta_read ? 2.0 : 1.0)) * 4.0 * static_cast<double>(rem) * tile_elems;
+        const double gain = t_last - t_tail - bytes / hbm - 2.5e-6;
+        if (gain > best_gain) {
+            best_gain = gain;
+            best = st;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 int validate(const Problem &q)
@@ -177,8 +209,21 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         if (units > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
         out->units = static_cast<int>(units);
         out->grid = static_cast<int>(std::min<long long>(units, q.num_sms));
+        if (ov.force_splits == 0) {
+            const int st = choose_tail_tf32(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
+            if (st > 1) {
+                const long long slots = q.num_sms;
+                const long long n_full = (ceil_div(units, slots) - 1) * slots;
+                out->tail_tiles = static_cast<int>(units - n_full);
+                out->tail_splits = st;
+                const long long u2 = n_full + static_cast<long long>(out->tail_tiles) * st;
+                if (u2 > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
+                out->units = static_cast<int>(u2);
+                out->grid = static_cast<int>(std::min<long long>(u2, slots));
+            }
+        }
         out->workspace_bytes = workspace_layout(q, *out).total;
-        out->launches = 1 + out->repack_a + 1;
+        out->launches = 1 + out->repack_a + 1 + (out->tail_splits > 1 ? 1 : 0);
         return SGEMM_OK;
     }
 

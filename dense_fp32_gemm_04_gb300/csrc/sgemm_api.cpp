@@ -165,7 +165,30 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     p.vec_c = plan.vec_c;
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
-    return launch_tf32(tmA, tmBt, p, plan.grid, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    if (plan.tail_splits > 1) {
+        p.W = reinterpret_cast<float *>(ws + w.w_off);
+        p.n_full = plan.tiles_m * plan.tiles_n - plan.tail_tiles;
+        p.tail_splits = plan.tail_splits;
+    }
+    if (launch_tf32(tmA, tmBt, p, plan.grid, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (plan.tail_splits > 1) {
+        // Same tile-packed partial layout and tile raster as the FP32 tail split.
+        FfmaParams r{};
+        r.M = M;
+        r.N = N;
+        r.alpha = alpha;
+        r.beta = beta;
+        r.C = C;
+        r.ldc = ldc;
+        r.W = p.W;
+        r.tiles_m = plan.tiles_m;
+        r.tiles_n = plan.tiles_n;
+        r.vec_c = plan.vec_c;
+        r.n_full = p.n_full;
+        r.tail_splits = p.tail_splits;
+        if (launch_tail_reduce(r, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
 }
 
 // Streams and events of the host-buffer pipeline, created on first use.

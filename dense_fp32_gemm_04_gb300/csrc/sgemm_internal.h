@@ -61,6 +61,12 @@ struct Tf32Params {
     int vec_c;
     int *status;
     long long timeout_ns;
+    // Tail split, as in FfmaParams: units [0, n_full) are whole tiles, the
+    // rest are tail_splits K slices of the remaining tiles whose partial tiles
+    // go, tile-packed, to W + ((tile - n_full) * tail_splits + slice) * BM * BN.
+    float *W;
+    int n_full;
+    int tail_splits;  // <= 1: no tail split
 };
 
 // Plain-launch helpers implemented in the .cu files. All return the CUDA

@@ -69,6 +69,26 @@ __device__ __forceinline__ void decode_tile(const Tf32Params &p, int u, int &tm,
     tn = r / gsize;
 }
 
+// Work unit u -> tile t (grouped raster), K-block range [kb0, kb1), slice ks
+// of ns (ns == 1: the whole tile).
+__device__ __forceinline__ void decode_unit(const Tf32Params &p, int u, int &t, int &tm, int &tn, int &ks, int &ns,
+                                            int &kb0, int &kb1)
+{
+    if (p.tail_splits > 1 && u >= p.n_full) {
+        const int v = u - p.n_full;
+        t = p.n_full + v / p.tail_splits;
+        ks = v % p.tail_splits;
+        ns = p.tail_splits;
+    } else {
+        t = u;
+        ks = 0;
+        ns = 1;
+    }
+    decode_tile(p, t, tm, tn);
+    kb0 = static_cast<int>((static_cast<long long>(ks) * p.kblocks) / ns);
+    kb1 = static_cast<int>((static_cast<long long>(ks + 1) * p.kblocks) / ns);
+}
+
 __device__ __forceinline__ void raise_abort(Bars *b, const Tf32Params &p, int where)
 {
     volatile int *f = &b->abort_flag;
@@ -123,9 +143,9 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t phase = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-            int tm, tn;
-            decode_tile(p, u, tm, tn);
-            for (int kb = 0; kb < p.kblocks; ++kb) {
+            int t, tm, tn, ks, ns, kb0, kb1;
+            decode_unit(p, u, t, tm, tn, ks, ns, kb0, kb1);
+            for (int kb = kb0; kb < kb1; ++kb) {
                 const uint32_t full = smem_addr(&bars->full[stage]);
                 if (!mbar_wait_bounded(smem_addr(&bars->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
                     raise_abort(bars, p, kWhereProducerEmpty);
@@ -163,7 +183,9 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
-            for (int kb = 0; kb < p.kblocks; ++kb) {
+            int t, tm, tn, ks, ns, kb0, kb1;
+            decode_unit(p, u, t, tm, tn, ks, ns, kb0, kb1);
+            for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait_bounded(smem_addr(&bars->full[stage]), phase, abort_flag, p.timeout_ns)) {
                     raise_abort(bars, p, kWhereMmaEmpty);
                     ok = false;
@@ -176,7 +198,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int k = 0; k < BK / MMA_K; ++k) {
                     // K advances 8 TF32 = 32 bytes inside the 128-byte swizzle atom.
                     mma_tf32(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4), smem_desc_k_sw128(b_s + k * MMA_K * 4),
-                             IDESC, (kb | k) != 0 ? 1u : 0u);
+                             IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
                 }
                 mma_commit(smem_addr(&bars->empty[stage]));  // stage free once these MMAs are done
                 if (++stage == STAGES) {
@@ -205,10 +227,32 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after_sync();
-            int tm, tn;
-            decode_tile(p, u, tm, tn);
+            int t, tm, tn, ks, ns, kb0, kb1;
+            decode_unit(p, u, t, tm, tn, ks, ns, kb0, kb1);
             const int row = tm * BM + quarter * 32 + lane;
             const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
+            if (ns > 1) {
+                // Tail slice: the raw partial tile, tile-packed (rows and columns past
+                // M and N hold sums of the copy engine's zero fill); the tail
+                // reduction adds the slices in order and applies alpha / beta.
+                float *wrow = p.W + (static_cast<long long>(t - p.n_full) * p.tail_splits + ks) * (BM * BN) +
+                              (quarter * 32 + lane) * BN;
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 16; ++ch) {
+                    uint32_t v[16];
+                    tmem_ld_16(t_row + ch * 16, v);
+                    tmem_wait_ld(v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<float4 *>(wrow + ch * 16 + 4 * q) =
+                            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&bars->acc_empty[buf]));
+                continue;
+            }
             float *crow = p.C + static_cast<long long>(row) * p.ldc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 16; ++ch) {

@@ -178,6 +178,9 @@ def test_plan_invariants_random_shapes(lib):
 def test_tf32_plan(lib):
     p = sg.plan(4096, 4096, 4096, math_mode=sg.MATH_TF32)
     assert p.kernel == sg.KERNEL_TF32 and (p.bm, p.bn, p.bk) == (128, 256, 32)
-    assert p.repack_b == 1 and p.launches == 2 and p.units == 32 * 16 and p.grid == 152
-    assert p.transpose_a == 0
+    assert p.repack_b == 1 and p.grid == 152 and p.transpose_a == 0
+    # 512 tiles on 152 SMs: 3 whole rounds, then the 56 remaining tiles in 2 K slices
+    assert p.tail_tiles == 56 and p.tail_splits == 2 and p.units == 456 + 112
+    assert p.launches == 3  # B transpose, mainloop, tail reduction
+    assert p.workspace_bytes >= 4096 * 4096 * 4 + 56 * 2 * 128 * 256 * 4
     assert p.workspace_bytes >= 4096 * 4096 * 4  # B transposed to K-major
