@@ -1,5 +1,6 @@
-// FP32 FFMA SGEMM mainloop for sm_103a, plus the split-K reduction, the
-// beta-only scaling kernel and the operand repack used for unaligned inputs.
+// FP32 FFMA SGEMM mainloop for sm_103a, plus the operand layout kernels
+// (A / B transposition, repack of unaligned operands), the split-K and
+// tail-split reductions and the beta-only scaling kernel.
 //
 // C = alpha * A * B + beta * C, row-major ("SGEMM CUDA kernel (First Half)",
 // opening definition). The structure follows the tiling ladder of the pages —
@@ -10,13 +11,13 @@
 // CUDA", 2D thread tiling), warps own 32 x 64 sub-tiles (same page, warp
 // tiling) — rebuilt for Blackwell:
 //
-//  * Staging: one producer thread issues TMA tile copies (A box 32 x BM with
-//    the 128-byte swizzle, B box BN x 32) into a STAGES-deep ring guarded by
-//    full/empty mbarriers, in place of the pages' load / __syncthreads /
-//    compute / __syncthreads phase loop. Out-of-range rows and columns are
-//    zero-filled by the copy engine, which is the pages' zero-fill
-//    predication ("SGEMM CUDA kernel (First Half)", Part 5 load_ast) done in
-//    hardware.
+//  * Staging: one producer thread issues TMA tile copies (A^T box BM x 32 or,
+//    for A as given, A box 32 x BM with the 128-byte swizzle; B box BN x 32)
+//    into a STAGES-deep ring guarded by full/empty mbarriers, in place of the
+//    pages' load / __syncthreads / compute / __syncthreads phase loop.
+//    Out-of-range rows and columns are zero-filled by the copy engine, which
+//    is the pages' zero-fill predication ("SGEMM CUDA kernel (First Half)",
+//    Part 5 load_ast) done in hardware.
 //  * A layout and bank conflicts: the pages transpose A in shared memory so a
 //    thread's TM values of A are contiguous (same page, Part 5). Here the
 //    transposition happens once per call, in global memory: transpose_kernel

@@ -102,3 +102,11 @@ def test_two_gloo_ranks_take_the_max():
     assert got == {0: 0.8, 1: 0.8}
     value, t = bench.aggregate([0.5, 0.8], [2e12, 2e12])
     assert t == 0.8 and abs(value - 4e12 / 0.8 / 1e12) < 1e-12
+
+
+def test_kernel_hash_ignores_comments():
+    src = 'int a = 1; // note\n/* block\n note */ const char *s = "x // kept"; char c = \'/\';\n'
+    assert bench.strip_comments(src) == 'int a = 1; const char *s = "x // kept"; char c = \'/\';'
+    assert bench.strip_comments("a  =\n b;") == bench.strip_comments("a = b;".replace(" b", "\n  b"))
+    assert bench.strip_comments("x = 1; // a") == bench.strip_comments("x = 1; // b")
+    assert bench.strip_comments("x = 1;") != bench.strip_comments("x = 2;")
