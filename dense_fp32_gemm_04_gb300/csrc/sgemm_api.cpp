@@ -1,6 +1,7 @@
 // C ABI of the GB300 SGEMM library: handle lifetime, argument checks, plan
 // execution (repack -> mainloop -> split-K reduce), host-buffer entry point
 // and status reporting. Declarations and contracts: include/sgemm.h.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <new>
@@ -210,17 +211,36 @@ int ensure_host_pipeline(sgemm_handle_t h)
     return SGEMM_OK;
 }
 
-// Row panels for sgemm_run_host: enough that copies of later panels overlap the
-// compute of earlier ones, few enough that each panel still fills the GPU for
-// about two rounds of 128 x 128 tiles.
-int host_panels(sgemm_handle_t h, int M, int N, int K)
+// Row panels for sgemm_run_host, as start rows (start[P] = M). The first and
+// last panels are about M / 8 rows so that the copy-in before the first GEMM
+// and the copy-out after the last one are short; the rows between them are
+// split evenly into panels of at least two rounds of 128 x 128 tiles (at most
+// 4), whose copies overlap the GEMMs of their neighbours. Problems with less
+// than two such rounds between the edges are one panel. The edge panels and
+// all middle panels but the last have a multiple of 128 rows.
+int host_panel_starts(sgemm_handle_t h, int M, int N, int K, int *start)
 {
-    if (static_cast<double>(M) * N * K < 1.0e9 || M < 256) return 1;
-    const long long tiles = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
-    long long p = tiles / (2LL * h->num_sms);
-    if (p > 4) p = 4;
-    if (p > M / 128) p = M / 128;
-    return p < 1 ? 1 : static_cast<int>(p);
+    start[0] = 0;
+    if (static_cast<double>(M) * N * K < 1.0e9 || M < 1024) {
+        start[1] = M;
+        return 1;
+    }
+    const int edge = std::max(128, M / 8 / 128 * 128);
+    const int mid = M - 2 * edge;
+    const long long mid_tiles = static_cast<long long>((mid + 127) / 128) * ((N + 127) / 128);
+    if (mid_tiles < 2LL * h->num_sms) {  // too little work to hide the copies behind
+        start[1] = M;
+        return 1;
+    }
+    long long nmid = mid_tiles / (2LL * h->num_sms);
+    nmid = std::max(1LL, std::min({nmid, 4LL, static_cast<long long>(mid / 128)}));
+    const int mid_rows = ((mid + static_cast<int>(nmid) - 1) / static_cast<int>(nmid) + 127) / 128 * 128;
+    int P = 0;
+    start[++P] = edge;
+    for (int i = 0; i < nmid - 1 && start[P] + mid_rows < M - edge; ++i) start[P + 1] = start[P] + mid_rows, ++P;
+    start[++P] = M - edge;
+    start[++P] = M;
+    return P;
 }
 
 int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
@@ -462,8 +482,8 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     // panel p + 1 is copied in and panel p - 1 is copied out on the copy-out
     // stream. Every panel is an ordinary device call on the staged copies.
     cudaStream_t s = stream;
-    const int P = host_panels(h, M, N, K);
-    const int rows_per = ((M + P - 1) / P + 127) / 128 * 128;
+    int start[kMaxHostPanels + 1];
+    const int P = host_panel_starts(h, M, N, K, start);
     const bool copy_c_in = beta != 0.0f;
     bool ok = cudaEventRecord(h->ev_start, s) == cudaSuccess && cudaStreamWaitEvent(h->h2d, h->ev_start, 0) == cudaSuccess &&
               cudaStreamWaitEvent(h->d2h, h->ev_start, 0) == cudaSuccess;
@@ -474,9 +494,8 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     int panels = 0;
     bool c_changed = true;
     for (int p = 0; ok && p < P; ++p) {
-        const int r0 = p * rows_per;
-        if (r0 >= M) break;
-        const int mp = (M - r0 < rows_per) ? (M - r0) : rows_per;
+        const int r0 = start[p];
+        const int mp = start[p + 1] - r0;
         const float *hA = A + static_cast<long long>(r0) * lda;
         float *hC = C + static_cast<long long>(r0) * ldc;
         float *pA = dA + static_cast<long long>(r0) * dlda;
