@@ -82,7 +82,8 @@ typedef struct sgemm_plan_s {
     int ctas_per_sm;         /* resident CTAs per SM the grid is sized for */
     int splits;              /* split-K factor S (1 = fused epilogue) */
     int tiles_m, tiles_n;    /* output tiles */
-    int units;               /* tiles_m * tiles_n * splits work units */
+    int units;               /* work units: tiles_m * tiles_n * splits, or with a tail split the
+                                whole tiles plus tail_tiles * tail_splits K slices */
     int grid;                /* CTAs launched (persistent: min(units, SMs * ctas_per_sm)) */
     int repack_a, repack_b;  /* operand first copied to a 16-byte-aligned workspace copy */
     int vec_c;               /* 1: C read/written with 16-byte accesses */
@@ -117,8 +118,9 @@ typedef enum sgemm_option {
  * out: receives the handle (set to NULL on failure).
  * Returns SGEMM_ERR_ARCH unless the device is compute capability 10.3,
  * SGEMM_ERR_ALLOC if its small device status word cannot be allocated.
- * The handle owns a lazily grown device workspace (split-K partials and
- * aligned operand copies) and, for sgemm_run_host, device staging buffers.
+ * The handle owns a lazily grown device workspace (the transposed copy of A,
+ * aligned operand copies, split-K and tail-split partials) and, for
+ * sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
  * SGEMM_FORCE_SPLITS=<S> and SGEMM_FORCE_TRANSPOSE_A=<-1|0|1> preset the
