@@ -20,7 +20,6 @@ LIB = os.path.join(OUT_DIR, "libsgemm_gb300.so")
 OBJ_DIR = os.path.join(ROOT, "_build", "obj")
 
 SOURCES = ["ffma_kernels.cu", "tf32_kernels.cu", "min2_kernels.cu", "ladder_kernels.cu", "planner.cpp", "sgemm_api.cpp", "static_scratch.cu"]
-HEADERS = ["device_ptx.cuh", "sgemm_internal.h", "tile_table.h", "planner.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -37,8 +36,10 @@ def _flags(extra=()):
 
 
 def _deps():
-    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", h)
-                                                                 for h in ("sgemm.h", "sgemm_ladder.h")]
+    """Newest modification time of everything the library is built from."""
+    inc = os.path.join(ROOT, "include")
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h", ".cpp"))]
+    files += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

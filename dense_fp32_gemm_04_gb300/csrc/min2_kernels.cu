@@ -34,6 +34,7 @@ __device__ __forceinline__ bool before(float a, long long pa, float b, long long
 
 __device__ __forceinline__ void push(Top2 &t, float v, long long p)
 {
+    if (v > t.v1) return;  // the common case: above the current second (v0 <= v1, never NaN)
     if (v != v) v = __int_as_float(0x7f800000);  // NaN ranks as +inf
     if (before(v, p, t.v0, t.p0)) {
         t.v1 = t.v0;
@@ -90,14 +91,25 @@ __global__ void __launch_bounds__(kThreads) min2_pass1(const float *__restrict__
         const float *crow = C + static_cast<long long>(row) * ldc;
         const long long base = static_cast<long long>(row) * N;
         if (VEC) {
-            // 16-byte loads of 4 consecutive columns (C 16-byte aligned, ldc % 4 == 0)
+            // 16-byte loads of 4 consecutive columns (C 16-byte aligned, ldc % 4 == 0),
+            // four of them in flight per thread before any is compared
             const int n4 = N & ~3;
-            for (int col = 4 * threadIdx.x; col < n4; col += 4 * kThreads) {
-                const float4 v = *reinterpret_cast<const float4 *>(crow + col);
-                push(t, v.x, base + col);
-                push(t, v.y, base + col + 1);
-                push(t, v.z, base + col + 2);
-                push(t, v.w, base + col + 3);
+            constexpr int kStep = 4 * kThreads;
+            for (int c0 = 4 * threadIdx.x; c0 < n4; c0 += 4 * kStep) {
+                float4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (c0 + j * kStep < n4) v[j] = __ldcs(reinterpret_cast<const float4 *>(crow + c0 + j * kStep));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col = c0 + j * kStep;
+                    if (col < n4) {
+                        push(t, v[j].x, base + col);
+                        push(t, v[j].y, base + col + 1);
+                        push(t, v[j].z, base + col + 2);
+                        push(t, v[j].w, base + col + 3);
+                    }
+                }
             }
             for (int col = n4 + threadIdx.x; col < N; col += kThreads) push(t, crow[col], base + col);
         } else {

@@ -92,3 +92,58 @@ def test_deterministic_under_ties(h):
     B = np.ones((17, 500), np.float32)
     got, vals, ij = _run(h, A, B, np.zeros((300, 500), np.float32), 1.0, 0.0)
     assert list(vals) == [17.0, 17.0] and list(ij) == [0, 0, 0, 1]
+
+
+@pytest.mark.parametrize("force", [dict(), dict(config=1, splits=3), dict(config=3, splits=1),
+                                   dict(config=0, splits=1, transpose_a=0), dict(config=2, splits=5, transpose_a=1)])
+@pytest.mark.parametrize("shape", [(300, 200, 100), (1000, 2500, 513), (2047, 3001, 1531)])
+def test_every_plan(h, force, shape):
+    """Whichever kernel writes the final C values (whole-tile epilogue with either A
+    layout, tail-split reduction, split-K reduction), the pass over C finds the two
+    minima. Integer operands: values and positions equal the oracle's."""
+    M, N, K = shape
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=7 * M + N, dist=("int", "int", "int"))
+    h.set_option(sg.OPT_FORCE_CONFIG, force.get("config", -1))
+    h.set_option(sg.OPT_FORCE_SPLITS, force.get("splits", 0))
+    h.set_option(sg.OPT_FORCE_TRANSPOSE_A, force.get("transpose_a", -1))
+    try:
+        got, vals, ij = _run(h, A, B, C, -1.0, 1.0)
+    finally:
+        h.set_option(sg.OPT_FORCE_CONFIG, -1)
+        h.set_option(sg.OPT_FORCE_SPLITS, 0)
+        h.set_option(sg.OPT_FORCE_TRANSPOSE_A, -1)
+    ref, _ = oracle.sgemm_f64(A, B, C, -1.0, 1.0, with_mag=False)
+    assert oracle.exact(got, ref)
+    rv, rr, rc = oracle.min2(ref)
+    assert list(vals.astype(np.float64)) == rv and list(ij) == [rr[0], rc[0], rr[1], rc[1]]
+
+
+def test_tail_split_plan(h):
+    # whole tiles plus a K-split last round (104 tail tiles in 4 slices on 152 SMs)
+    M, N, K = 2048, 2048, 2048
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=99, dist=("int", "int", "zero"))
+    got, vals, ij = _run(h, A, B, C, 1.0, 0.0)
+    plan = h.last_plan()
+    ref, _ = oracle.sgemm_f64(A, B, None, 1.0, 0.0, with_mag=False)
+    assert oracle.exact(got, ref)
+    rv, rr, rc = oracle.min2(ref)
+    assert list(vals.astype(np.float64)) == rv and list(ij) == [rr[0], rc[0], rr[1], rc[1]]
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert plan.tail_splits > 1, plan.as_dict()
+
+
+def test_tf32_and_scale_only_plans(h):
+    """TF32 mode and C = beta * C (alpha == 0): the same pass over C."""
+    A, B, C = inputs.problem_operands(M=333, N=444, K=96, seed=5, dist=("int", "int", "int"))
+    got, vals, ij = _run(h, A, B, C, 0.0, 2.0)
+    rv, rr, rc = oracle.min2(2.0 * C.astype(np.float64))
+    assert list(vals.astype(np.float64)) == rv and list(ij) == [rr[0], rc[0], rr[1], rc[1]]
+    h.set_math_mode(sg.MATH_TF32)
+    try:
+        got, vals, ij = _run(h, A, B, C, 1.0, 1.0)
+    finally:
+        h.set_math_mode(sg.MATH_FP32)
+    ref, _ = oracle.sgemm_f64(A, B, C, 1.0, 1.0, with_mag=False)
+    assert oracle.exact(got, ref)  # integer operands are exact in TF32
+    rv, rr, rc = oracle.min2(ref)
+    assert list(vals.astype(np.float64)) == rv and list(ij) == [rr[0], rc[0], rr[1], rc[1]]
