@@ -46,6 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--tf32-steps", type=int, default=50, help="calls timed in the flagged TF32 mode (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other configured problem sizes")
+    ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS context timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
 
@@ -462,6 +463,33 @@ def measure_configs(torch, sg, h, dev, stream, hbm_gbs, min_seconds=1.0):
                     "beta != 0) / time"}
 
 
+def measure_library_context(torch, dA, dB, dC, alpha, beta, flops, steps=20):
+    """cuBLAS through torch.addmm on the same operands (C <- alpha*A*B + beta*C), FP32 and
+    TF32: context only, never on the product path."""
+    out = {"note": "torch.addmm (cuBLAS) on the same operands, alpha/beta included; context only"}
+    prev = torch.backends.cuda.matmul.allow_tf32
+    D = torch.empty_like(dC)
+    try:
+        for mode, tf32 in (("fp32", False), ("tf32", True)):
+            torch.backends.cuda.matmul.allow_tf32 = tf32
+            for _ in range(3):
+                torch.addmm(dC, dA, dB, beta=beta, alpha=alpha, out=D)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                torch.addmm(dC, dA, dB, beta=beta, alpha=alpha, out=D)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            out[f"{mode}_tflops"] = flops / (ms * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    del D
+    return out
+
+
 def measured_hbm_gbs():
     try:
         return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
@@ -548,6 +576,8 @@ def run_ours(args, world):
     min2 = measure_min2(torch, sg, h, dA, dB, dC, M, N, K, alpha, beta, stream, ms_per_call=elapsed / args.steps * 1e3)
     configs = (measure_configs(torch, sg, h, dev, stream, measured_hbm_gbs())
                if world.size == 1 and not args.no_configs else None)
+    library = (measure_library_context(torch, dA, dB, dC, alpha, beta, flops)
+               if world.size == 1 and not args.no_context else None)
     tf32 = (measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, world.local_rank, args.tf32_steps)
             if args.tf32_steps > 0 else None)
 
@@ -586,6 +616,7 @@ def run_ours(args, world):
         "tf32_mode": tf32,
         "min2": min2,
         "configs": configs,
+        "library_context": library,
     }
     if world.rank == 0 and world.size == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds, A, B, C)
