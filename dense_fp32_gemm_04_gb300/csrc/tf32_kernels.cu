@@ -98,6 +98,86 @@ __device__ __forceinline__ void raise_abort(Bars *b, const Tf32Params &p, int wh
     }
 }
 
+// Epilogue of one accumulator row (a thread's TMEM lane: 256 columns), NB x 16
+// columns per step: NB TMEM loads, one wait, then (beta != 0) all of the step's
+// C loads before any use. Short K (few k-blocks per tile) makes the epilogue the
+// critical path, so there NB = 4 keeps 16 loads in flight per thread; with long
+// K it overlaps the next tile's mainloop and NB = 1 keeps its memory traffic
+// from crowding the operand copies (measured: NB = 4 everywhere cost 2-4 % at
+// 4096^3 and 8192^2 x 4096, and saved 44 % at K = 32).
+constexpr int kShortK = 16;  // k-blocks of 32
+
+template <int NB>
+__device__ __forceinline__ void load_row_chunks(uint32_t t_col, uint32_t (&v)[NB][16])
+{
+#pragma unroll
+    for (int j = 0; j < NB; ++j) tmem_ld_16(t_col + j * 16, v[j]);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) tmem_wait_ld(v[j]);
+}
+
+// Raw partial row of a tail slice (tile-packed workspace row of BN floats).
+template <int NB>
+__device__ __forceinline__ void store_partial_row(uint32_t t_row, float *wrow)
+{
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 16; ch += NB) {
+        uint32_t v[NB][16];
+        load_row_chunks<NB>(t_row + ch * 16, v);
+#pragma unroll
+        for (int q = 0; q < 4 * NB; ++q) {
+            const uint32_t *w = &v[q >> 2][4 * (q & 3)];
+            *reinterpret_cast<float4 *>(wrow + ch * 16 + 4 * q) =
+                make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
+                            __uint_as_float(w[3]));
+        }
+    }
+}
+
+// C[row, tn*BN ...] = alpha * acc + beta * C (beta == 0: C not read).
+template <int NB>
+__device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row, int row, int tn)
+{
+    float *crow = p.C + static_cast<long long>(row) * p.ldc;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 16; ch += NB) {
+        uint32_t v[NB][16];
+        load_row_chunks<NB>(t_row + ch * 16, v);  // every lane: .sync.aligned
+        if (row >= p.M) continue;
+        const int colb = tn * BN + ch * 16;
+        if (p.vec_c && colb + 16 * NB - 1 < p.N) {
+            float4 c[4 * NB];
+            if (p.beta != 0.0f) {
+#pragma unroll
+                for (int q = 0; q < 4 * NB; ++q) c[q] = *reinterpret_cast<const float4 *>(crow + colb + 4 * q);
+            }
+#pragma unroll
+            for (int q = 0; q < 4 * NB; ++q) {
+                const uint32_t *w = &v[q >> 2][4 * (q & 3)];
+                const float4 acc = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
+                                               __uint_as_float(w[3]));
+                float4 out;
+                if (p.beta != 0.0f)
+                    out = make_float4(fmaf(p.alpha, acc.x, p.beta * c[q].x), fmaf(p.alpha, acc.y, p.beta * c[q].y),
+                                      fmaf(p.alpha, acc.z, p.beta * c[q].z), fmaf(p.alpha, acc.w, p.beta * c[q].w));
+                else
+                    out = make_float4(p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w);
+                *reinterpret_cast<float4 *>(crow + colb + 4 * q) = out;
+            }
+        } else {
+            // N edge or C not 16-byte accessible: element by element
+#pragma unroll
+            for (int q = 0; q < 16 * NB; ++q) {
+                const int col = colb + q;
+                if (col < p.N) {
+                    const float a = __uint_as_float(v[q >> 4][q & 15]);
+                    crow[col] = (p.beta != 0.0f) ? fmaf(p.alpha, a, p.beta * crow[col]) : p.alpha * a;
+                }
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
 tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBt,
                   const Tf32Params p)
@@ -237,56 +317,19 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // reduction adds the slices in order and applies alpha / beta.
                 float *wrow = p.W + (static_cast<long long>(t - p.n_full) * p.tail_splits + ks) * (BM * BN) +
                               (quarter * 32 + lane) * BN;
-#pragma unroll 1
-                for (int ch = 0; ch < BN / 16; ++ch) {
-                    uint32_t v[16];
-                    tmem_ld_16(t_row + ch * 16, v);
-                    tmem_wait_ld(v);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<float4 *>(wrow + ch * 16 + 4 * q) =
-                            make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                        __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                }
+                if (p.kblocks <= kShortK)
+                    store_partial_row<4>(t_row, wrow);
+                else
+                    store_partial_row<1>(t_row, wrow);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&bars->acc_empty[buf]));
                 continue;
             }
-            float *crow = p.C + static_cast<long long>(row) * p.ldc;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 16; ++ch) {
-                uint32_t v[16];
-                tmem_ld_16(t_row + ch * 16, v);
-                tmem_wait_ld(v);
-                const int col0 = tn * BN + ch * 16;
-                if (row < p.M) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int col = col0 + 4 * q;
-                        const float4 acc = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                       __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                        float *dst = crow + col;
-                        if (p.vec_c && col + 3 < p.N) {
-                            float4 out;
-                            if (p.beta != 0.0f) {
-                                const float4 c = *reinterpret_cast<const float4 *>(dst);
-                                out = make_float4(fmaf(p.alpha, acc.x, p.beta * c.x), fmaf(p.alpha, acc.y, p.beta * c.y),
-                                                  fmaf(p.alpha, acc.z, p.beta * c.z), fmaf(p.alpha, acc.w, p.beta * c.w));
-                            } else {
-                                out = make_float4(p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w);
-                            }
-                            *reinterpret_cast<float4 *>(dst) = out;
-                        } else {
-                            const float e[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-                            for (int t = 0; t < 4; ++t)
-                                if (col + t < p.N)
-                                    dst[t] = (p.beta != 0.0f) ? fmaf(p.alpha, e[t], p.beta * dst[t]) : p.alpha * e[t];
-                        }
-                    }
-                }
-            }
+            if (p.kblocks <= kShortK)
+                store_c_row<4>(p, t_row, row, tn);
+            else
+                store_c_row<1>(p, t_row, row, tn);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&bars->acc_empty[buf]));
