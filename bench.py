@@ -438,8 +438,8 @@ def measure_configs(torch, sg, h, dev, stream, hbm_gbs, min_seconds=1.0):
                      "ms_median": ms, "ms_min": min(times), "tflops": flops / (ms * 1e-3) / 1e12,
                      "tflops_best": flops / (min(times) * 1e-3) / 1e12, "hbm_gbs": bytes_alg / (ms * 1e-3) / 1e9,
                      "flop_per_byte": flops / bytes_alg, "status": st,
-                     "plan": {"config": plan.config, "splits": plan.splits, "tail_tiles": plan.tail_tiles,
-                              "tail_splits": plan.tail_splits, "launches": plan.launches}})
+                     "plan": {"config": plan.config, "splits": plan.splits, "sk_tiles": plan.sk_tiles,
+                              "transpose_a": plan.transpose_a, "launches": plan.launches}})
         del dA, dB, dC
     t1 = time.time()
     sampler.stop()
@@ -592,7 +592,8 @@ def run_ours(args, world):
                 "kernel": ("ffma_sgemm_kernel (plan config %d, %dx%d tile, A %s)" %
                            (plan.config, plan.bm, plan.bn, "transposed first" if plan.transpose_a else "as given")) +
                           (" + transpose_kernel (A^T)" if plan.transpose_a else "") +
-                          (" + tail_reduce_kernel" if plan.tail_splits > 1 else "") +
+                          (" + sk_reduce_kernel" if plan.sk_tiles > 0 else "") +
+                          (" + splitk_reduce_kernel" if plan.splits > 1 else "") +
                           (" (timed together per call: a lower bound for the mainloop)" if plan.launches > 1 else ""),
                 "peak_basis": f"{nsm} SMs x 128 FP32 FMA/clk x 2 FLOP x median SM clock under load "
                               f"({sm_mhz} MHz, nvidia-smi during the timed region)",

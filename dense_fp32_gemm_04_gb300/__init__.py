@@ -40,6 +40,7 @@ OPT_INJECT_SKIP = 4
 OPT_LOG = 5
 OPT_SKEW_NS = 6
 OPT_FORCE_TRANSPOSE_A = 7
+OPT_FORCE_STREAMK = 8
 
 
 class Plan(ctypes.Structure):
@@ -49,7 +50,7 @@ class Plan(ctypes.Structure):
         "kernel", "config", "bm", "bn", "bk", "stages", "threads", "ctas_per_sm", "splits",
         "tiles_m", "tiles_n", "units", "grid", "repack_a", "repack_b", "vec_c", "math_mode",
         "launches")] + [("workspace_bytes", ctypes.c_longlong), ("tail_tiles", ctypes.c_int),
-                        ("tail_splits", ctypes.c_int), ("transpose_a", ctypes.c_int)]
+                        ("tail_splits", ctypes.c_int), ("transpose_a", ctypes.c_int), ("sk_tiles", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -92,35 +92,58 @@ __device__ __forceinline__ void decode_tile(int tiles_m, int tiles_n, int t, int
     tn = r / gsize;
 }
 
-// Work unit u -> (tile row tm, tile column tn, K slice ks of nsplit). Slices
-// of a tile are adjacent units. In tail-split mode the first n_full units are
-// whole tiles and the rest are tail_splits slices of the remaining tiles.
-__device__ __forceinline__ void decode_unit(const FfmaParams &p, int u, int &t, int &tm, int &tn, int &ks,
-                                            int &nsplit)
-{
-    if (p.tail_splits > 1) {
-        if (u < p.n_full) {
-            t = u;
-            ks = 0;
-            nsplit = 1;
-        } else {
-            const int v = u - p.n_full;
-            t = p.n_full + v / p.tail_splits;
-            ks = v % p.tail_splits;
-            nsplit = p.tail_splits;
-        }
-    } else {
-        ks = u % p.splits;
-        t = u / p.splits;
-        nsplit = p.splits;
-    }
-    decode_tile(p.tiles_m, p.tiles_n, t, tm, tn);
-}
-
 // First k-block of slice ks of nsplit (balanced integer split of kblocks).
 __device__ __forceinline__ int split_begin(const FfmaParams &p, int ks, int nsplit)
 {
     return static_cast<int>((static_cast<long long>(ks) * p.kblocks) / nsplit);
+}
+
+// One piece of a CTA's work: tile t (tm, tn), k-blocks [kb0, kb1), and where
+// its result goes (kToC: alpha/beta into C; kToSplit: split-K slice idx;
+// kToPartial: stream-K partial tile slot idx).
+enum : int { kToC = 0, kToSplit = 1, kToPartial = 2 };
+struct Work {
+    int t, tm, tn, kb0, kb1, dest, idx;
+};
+
+// Item i of this CTA's work: first its units (u = blockIdx.x + i * gridDim.x),
+// then the pieces of its stream-K range, one per tile the range touches.
+// Computed from i alone, so that only i stays live across the mainloop;
+// producer and consumers walk the same sequence. Returns false past the end.
+__device__ __forceinline__ bool work_at(const FfmaParams &p, int i, Work &w)
+{
+    const int g = blockIdx.x, G = gridDim.x;
+    const int n_units = g < p.units ? (p.units - g + G - 1) / G : 0;
+    if (i < n_units) {
+        const int u = g + i * G;
+        const int ks = u % p.splits;
+        w.t = u / p.splits;
+        decode_tile(p.tiles_m, p.tiles_n, w.t, w.tm, w.tn);
+        w.kb0 = split_begin(p, ks, p.splits);
+        w.kb1 = split_begin(p, ks + 1, p.splits);
+        w.dest = p.splits > 1 ? kToSplit : kToC;
+        w.idx = ks;
+        return true;
+    }
+    if (p.sk_tiles <= 0 || g >= p.sk_grid) return false;
+    const long long S = static_cast<long long>(p.sk_tiles) * p.kblocks;
+    const long long b0 = static_cast<long long>(g) * S / p.sk_grid;
+    const long long b1 = static_cast<long long>(g + 1) * S / p.sk_grid;
+    const int j = i - n_units;
+    const long long first_rel = b0 / p.kblocks;
+    const long long rel = first_rel + j;
+    const long long tile_start = rel * p.kblocks;
+    const long long seg0 = j == 0 ? b0 : tile_start;
+    if (seg0 >= b1) return false;
+    const long long seg1 = b1 < tile_start + p.kblocks ? b1 : tile_start + p.kblocks;
+    w.t = p.units + static_cast<int>(rel);
+    decode_tile(p.tiles_m, p.tiles_n, w.t, w.tm, w.tn);
+    w.kb0 = static_cast<int>(seg0 - tile_start);
+    w.kb1 = static_cast<int>(seg1 - tile_start);
+    // a tile inside this CTA's range needs no partial
+    w.dest = (w.kb0 == 0 && w.kb1 == p.kblocks) ? kToC : kToPartial;
+    w.idx = 2 * g + (j == 0 ? 0 : 1);
+    return true;
 }
 
 template <class T, bool AT>
@@ -133,11 +156,10 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
     uint32_t issued = 0, issued_parity = 0;  // per stage: has a copy outstanding, and its phase parity
     int seq = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-        int t, tm, tn, ks, ns;
-        decode_unit(p, u, t, tm, tn, ks, ns);
-        const int kb1 = split_begin(p, ks + 1, ns);
-        for (int kb = split_begin(p, ks, ns); kb < kb1; ++kb) {
+    Work w;
+    for (int item = 0; ok && work_at(p, item, w); ++item) {
+        const int tm = w.tm, tn = w.tn;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             const uint32_t empty = bar_base + 8 * (T::STAGES + stage);
             if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -310,15 +332,15 @@ __device__ __forceinline__ void store_c4(const FfmaParams &p, int row, int col, 
 }
 
 template <class T, bool AT>
-__device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc, int tile, int tm, int tn, int ks,
-                                         int nsplit, int wm, int wn, int r, int c)
+__device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc, const Work &w, int wm, int wn,
+                                         int r, int c)
 {
-    const int row0 = tm * T::BM + wm * T::WM;
-    const int col0 = tn * T::BN + wn * T::WN + c * 4;
-    if (p.tail_splits > 1 && nsplit > 1) {
-        // Tail-split slice: the whole partial tile, tile-packed (rows beyond M
+    const int row0 = w.tm * T::BM + wm * T::WM;
+    const int col0 = w.tn * T::BN + wn * T::WN + c * 4;
+    if (w.dest == kToPartial) {
+        // Stream-K partial: the whole partial tile, tile-packed (rows beyond M
         // or columns beyond N hold sums of the copy engine's zero fill).
-        float *W = p.W + (static_cast<long long>(tile - p.n_full) * p.tail_splits + ks) * (T::BM * T::BN);
+        float *W = p.W + static_cast<long long>(w.idx) * (T::BM * T::BN);
         const int lr0 = wm * T::WM;
         const int lc0 = wn * T::WN + c * 4;
 #pragma unroll
@@ -331,9 +353,9 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc
         }
         return;
     }
-    if (p.splits > 1) {
+    if (w.dest == kToSplit) {
         // Partial sums to this split's slice; the reduction applies alpha/beta.
-        float *W = p.W + static_cast<long long>(ks) * p.wstride;
+        float *W = p.W + static_cast<long long>(w.idx) * p.wstride;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int row = row0 + out_row<AT>(r, i);
@@ -406,10 +428,14 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     int stage = 0;
     uint32_t phase = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        int tm, tn, ks;
-        int t, ns;
-        decode_unit(p, u, t, tm, tn, ks, ns);
+    for (int item = 0;; ++item) {
+        int kb0, kb1;
+        {
+            Work w;
+            if (!work_at(p, item, w)) break;
+            kb0 = w.kb0;
+            kb1 = w.kb1;
+        }
         Acc<AT> acc;
         constexpr int kRows = AT ? 4 : 8;
 #pragma unroll
@@ -417,8 +443,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 32 / kRows; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
-        const int kb1 = split_begin(p, ks + 1, ns);
-        for (int kb = split_begin(p, ks, ns); kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
@@ -442,7 +467,9 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 phase ^= 1u;
             }
         }
-        epilogue<T, AT>(p, acc, t, tm, tn, ks, ns, wm, wn, r, c);
+        Work w;  // recomputed here so that only `item` stays live across the mainloop
+        work_at(p, item, w);
+        epilogue<T, AT>(p, acc, w, wm, wn, r, c);
     }
 }
 
@@ -549,6 +576,49 @@ __global__ void tail_reduce_kernel(const FfmaParams p, int bm, int bn)
             s.y += t.y;
             s.z += t.z;
             s.w += t.w;
+        }
+        store_c4(p, row, col, s);
+    }
+}
+
+// Stream-K reduction: for every stream-K tile covered by more than one CTA,
+// C = alpha * sum_g P_g + beta * C with the partial tiles of the covering CTAs
+// added in CTA order, which is k order (see FfmaParams: CTA g covers k-blocks
+// [g S / G, (g + 1) S / G) of the span; the tile's first k-block lies in CTA
+// ((start + 1) G - 1) / S, its last in ((start + kblocks) G - 1) / S).
+__global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int bm, int bn)
+{
+    const long long S = static_cast<long long>(p.sk_tiles) * p.kblocks;
+    const long long G = p.sk_grid;
+    const int q4 = bn / 4;
+    const long long per_tile = static_cast<long long>(bm) * q4;
+    const long long total = per_tile * p.sk_tiles;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int rel = static_cast<int>(idx / per_tile);
+        const int e = static_cast<int>(idx - static_cast<long long>(rel) * per_tile);
+        const int lr = e / q4, lc = (e - lr * q4) * 4;
+        const long long start = static_cast<long long>(rel) * p.kblocks;
+        const long long g0 = ((start + 1) * G - 1) / S;
+        const long long g1 = ((start + p.kblocks) * G - 1) / S;
+        if (g0 == g1) continue;  // inside one CTA's range: written to C by the mainloop
+        int tm, tn;
+        decode_tile(p.tiles_m, p.tiles_n, p.units + rel, tm, tn);
+        const int row = tm * bm + lr, col = tn * bn + lc;
+        if (row >= p.M || col >= p.N) continue;
+        float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (long long g = g0; g <= g1; ++g) {
+            const long long first = (g * S / G) / p.kblocks;  // CTA g's first stream-K tile
+            const long long slot = 2 * g + (rel == first ? 0 : 1);
+            const float4 v = *reinterpret_cast<const float4 *>(p.W + slot * bm * bn + lr * bn + lc);
+            if (g == g0) {
+                s = v;
+            } else {
+                s.x += v.x;
+                s.y += v.y;
+                s.z += v.z;
+                s.w += v.w;
+            }
         }
         store_c4(p, row, col, s);
     }
@@ -674,6 +744,13 @@ cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms,
 {
     const long long work = static_cast<long long>(p.tiles_m * p.tiles_n - p.n_full) * bm * (bn / 4);
     tail_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(p, bm, bn);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)
+{
+    const long long work = static_cast<long long>(p.sk_tiles) * bm * (bn / 4);
+    sk_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(p, bm, bn);
     return cudaGetLastError();
 }
 

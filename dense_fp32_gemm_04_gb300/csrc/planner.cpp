@@ -37,10 +37,12 @@ double model_time(const sgemm_cfg::TileConfig &c, int M, int N, int K, int S, in
     return t;
 }
 
-// Tail split: with R rounds of `slots` tiles, the last round holds only `rem`
-// tiles. Splitting each of them into St K slices spreads them over the idle
-// CTAs; the partial tiles are then reduced. Returns the best St (0: not worth it).
-int choose_tail(const sgemm_cfg::TileConfig &c, int M, int N, int K, int num_sms, bool beta_read)
+// Stream-K: the first (R - 1) rounds of `slots` whole tiles run data-parallel;
+// the `rem` tiles of the last, partial round become one span of rem * kb
+// k-blocks cut evenly over the slots CTAs (each CTA then has at most two partial
+// tiles, reduced afterwards). Modelled time, or infinity when the last round is
+// full (nothing to balance).
+double model_time_sk(const sgemm_cfg::TileConfig &c, int M, int N, int K, int num_sms, bool beta_read)
 {
     const double fma_per_sm = 128.0 * 1.9e9 * 0.88;
     const double hbm = 5.5e12;
@@ -49,22 +51,16 @@ int choose_tail(const sgemm_cfg::TileConfig &c, int M, int N, int K, int num_sms
     const long long slots = static_cast<long long>(num_sms) * c.ctas_per_sm;
     const long long rounds = ceil_div(tiles, slots);
     const long long rem = tiles - (rounds - 1) * slots;
-    if (rounds < 2 || rem >= slots) return 0;
+    if (rem >= slots) return INFINITY;
+    const long long span = rem * kb;
+    const long long G = std::min(slots, span);
     const double t_kb = static_cast<double>(c.bm) * c.bn * sgemm_cfg::kFfmaBK * c.ctas_per_sm / fma_per_sm * c.rel_cost;
-    const double t_last = (static_cast<double>(kb) + 1.5) * t_kb;  // one round of whole tiles
-    double best_gain = 0.01 * static_cast<double>(rounds) * t_last;  // require at least 1 % overall
-    int best = 0;
-    for (int st = 2; st <= 8 && st <= kb; ++st) {
-        const double t_tail = static_cast<double>(ceil_div(rem * st, slots)) *
-                              (static_cast<double>(ceil_div(kb, st)) + 1.5) * t_kb;
-        const double bytes = (2.0 * st + (beta_read ? 2.0 : 1.0)) * 4.0 * rem * c.bm * c.bn;
-        const double gain = t_last - t_tail - bytes / hbm - 2.5e-6;
-        if (gain > best_gain) {
-            best_gain = gain;
-            best = st;
-        }
-    }
-    return best;
+    double t = static_cast<double>(rounds - 1) * (static_cast<double>(kb) + 1.5) * t_kb +
+               (static_cast<double>(ceil_div(span, G)) + 3.0) * t_kb + 2.0e-6;
+    const double tile_bytes = 4.0 * c.bm * c.bn;
+    const double bytes = (2.0 * static_cast<double>(G + rem) + (beta_read ? 2.0 : 1.0) * static_cast<double>(rem)) *
+                         tile_bytes;
+    return t + bytes / hbm + 2.5e-6;
 }
 
 // Transposing A first pays when its copy (read + write of A, one more launch)
@@ -243,18 +239,21 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     if (units > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
     out->units = static_cast<int>(units);
     out->grid = static_cast<int>(std::min<long long>(units, static_cast<long long>(q.num_sms) * c.ctas_per_sm));
-    if (S == 1 && ov.force_splits == 0) {
-        const int st = choose_tail(c, q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
-        if (st > 1) {
+    if (ov.force_splits == 0 && ov.force_streamk != 0) {
+        // Stream-K on the chosen row when it beats the split-K plan (or is forced).
+        const bool beta_read = q.beta != 0.0f;
+        const double t_sk = model_time_sk(c, q.M, q.N, q.K, q.num_sms, beta_read);
+        const double t_dp = model_time(c, q.M, q.N, q.K, S, q.num_sms, beta_read);
+        if (t_sk < INFINITY && (ov.force_streamk == 1 || t_sk < 0.99 * t_dp)) {
             const long long slots = static_cast<long long>(q.num_sms) * c.ctas_per_sm;
-            const long long tiles = units;
+            const long long tiles = static_cast<long long>(out->tiles_m) * out->tiles_n;
             const long long n_full = (ceil_div(tiles, slots) - 1) * slots;
-            out->tail_tiles = static_cast<int>(tiles - n_full);
-            out->tail_splits = st;
-            const long long u2 = n_full + static_cast<long long>(out->tail_tiles) * st;
-            if (u2 > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
-            out->units = static_cast<int>(u2);
-            out->grid = static_cast<int>(std::min<long long>(u2, slots));
+            const long long span = (tiles - n_full) * ceil_div(q.K, sgemm_cfg::kFfmaBK);
+            out->splits = S = 1;
+            out->units = static_cast<int>(n_full);
+            out->sk_tiles = static_cast<int>(tiles - n_full);
+            // every slot runs the whole tiles; the span needs at most one CTA per k-block
+            out->grid = static_cast<int>(n_full > 0 ? slots : std::min(slots, span));
         }
     }
 
@@ -268,7 +267,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
 
     const Workspace w = workspace_layout(q, *out);
     out->workspace_bytes = w.total;
-    out->launches = 1 + out->transpose_a + out->repack_a + out->repack_b + (S > 1 || out->tail_splits > 1 ? 1 : 0);
+    out->launches = 1 + out->transpose_a + out->repack_a + out->repack_b + (S > 1 || out->sk_tiles > 0 ? 1 : 0);
     return SGEMM_OK;
 }
 
@@ -295,7 +294,11 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
         w.b_off = off;
         off += round_up(static_cast<long long>(q.K) * w.ldb * 4, 256);
     }
-    if (p.tail_splits > 1) {
+    if (p.sk_tiles > 0) {
+        // two partial tiles per CTA of the stream-K grid
+        w.w_off = off;
+        off += round_up(2LL * p.grid * p.bm * p.bn * 4, 256);
+    } else if (p.tail_splits > 1) {
         w.w_off = off;
         off += round_up(static_cast<long long>(p.tail_tiles) * p.tail_splits * p.bm * p.bn * 4, 256);
     } else if (p.splits > 1) {

@@ -22,13 +22,14 @@ struct Overrides {
     int force_config = -1;  // table row, -1 automatic
     int force_splits = 0;   // 0 automatic
     int force_transpose_a = -1;  // -1 automatic, 0 never, 1 always (FFMA kernel)
+    int force_streamk = -1;      // -1 automatic, 0 never, 1 whenever the last round is partial
 };
 
 // Offsets (bytes) into the handle's workspace and the strides used there.
 struct Workspace {
     long long a_off = 0, lda = 0;       // repacked A (M x lda, plan.repack_a) or A^T (K x lda, plan.transpose_a)
     long long b_off = 0, ldb = 0;       // repacked B (K x ldb), when plan.repack_b
-    long long w_off = 0, ldw = 0, wstride = 0;  // split-K partials (plan.splits > 1) or tail partials
+    long long w_off = 0, ldw = 0, wstride = 0;  // split-K, stream-K or TF32 tail-split partials
     long long total = 0;
 };
 

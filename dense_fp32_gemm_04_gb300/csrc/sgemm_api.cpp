@@ -122,10 +122,10 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
 {
     std::fprintf(stderr,
                  "[sgemm] M=%d N=%d K=%d kernel=%d config=%d tile=%dx%dx%d stages=%d splits=%d units=%d grid=%d "
-                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld tail=%dx%d\n",
+                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld tail=%dx%d sk_tiles=%d\n",
                  M, N, K, p.kernel, p.config, p.bm, p.bn, p.bk, p.stages, p.splits, p.units, p.grid, p.repack_a,
                  p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.tail_tiles,
-                 p.tail_splits);
+                 p.tail_splits, p.sk_tiles);
 }
 
 // TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop.
@@ -315,14 +315,15 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     p.timeout_ns = h->timeout_ns;
     p.inject_skip = h->inject_skip;
     p.skew_ns = h->skew_ns;
-    if (plan.tail_splits > 1) {
+    if (plan.sk_tiles > 0) {
         p.W = reinterpret_cast<float *>(ws + w.w_off);
-        p.n_full = plan.tiles_m * plan.tiles_n - plan.tail_tiles;
-        p.tail_splits = plan.tail_splits;
+        p.sk_tiles = plan.sk_tiles;
+        // the span is cut over at most one CTA per k-block (the rest only run whole tiles)
+        p.sk_grid = static_cast<int>(std::min<long long>(plan.grid, static_cast<long long>(plan.sk_tiles) * p.kblocks));
     }
     if (launch_ffma(plan.config, plan.transpose_a != 0, tmA, tmB, p, plan.grid, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
-    if (plan.tail_splits > 1 && launch_tail_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
+    if (plan.sk_tiles > 0 && launch_sk_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1) {
         if (launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
@@ -406,6 +407,10 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
     if (const char *ft = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
         const long v = std::strtol(ft, nullptr, 10);
         if (v >= -1 && v <= 1) h->ov.force_transpose_a = static_cast<int>(v);
+    }
+    if (const char *fk = std::getenv("SGEMM_FORCE_STREAMK")) {
+        const long v = std::strtol(fk, nullptr, 10);
+        if (v >= -1 && v <= 1) h->ov.force_streamk = static_cast<int>(v);
     }
     *out = h;
     return SGEMM_OK;
@@ -615,6 +620,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
     case SGEMM_OPT_FORCE_TRANSPOSE_A:
         if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
         h->ov.force_transpose_a = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_FORCE_STREAMK:
+        if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.force_streamk = static_cast<int>(value);
         return SGEMM_OK;
     default:
         return SGEMM_ERR_INVALID_VALUE;

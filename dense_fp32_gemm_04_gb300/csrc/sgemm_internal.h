@@ -31,16 +31,25 @@ struct FfmaParams {
     long long wstride;
     int splits;
     int tiles_m, tiles_n;
-    int units;         // tiles_m * tiles_n * splits
+    int units;         // tiles_m * tiles_n * splits, or the whole tiles before a stream-K region
     int kblocks;       // ceil(K / 32)
     int vec_c;         // C may be accessed with 16-byte vectors
     int *status;       // device status word (first error wins)
     long long timeout_ns;
     int inject_skip;   // test only: CTA 0's producer never fills its n-th stage (-1 off)
-    // Tail split (wave quantisation): when tail_splits > 1, units [0, n_full)
-    // are whole tiles written straight to C, and each remaining tile is split
-    // into tail_splits K slices whose partial tiles go, tile-packed, to
-    // W + ((tile - n_full) * tail_splits + slice) * BM * BN. `splits` is then 1.
+    // Stream-K region (FFMA kernel, sk_tiles > 0, splits == 1): after the
+    // `units` whole tiles, the last sk_tiles tiles of the raster form one span of
+    // S = sk_tiles * kblocks k-blocks cut evenly over the sk_grid CTAs: CTA g
+    // takes [g * S / G, (g + 1) * S / G). A tile inside one CTA's range is written
+    // to C; otherwise every CTA that covers part of it writes its partial tile,
+    // tile-packed, to W + slot * BM * BN with slot = 2g for the CTA's first tile
+    // and 2g + 1 for its last, and sk_reduce_kernel adds them in CTA (= k) order.
+    int sk_tiles;
+    int sk_grid;
+    // Tail split (TF32 kernel's tail reduction, tail_reduce_kernel): units
+    // [0, n_full) are whole tiles, each remaining tile is split into
+    // tail_splits K slices whose partial tiles go, tile-packed, to
+    // W + ((tile - n_full) * tail_splits + slice) * BM * BN.
     int n_full;
     int tail_splits;
     // Test only (race detection): > 0 delays the producer by this many ns before
@@ -79,6 +88,7 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
                                  int vec_c, int num_sms, cudaStream_t stream);
 cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
+cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
 cudaError_t launch_ladder(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta,
                           float *C, cudaStream_t stream);
 size_t min2_candidate_bytes(int blocks);

@@ -149,6 +149,7 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
     Overrides ov;
     ov.force_splits = splits;
     ov.force_transpose_a = 0;  // the scratch array holds split-K partials only
+    ov.force_streamk = 0;
     sgemm_plan_t plan;
     if ((rc = sgemm_impl::make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
     if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;

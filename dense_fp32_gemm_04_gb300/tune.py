@@ -96,8 +96,8 @@ def sweep(shapes, budget_flops=4e11, layout_only=False):
                "best": best, "auto_over_best": auto_ms / best["ms"], "status": st, "forced": rows,
                "a_as_given_ms": lay[0], "a_transposed_ms": lay[1]}
         results.append(rec)
-        print(f"{M:6d} {N:6d} {K:6d}  auto cfg {auto['config']} S {auto['splits']} tail {auto['tail_tiles']}x"
-              f"{auto['tail_splits']}: {auto_ms:8.3f} ms {rec['auto_tflops']:6.2f} TFLOP/s | best cfg {best['config']} "
+        print(f"{M:6d} {N:6d} {K:6d}  auto cfg {auto['config']} S {auto['splits']} sk {auto['sk_tiles']}"
+              f": {auto_ms:8.3f} ms {rec['auto_tflops']:6.2f} TFLOP/s | best cfg {best['config']} "
               f"S {best['splits']}: {best['ms']:8.3f} ms {best['tflops']:6.2f} | auto/best {rec['auto_over_best']:.3f}"
               f" | {lay_line}", flush=True)
     h.close()

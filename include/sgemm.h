@@ -82,19 +82,23 @@ typedef struct sgemm_plan_s {
     int ctas_per_sm;         /* resident CTAs per SM the grid is sized for */
     int splits;              /* split-K factor S (1 = fused epilogue) */
     int tiles_m, tiles_n;    /* output tiles */
-    int units;               /* work units: tiles_m * tiles_n * splits, or with a tail split the
-                                whole tiles plus tail_tiles * tail_splits K slices */
+    int units;               /* work units: tiles_m * tiles_n * splits; with stream-K the whole
+                                tiles before the stream-K span; TF32 tail split: whole tiles plus
+                                tail_tiles * tail_splits K slices */
     int grid;                /* CTAs launched (persistent: min(units, SMs * ctas_per_sm)) */
     int repack_a, repack_b;  /* operand first copied to a 16-byte-aligned workspace copy */
     int vec_c;               /* 1: C read/written with 16-byte accesses */
     int math_mode;           /* sgemm_math_mode_t */
     int launches;            /* kernels one sgemm_run launches for this plan */
     long long workspace_bytes; /* device workspace the handle holds for it */
-    int tail_tiles;          /* tiles of the last, partial round of the persistent grid that are
-                                split along K to even out the waves (0 = none) */
-    int tail_splits;         /* K slices per tail tile (their partials are reduced in order) */
+    int tail_tiles;          /* TF32 mode: tiles of the last, partial round of the persistent grid
+                                that are split along K to even out the waves (0 = none) */
+    int tail_splits;         /* TF32 mode: K slices per tail tile (partials reduced in order) */
     int transpose_a;         /* 1: A is first transposed into the workspace (K x M, M contiguous)
                                 and the FP32 mainloop reads A^T; 0: it reads A as given */
+    int sk_tiles;            /* FP32 mode, stream-K: the last sk_tiles tiles (after `units` whole
+                                tiles) form one span of k-blocks cut evenly over the grid's CTAs;
+                                tiles shared by two or more CTAs are reduced in k order (0 = none) */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */
@@ -109,8 +113,10 @@ typedef enum sgemm_option {
     SGEMM_OPT_SKEW_NS = 6,        /* TEST ONLY (race detection): > 0 delays the FP32 kernel's copy
                                      issue by this many ns per k-slab, < 0 delays every compute warp
                                      before it releases a slab; |value| <= 100000, 0 = off */
-    SGEMM_OPT_FORCE_TRANSPOSE_A = 7 /* FP32 path: -1 = automatic (the default), 0 = read A as given,
+    SGEMM_OPT_FORCE_TRANSPOSE_A = 7,/* FP32 path: -1 = automatic (the default), 0 = read A as given,
                                      1 = always transpose A first (same results either way) */
+    SGEMM_OPT_FORCE_STREAMK = 8   /* FP32 path: -1 = automatic (the default), 0 = never, 1 = whenever
+                                     the last round of tiles is partial (ignored with forced splits) */
 } sgemm_option_t;
 
 /*
@@ -123,8 +129,8 @@ typedef enum sgemm_option {
  * sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
- * SGEMM_FORCE_SPLITS=<S> and SGEMM_FORCE_TRANSPOSE_A=<-1|0|1> preset the
- * planner overrides of sgemm_set_option.
+ * SGEMM_FORCE_SPLITS=<S>, SGEMM_FORCE_TRANSPOSE_A=<-1|0|1> and
+ * SGEMM_FORCE_STREAMK=<-1|0|1> preset the planner overrides of sgemm_set_option.
  */
 int sgemm_create(sgemm_handle_t *out);
 

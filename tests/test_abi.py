@@ -78,22 +78,22 @@ def test_plan_square_4096(lib):
     assert p.kernel == sg.KERNEL_FFMA and p.splits == 1
     assert p.repack_a == 0 and p.repack_b == 0 and p.vec_c == 1
     assert p.grid <= 152 * p.ctas_per_sm
-    # 1024 tiles on 152 CTAs: 6 whole rounds, then the 112 remaining tiles are
-    # split along K so the last round is shared by every CTA
+    # 1024 tiles on 152 CTAs: 6 whole rounds, then the 112 remaining tiles form
+    # one stream-K span of 112 * 128 k-blocks shared evenly by every CTA
     tiles = p.tiles_m * p.tiles_n
     slots = 152 * p.ctas_per_sm
-    assert p.tail_tiles == tiles - (tiles // slots) * slots == 112
-    assert p.tail_splits > 1
-    assert p.units == tiles - p.tail_tiles + p.tail_tiles * p.tail_splits
-    # A is transposed first (A^T mainloop): transpose + mainloop + tail reduce
+    assert p.sk_tiles == tiles - (tiles // slots) * slots == 112
+    assert p.units == tiles - p.sk_tiles == 912 and p.grid == 152
+    assert p.tail_tiles == 0 and p.tail_splits == 0
+    # A is transposed first (A^T mainloop): transpose + mainloop + stream-K reduction
     assert p.transpose_a == 1 and p.launches == 3
-    assert p.workspace_bytes >= p.tail_tiles * p.tail_splits * p.bm * p.bn * 4 + 4096 * 4096 * 4
+    assert p.workspace_bytes >= 2 * 152 * p.bm * p.bn * 4 + 4096 * 4096 * 4
 
 
 def test_plan_full_rounds_have_no_tail(lib):
     # 8192^3: 4096 tiles -> 26.9 rounds, the last one 94 % full: not worth splitting
     p = sg.plan(8192, 8192, 8192, num_sms=152)
-    assert p.tail_tiles == 0 and p.units == p.tiles_m * p.tiles_n
+    assert p.sk_tiles == 0 and p.units == p.tiles_m * p.tiles_n
     assert p.transpose_a == 1 and p.launches == 2
 
 
@@ -103,7 +103,7 @@ def test_plan_ragged_unaligned_repacks(lib):
     # aligned workspace copy, and C is accessed with scalar loads and stores.
     p = sg.plan(2047, 3001, 1531, lda=1531, ldb=3001, ldc=3001)
     assert p.transpose_a == 1 and p.repack_a == 0 and p.repack_b == 1 and p.vec_c == 0
-    assert p.launches == 3 + (1 if (p.splits > 1 or p.tail_splits > 1) else 0)
+    assert p.launches == 3 + (1 if (p.splits > 1 or p.sk_tiles > 0) else 0)
     assert p.workspace_bytes >= 4 * (1531 * 2048 + 1531 * 3004)
     # Without the transposition (small N) an unaligned A is repacked instead.
     q = sg.plan(20000, 16, 1531, lda=1531, ldb=16, ldc=16)
@@ -115,13 +115,18 @@ def test_plan_misaligned_pointer_repacks(lib):
     assert p.transpose_a == 0 and p.repack_a == 1 and p.repack_b == 0
 
 
-def test_plan_skinny_uses_split_k(lib):
+def test_plan_skinny_shares_k(lib):
     for M, N in ((16384, 64), (64, 16384)):
         p = sg.plan(M, N, 8192, num_sms=152)
         assert p.kernel == sg.KERNEL_FFMA
-        assert p.splits > 1, p.as_dict()
-        assert p.units >= 152
-        assert p.workspace_bytes >= p.splits * M * N * 4
+        # fewer tiles than CTAs: K is shared, by split-K or by one stream-K span
+        tiles = p.tiles_m * p.tiles_n
+        if p.sk_tiles:
+            assert p.splits == 1 and p.sk_tiles == tiles and p.units == 0 and p.grid == 152 * p.ctas_per_sm
+            assert p.workspace_bytes >= 2 * p.grid * p.bm * p.bn * 4
+        else:
+            assert p.splits > 1 and p.units >= 152, p.as_dict()
+            assert p.workspace_bytes >= p.splits * M * N * 4
         # transposing a 16384 x 8192 A costs more than it saves; a 64 x 8192 A is cheap
         assert p.transpose_a == (1 if M == 64 else 0)
 
@@ -155,23 +160,24 @@ def test_plan_invariants_random_shapes(lib):
         kb = -(-K // 32)
         assert 1 <= p.splits <= min(kb, 16)
         slots = sms * p.ctas_per_sm
-        if p.tail_splits > 1:
-            assert p.splits == 1 and 0 < p.tail_tiles < slots
-            assert (tiles - p.tail_tiles) % slots == 0
-            assert p.units == tiles - p.tail_tiles + p.tail_tiles * p.tail_splits
-            assert p.workspace_bytes >= p.tail_tiles * p.tail_splits * p.bm * p.bn * 4
+        assert p.tail_tiles == 0 and p.tail_splits == 0  # the TF32 mode's tail split
+        if p.sk_tiles > 0:
+            assert p.splits == 1 and 0 < p.sk_tiles < slots
+            assert p.units == tiles - p.sk_tiles and p.units % slots == 0
+            assert p.grid == (slots if p.units > 0 else min(slots, p.sk_tiles * kb))
+            assert p.workspace_bytes >= 2 * p.grid * p.bm * p.bn * 4
         else:
-            assert p.tail_tiles == 0 and p.units == tiles * p.splits
+            assert p.units == tiles * p.splits
             if p.splits > 1:
                 assert p.workspace_bytes >= p.splits * M * (-(-N // 4) * 4) * 4
-        assert 1 <= p.grid <= min(p.units, slots)
+        assert 1 <= p.grid <= (slots if p.sk_tiles else min(p.units, slots))
         assert p.transpose_a in (0, 1)
         assert p.repack_a == (0 if (p.transpose_a or (align & 1 and lda % 4 == 0)) else 1)
         assert p.repack_b == (0 if (align & 2 and ldb % 4 == 0) else 1)
         assert p.vec_c == (1 if (align & 4 and ldc % 4 == 0) else 0)
         if p.transpose_a:
             assert p.workspace_bytes >= K * (-(-M // 4) * 4) * 4
-        extra = 1 if (p.splits > 1 or p.tail_splits > 1) else 0
+        extra = 1 if (p.splits > 1 or p.sk_tiles > 0) else 0
         assert p.launches == 1 + p.transpose_a + p.repack_a + p.repack_b + extra
 
 

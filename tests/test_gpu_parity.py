@@ -242,31 +242,50 @@ def test_skinny(h, name):
     p, A, B, C = _problem(name)
     got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
     assert st == sg.SGEMM_OK and guards
-    assert h.last_plan().splits > 1
+    plan = h.last_plan()
+    assert plan.splits > 1 or plan.sk_tiles > 0  # K shared: split-K or stream-K
     rows = sample_rows(p["M"]) if p["M"] > 4096 else None
     check_against_oracle(got, A, B, C, p["alpha"], p["beta"], rows=rows)
 
 
-@pytest.mark.parametrize("shape", [(1000, 2500, 513), (1999, 3001, 1031), (1500, 4095, 2050)])
+@pytest.mark.parametrize("shape", [(1000, 2500, 513), (1999, 3001, 1031), (1500, 4095, 2050), (1024, 1024, 1024),
+                                   (300, 260, 777), (129, 127, 95)])
 @pytest.mark.parametrize("ta", [0, 1])
-def test_tail_split(h, shape, ta):
-    """Shapes whose last round is split along K (tail split): exact on integers, bound on reals."""
+def test_stream_k(h, shape, ta):
+    """Stream-K: the tiles of the last, partial round share one span of k-blocks cut
+    evenly over the CTAs (whole tiles before it; for small problems the span is all
+    of them). Exact on integers, bound on reals, bitwise repeatable."""
     h.set_option(sg.OPT_FORCE_TRANSPOSE_A, ta)
+    h.set_option(sg.OPT_FORCE_STREAMK, 1)
     try:
-        _tail_split_case(h, shape)
+        _stream_k_case(h, shape)
         assert h.last_plan().transpose_a == ta
     finally:
         h.set_option(sg.OPT_FORCE_TRANSPOSE_A, -1)
+        h.set_option(sg.OPT_FORCE_STREAMK, -1)
 
 
-def _tail_split_case(h, shape):
+@pytest.mark.parametrize("cfg", range(4))
+def test_stream_k_every_config(h, cfg):
+    """Each tile-config row (1-3 CTAs per SM) with a stream-K span."""
+    force(h, config=cfg)
+    h.set_option(sg.OPT_FORCE_STREAMK, 1)
+    try:
+        for shape in [(700, 900, 1500), (65, 4000, 333)]:
+            _stream_k_case(h, shape)
+            assert h.last_plan().config == cfg
+    finally:
+        force(h)
+        h.set_option(sg.OPT_FORCE_STREAMK, -1)
+
+
+def _stream_k_case(h, shape):
     M, N, K = shape
     A, B, C = ops(M, N, K, seed=M + N, dist=("int", "int", "int"))
     got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
     assert st == sg.SGEMM_OK and guards
     plan = h.last_plan()
-    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert plan.tail_splits > 1 and plan.tail_tiles > 0, plan.as_dict()
+    assert plan.sk_tiles > 0 and plan.splits == 1, plan.as_dict()
     check_against_oracle(got, A, B, C, 1.5, 0.5, exact=True)
     Ar, Br, Cr = ops(M, N, K, seed=M + N + 1, dist=("normal", "uniform", "uniform"))
     got, guards, st = run_gemm(torch, h, Ar, Br, Cr, -1.0, 0.25)
@@ -274,6 +293,7 @@ def _tail_split_case(h, shape):
     check_against_oracle(got, Ar, Br, Cr, -1.0, 0.25)
     r2, _, _ = run_gemm(torch, h, Ar, Br, Cr, -1.0, 0.25)
     assert np.array_equal(got.view(np.uint32), r2.view(np.uint32))
+    assert h.check_device_status() == (sg.SGEMM_OK, 0)
 
 
 def test_run_host_pipelined_panels(h):
