@@ -51,6 +51,7 @@
 #include <type_traits>
 
 #include "device_ptx.cuh"
+#include "schedule.cuh"
 #include "sgemm_internal.h"
 
 namespace sgemm_impl {
@@ -60,7 +61,6 @@ using namespace sgemm_dev;
 using sgemm_cfg::kFfmaBK;
 
 constexpr int kTimeoutCode = 5 << 16;  // SGEMM_ERR_TIMEOUT << 16
-constexpr int kGroupM = 8;             // tile rows per raster group (L2 reuse of B)
 
 template <int BM_, int BN_, int STAGES_, int MINB_>
 struct Tile {
@@ -77,74 +77,6 @@ struct Tile {
     static_assert(BM <= 256 && BN <= 256, "a TMA box side is at most 256 elements");
     static_assert(A_BYTES % 1024 == 0, "A stages must keep the 1024-byte swizzle alignment");
 };
-
-// Tile index t -> (tile row, tile column): tiles run in groups of kGroupM
-// tile rows, column by column, so concurrently running CTAs share B columns
-// and A rows in L2.
-__device__ __forceinline__ void decode_tile(int tiles_m, int tiles_n, int t, int &tm, int &tn)
-{
-    const int per_group = kGroupM * tiles_n;
-    const int g = t / per_group;
-    const int first_m = g * kGroupM;
-    const int gsize = min(tiles_m - first_m, kGroupM);
-    const int r = t - g * per_group;
-    tm = first_m + r % gsize;
-    tn = r / gsize;
-}
-
-// First k-block of slice ks of nsplit (balanced integer split of kblocks).
-__device__ __forceinline__ int split_begin(const FfmaParams &p, int ks, int nsplit)
-{
-    return static_cast<int>((static_cast<long long>(ks) * p.kblocks) / nsplit);
-}
-
-// One piece of a CTA's work: tile t (tm, tn), k-blocks [kb0, kb1), and where
-// its result goes (kToC: alpha/beta into C; kToSplit: split-K slice idx;
-// kToPartial: stream-K partial tile slot idx).
-enum : int { kToC = 0, kToSplit = 1, kToPartial = 2 };
-struct Work {
-    int t, tm, tn, kb0, kb1, dest, idx;
-};
-
-// Item i of this CTA's work: first its units (u = blockIdx.x + i * gridDim.x),
-// then the pieces of its stream-K range, one per tile the range touches.
-// Computed from i alone, so that only i stays live across the mainloop;
-// producer and consumers walk the same sequence. Returns false past the end.
-__device__ __forceinline__ bool work_at(const FfmaParams &p, int i, Work &w)
-{
-    const int g = blockIdx.x, G = gridDim.x;
-    const int n_units = g < p.units ? (p.units - g + G - 1) / G : 0;
-    if (i < n_units) {
-        const int u = g + i * G;
-        const int ks = u % p.splits;
-        w.t = u / p.splits;
-        decode_tile(p.tiles_m, p.tiles_n, w.t, w.tm, w.tn);
-        w.kb0 = split_begin(p, ks, p.splits);
-        w.kb1 = split_begin(p, ks + 1, p.splits);
-        w.dest = p.splits > 1 ? kToSplit : kToC;
-        w.idx = ks;
-        return true;
-    }
-    if (p.sk_tiles <= 0 || g >= p.sk_grid) return false;
-    const long long S = static_cast<long long>(p.sk_tiles) * p.kblocks;
-    const long long b0 = static_cast<long long>(g) * S / p.sk_grid;
-    const long long b1 = static_cast<long long>(g + 1) * S / p.sk_grid;
-    const int j = i - n_units;
-    const long long first_rel = b0 / p.kblocks;
-    const long long rel = first_rel + j;
-    const long long tile_start = rel * p.kblocks;
-    const long long seg0 = j == 0 ? b0 : tile_start;
-    if (seg0 >= b1) return false;
-    const long long seg1 = b1 < tile_start + p.kblocks ? b1 : tile_start + p.kblocks;
-    w.t = p.units + static_cast<int>(rel);
-    decode_tile(p.tiles_m, p.tiles_n, w.t, w.tm, w.tn);
-    w.kb0 = static_cast<int>(seg0 - tile_start);
-    w.kb1 = static_cast<int>(seg1 - tile_start);
-    // a tile inside this CTA's range needs no partial
-    w.dest = (w.kb0 == 0 && w.kb1 == p.kblocks) ? kToC : kToPartial;
-    w.idx = 2 * g + (j == 0 ? 0 : 1);
-    return true;
-}
 
 template <class T, bool AT>
 __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUtensorMap *tmB,
@@ -550,78 +482,55 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, long long ldw,
     }
 }
 
-// Tail-split reduction: for every tail tile, C = alpha * sum_s P_s + beta * C
-// with its tail_splits partial tiles added in slice order. One thread per 4
-// consecutive columns of a tile row.
-__global__ void tail_reduce_kernel(const FfmaParams p, int bm, int bn)
-{
-    const int n_tail = p.tiles_m * p.tiles_n - p.n_full;
-    const int q4 = bn / 4;
-    const long long per_tile = static_cast<long long>(bm) * q4;
-    const long long total = per_tile * n_tail;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int q = static_cast<int>(idx / per_tile);
-        const int e = static_cast<int>(idx - static_cast<long long>(q) * per_tile);
-        const int lr = e / q4, lc = (e - lr * q4) * 4;
-        int tm, tn;
-        decode_tile(p.tiles_m, p.tiles_n, p.n_full + q, tm, tn);
-        const int row = tm * bm + lr, col = tn * bn + lc;
-        if (row >= p.M || col >= p.N) continue;
-        const float *w = p.W + static_cast<long long>(q) * p.tail_splits * bm * bn + lr * bn + lc;
-        float4 s = *reinterpret_cast<const float4 *>(w);
-        for (int k = 1; k < p.tail_splits; ++k) {
-            const float4 t = *reinterpret_cast<const float4 *>(w + static_cast<long long>(k) * bm * bn);
-            s.x += t.x;
-            s.y += t.y;
-            s.z += t.z;
-            s.w += t.w;
-        }
-        store_c4(p, row, col, s);
-    }
-}
+// Stream-K reduction (schedule.cuh): for every span tile covered by more than
+// one CTA, C = alpha * sum_g P_g + beta * C with the partial tiles of the
+// covering CTAs added in CTA order, which is k order. Serves the FFMA and the
+// TF32 kernels (same raster, same partial-tile layout). Grid: blockIdx.y = span
+// tile, blockIdx.x = 256 column quads of it, one per thread; each block works
+// out the covering CTAs' partial-tile offsets once, in shared memory.
+constexpr int kSkMaxShared = 64;  // covering CTAs whose offsets are kept in shared memory
 
-// Stream-K reduction: for every stream-K tile covered by more than one CTA,
-// C = alpha * sum_g P_g + beta * C with the partial tiles of the covering CTAs
-// added in CTA order, which is k order (see FfmaParams: CTA g covers k-blocks
-// [g S / G, (g + 1) S / G) of the span; the tile's first k-block lies in CTA
-// ((start + 1) G - 1) / S, its last in ((start + kblocks) G - 1) / S).
 __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int bm, int bn)
 {
+    __shared__ long long off[kSkMaxShared];
     const long long S = static_cast<long long>(p.sk_tiles) * p.kblocks;
     const long long G = p.sk_grid;
-    const int q4 = bn / 4;
-    const long long per_tile = static_cast<long long>(bm) * q4;
-    const long long total = per_tile * p.sk_tiles;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int rel = static_cast<int>(idx / per_tile);
-        const int e = static_cast<int>(idx - static_cast<long long>(rel) * per_tile);
-        const int lr = e / q4, lc = (e - lr * q4) * 4;
-        const long long start = static_cast<long long>(rel) * p.kblocks;
-        const long long g0 = ((start + 1) * G - 1) / S;
-        const long long g1 = ((start + p.kblocks) * G - 1) / S;
-        if (g0 == g1) continue;  // inside one CTA's range: written to C by the mainloop
-        int tm, tn;
-        decode_tile(p.tiles_m, p.tiles_n, p.units + rel, tm, tn);
-        const int row = tm * bm + lr, col = tn * bn + lc;
-        if (row >= p.M || col >= p.N) continue;
-        float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (long long g = g0; g <= g1; ++g) {
-            const long long first = (g * S / G) / p.kblocks;  // CTA g's first stream-K tile
-            const long long slot = 2 * g + (rel == first ? 0 : 1);
-            const float4 v = *reinterpret_cast<const float4 *>(p.W + slot * bm * bn + lr * bn + lc);
-            if (g == g0) {
-                s = v;
-            } else {
-                s.x += v.x;
-                s.y += v.y;
-                s.z += v.z;
-                s.w += v.w;
-            }
-        }
-        store_c4(p, row, col, s);
+    const int rel = blockIdx.y;
+    const long long start = static_cast<long long>(rel) * p.kblocks;
+    const long long g0 = ((start + 1) * G - 1) / S;
+    const long long g1 = ((start + p.kblocks) * G - 1) / S;
+    if (g0 == g1) return;  // inside one CTA's range: written to C by the mainloop (whole block)
+    const int nseg = static_cast<int>(g1 - g0 + 1);
+    for (int j = threadIdx.x; j < nseg && j < kSkMaxShared; j += blockDim.x) {
+        const long long g = g0 + j;
+        off[j] = (2 * g + (rel == (g * S / G) / p.kblocks ? 0 : 1)) * bm * bn;  // slot of CTA g
     }
+    __syncthreads();
+    const int q4 = bn / 4;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= bm * q4) return;
+    int tm, tn;
+    decode_tile(p.tiles_m, p.tiles_n, p.units + rel, tm, tn);
+    const int lr = e / q4, lc = (e - lr * q4) * 4;
+    const int row = tm * bm + lr, col = tn * bn + lc;
+    if (row >= p.M || col >= p.N) return;
+    const float *w = p.W + lr * bn + lc;
+    float4 s = *reinterpret_cast<const float4 *>(w + off[0]);
+    for (int j = 1; j < nseg; ++j) {
+        long long o;
+        if (j < kSkMaxShared) {
+            o = off[j];
+        } else {
+            const long long g = g0 + j;
+            o = (2 * g + (rel == (g * S / G) / p.kblocks ? 0 : 1)) * bm * bn;
+        }
+        const float4 v = *reinterpret_cast<const float4 *>(w + o);
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+    }
+    store_c4(p, row, col, s);
 }
 
 // C = beta * C for K == 0 or alpha == 0 (beta == 0 writes +0 without reading C).
@@ -740,17 +649,11 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
     return cudaGetLastError();
 }
 
-cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)
-{
-    const long long work = static_cast<long long>(p.tiles_m * p.tiles_n - p.n_full) * bm * (bn / 4);
-    tail_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(p, bm, bn);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)
 {
-    const long long work = static_cast<long long>(p.sk_tiles) * bm * (bn / 4);
-    sk_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(p, bm, bn);
+    (void)num_sms;
+    const dim3 grid((bm * (bn / 4) + 255) / 256, p.sk_tiles);  // sk_tiles < SMs * CTAs per SM
+    sk_reduce_kernel<<<grid, 256, 0, stream>>>(p, bm, bn);
     return cudaGetLastError();
 }
 

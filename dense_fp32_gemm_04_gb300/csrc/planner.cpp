@@ -74,9 +74,13 @@ bool transpose_pays(const Problem &q, double t_main)
     return t_copy < kAtGain * t_main;
 }
 
-// Tail split of the TF32 mode (one 128 x 256 tile per SM per round): the last,
-// partial round's tiles are cut into St K slices (St <= 8, at least one 32-deep
-// block each) when the modelled time saved exceeds the partial-tile reduction.
+// Stream-K span of the TF32 mode (one 128 x 256 tile per SM per round), cut into
+// equal K slices: the span's rem tiles go to rem * St CTAs, so that every CTA
+// range is slice s of one tile (k-blocks [s kb / St, (s + 1) kb / St)) and each
+// writes one partial tile. St <= 8 with at least one 32-deep block per slice,
+// chosen when the modelled time saved exceeds the partial-tile reduction. (A span
+// spread over all CTAs, as on the FP32 path, gives two partials per CTA: the
+// TF32 epilogue writes those slower than it saves, 4096^3 219 -> 237 us.)
 // Rates: the mainloop's measured ~650 TFLOP/s, ~5.5 TB/s for the reduction.
 int choose_tail_tf32(int M, int N, int K, int num_sms, bool beta_read)
 {
@@ -205,21 +209,23 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         if (units > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
         out->units = static_cast<int>(units);
         out->grid = static_cast<int>(std::min<long long>(units, q.num_sms));
-        if (ov.force_splits == 0) {
-            const int st = choose_tail_tf32(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
-            if (st > 1) {
-                const long long slots = q.num_sms;
-                const long long n_full = (ceil_div(units, slots) - 1) * slots;
-                out->tail_tiles = static_cast<int>(units - n_full);
-                out->tail_splits = st;
-                const long long u2 = n_full + static_cast<long long>(out->tail_tiles) * st;
-                if (u2 > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
-                out->units = static_cast<int>(u2);
-                out->grid = static_cast<int>(std::min<long long>(u2, slots));
+        if (ov.force_splits == 0 && ov.force_streamk != 0) {
+            const long long slots = q.num_sms;
+            const long long n_full = (ceil_div(units, slots) - 1) * slots;
+            const long long rem = units - n_full;
+            const long long kb = ceil_div(q.K, sgemm_cfg::kTf32BK);
+            long long st = choose_tail_tf32(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
+            if (st < 2 && ov.force_streamk == 1) st = std::min(kb, slots / rem);  // forced: fill the idle CTAs
+            st = std::min(st, slots / rem);  // one slice per CTA: rem * st CTAs at most `slots`
+            if (st >= 2 && rem < slots) {
+                out->units = static_cast<int>(n_full);
+                out->sk_tiles = static_cast<int>(rem);
+                out->sk_grid = static_cast<int>(rem * st);
+                out->grid = static_cast<int>(n_full > 0 ? slots : std::min(slots, rem * st));
             }
         }
         out->workspace_bytes = workspace_layout(q, *out).total;
-        out->launches = 1 + out->repack_a + 1 + (out->tail_splits > 1 ? 1 : 0);
+        out->launches = 1 + out->repack_a + 1 + (out->sk_tiles > 0 ? 1 : 0);
         return SGEMM_OK;
     }
 
@@ -254,6 +260,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
             out->sk_tiles = static_cast<int>(tiles - n_full);
             // every slot runs the whole tiles; the span needs at most one CTA per k-block
             out->grid = static_cast<int>(n_full > 0 ? slots : std::min(slots, span));
+            out->sk_grid = static_cast<int>(std::min(slots, span));
         }
     }
 
@@ -298,9 +305,6 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
         // two partial tiles per CTA of the stream-K grid
         w.w_off = off;
         off += round_up(2LL * p.grid * p.bm * p.bn * 4, 256);
-    } else if (p.tail_splits > 1) {
-        w.w_off = off;
-        off += round_up(static_cast<long long>(p.tail_tiles) * p.tail_splits * p.bm * p.bn * 4, 256);
     } else if (p.splits > 1) {
         w.ldw = round_up(q.N, 4);
         w.wstride = static_cast<long long>(q.M) * w.ldw;

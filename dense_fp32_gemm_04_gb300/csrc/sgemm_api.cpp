@@ -122,10 +122,9 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
 {
     std::fprintf(stderr,
                  "[sgemm] M=%d N=%d K=%d kernel=%d config=%d tile=%dx%dx%d stages=%d splits=%d units=%d grid=%d "
-                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld tail=%dx%d sk_tiles=%d\n",
+                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld sk_tiles=%d\n",
                  M, N, K, p.kernel, p.config, p.bm, p.bn, p.bk, p.stages, p.splits, p.units, p.grid, p.repack_a,
-                 p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.tail_tiles,
-                 p.tail_splits, p.sk_tiles);
+                 p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.sk_tiles);
 }
 
 // TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop.
@@ -166,14 +165,15 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     p.vec_c = plan.vec_c;
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
-    if (plan.tail_splits > 1) {
+    p.splits = 1;
+    if (plan.sk_tiles > 0) {
         p.W = reinterpret_cast<float *>(ws + w.w_off);
-        p.n_full = plan.tiles_m * plan.tiles_n - plan.tail_tiles;
-        p.tail_splits = plan.tail_splits;
+        p.sk_tiles = plan.sk_tiles;
+        p.sk_grid = plan.sk_grid;
     }
     if (launch_tf32(tmA, tmBt, p, plan.grid, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    if (plan.tail_splits > 1) {
-        // Same tile-packed partial layout and tile raster as the FP32 tail split.
+    if (plan.sk_tiles > 0) {
+        // Same raster and tile-packed partial layout as the FP32 stream-K span.
         FfmaParams r{};
         r.M = M;
         r.N = N;
@@ -184,10 +184,13 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         r.W = p.W;
         r.tiles_m = plan.tiles_m;
         r.tiles_n = plan.tiles_n;
+        r.units = p.units;
+        r.splits = 1;
+        r.kblocks = p.kblocks;
         r.vec_c = plan.vec_c;
-        r.n_full = p.n_full;
-        r.tail_splits = p.tail_splits;
-        if (launch_tail_reduce(r, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        r.sk_tiles = p.sk_tiles;
+        r.sk_grid = p.sk_grid;
+        if (launch_sk_reduce(r, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
     }
     return SGEMM_OK;
 }
@@ -318,8 +321,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     if (plan.sk_tiles > 0) {
         p.W = reinterpret_cast<float *>(ws + w.w_off);
         p.sk_tiles = plan.sk_tiles;
-        // the span is cut over at most one CTA per k-block (the rest only run whole tiles)
-        p.sk_grid = static_cast<int>(std::min<long long>(plan.grid, static_cast<long long>(plan.sk_tiles) * p.kblocks));
+        p.sk_grid = plan.sk_grid;
     }
     if (launch_ffma(plan.config, plan.transpose_a != 0, tmA, tmB, p, plan.grid, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;

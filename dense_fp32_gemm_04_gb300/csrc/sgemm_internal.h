@@ -37,21 +37,12 @@ struct FfmaParams {
     int *status;       // device status word (first error wins)
     long long timeout_ns;
     int inject_skip;   // test only: CTA 0's producer never fills its n-th stage (-1 off)
-    // Stream-K region (FFMA kernel, sk_tiles > 0, splits == 1): after the
-    // `units` whole tiles, the last sk_tiles tiles of the raster form one span of
-    // S = sk_tiles * kblocks k-blocks cut evenly over the sk_grid CTAs: CTA g
-    // takes [g * S / G, (g + 1) * S / G). A tile inside one CTA's range is written
-    // to C; otherwise every CTA that covers part of it writes its partial tile,
-    // tile-packed, to W + slot * BM * BN with slot = 2g for the CTA's first tile
-    // and 2g + 1 for its last, and sk_reduce_kernel adds them in CTA (= k) order.
+    // Stream-K span (schedule.cuh; sk_tiles > 0 needs splits == 1): after the
+    // `units` whole tiles, the last sk_tiles tiles of the raster are cut evenly
+    // over sk_grid CTAs by k-block; partial tiles go, tile-packed, to
+    // W + slot * BM * BN and sk_reduce_kernel adds them in k order.
     int sk_tiles;
     int sk_grid;
-    // Tail split (TF32 kernel's tail reduction, tail_reduce_kernel): units
-    // [0, n_full) are whole tiles, each remaining tile is split into
-    // tail_splits K slices whose partial tiles go, tile-packed, to
-    // W + ((tile - n_full) * tail_splits + slice) * BM * BN.
-    int n_full;
-    int tail_splits;
     // Test only (race detection): > 0 delays the producer by this many ns before
     // every fill, < 0 delays every consumer warp before it releases a slab.
     int skew_ns;
@@ -65,17 +56,16 @@ struct Tf32Params {
     float *C;
     long long ldc;
     int tiles_m, tiles_n;
-    int units;         // tiles_m * tiles_n
+    int units;         // whole tiles (before a stream-K span)
+    int splits;        // always 1 (schedule.cuh interface)
     int kblocks;       // ceil(K / 32)
     int vec_c;
     int *status;
     long long timeout_ns;
-    // Tail split, as in FfmaParams: units [0, n_full) are whole tiles, the
-    // rest are tail_splits K slices of the remaining tiles whose partial tiles
-    // go, tile-packed, to W + ((tile - n_full) * tail_splits + slice) * BM * BN.
+    // Stream-K span, as in FfmaParams (partials at W + slot * BM * BN).
     float *W;
-    int n_full;
-    int tail_splits;  // <= 1: no tail split
+    int sk_tiles;
+    int sk_grid;
 };
 
 // Plain-launch helpers implemented in the .cu files. All return the CUDA
@@ -87,7 +77,6 @@ cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
                                  int vec_c, int num_sms, cudaStream_t stream);
-cudaError_t launch_tail_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
 cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
 cudaError_t launch_ladder(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta,
                           float *C, cudaStream_t stream);

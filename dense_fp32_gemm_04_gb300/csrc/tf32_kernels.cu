@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "device_ptx.cuh"
+#include "schedule.cuh"
 #include "sgemm_internal.h"
 
 namespace sgemm_impl {
@@ -42,7 +43,6 @@ constexpr int THREADS = sgemm_cfg::kTf32Threads;
 constexpr int MMA_K = 8;                  // K of one tcgen05.mma .kind::tf32
 constexpr uint32_t TMEM_COLS = 2 * BN;    // two accumulators
 constexpr uint32_t IDESC = idesc_tf32(BM, BN);
-constexpr int kGroupM = 8;
 static_assert(sgemm_cfg::tf32_smem_bytes() == 1024 + STAGES * STAGE_BYTES + 256, "smem layout");
 static_assert(TMEM_COLS == 512, "two 128 x 256 FP32 accumulators fill TMEM");
 
@@ -57,37 +57,6 @@ struct Bars {
     int issued[STAGES];
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
-
-__device__ __forceinline__ void decode_tile(const Tf32Params &p, int u, int &tm, int &tn)
-{
-    const int per_group = kGroupM * p.tiles_n;
-    const int g = u / per_group;
-    const int first_m = g * kGroupM;
-    const int gsize = min(p.tiles_m - first_m, kGroupM);
-    const int r = u - g * per_group;
-    tm = first_m + r % gsize;
-    tn = r / gsize;
-}
-
-// Work unit u -> tile t (grouped raster), K-block range [kb0, kb1), slice ks
-// of ns (ns == 1: the whole tile).
-__device__ __forceinline__ void decode_unit(const Tf32Params &p, int u, int &t, int &tm, int &tn, int &ks, int &ns,
-                                            int &kb0, int &kb1)
-{
-    if (p.tail_splits > 1 && u >= p.n_full) {
-        const int v = u - p.n_full;
-        t = p.n_full + v / p.tail_splits;
-        ks = v % p.tail_splits;
-        ns = p.tail_splits;
-    } else {
-        t = u;
-        ks = 0;
-        ns = 1;
-    }
-    decode_tile(p, t, tm, tn);
-    kb0 = static_cast<int>((static_cast<long long>(ks) * p.kblocks) / ns);
-    kb1 = static_cast<int>((static_cast<long long>(ks + 1) * p.kblocks) / ns);
-}
 
 __device__ __forceinline__ void raise_abort(Bars *b, const Tf32Params &p, int where)
 {
@@ -116,7 +85,7 @@ __device__ __forceinline__ void load_row_chunks(uint32_t t_col, uint32_t (&v)[NB
     for (int j = 0; j < NB; ++j) tmem_wait_ld(v[j]);
 }
 
-// Raw partial row of a tail slice (tile-packed workspace row of BN floats).
+// Raw partial row of a stream-K piece (tile-packed workspace row of BN floats).
 template <int NB>
 __device__ __forceinline__ void store_partial_row(uint32_t t_row, float *wrow)
 {
@@ -222,10 +191,10 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-            int t, tm, tn, ks, ns, kb0, kb1;
-            decode_unit(p, u, t, tm, tn, ks, ns, kb0, kb1);
-            for (int kb = kb0; kb < kb1; ++kb) {
+        Work w;
+        for (int item = 0; ok && work_at(p, item, w); ++item) {
+            const int tm = w.tm, tn = w.tn;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 const uint32_t full = smem_addr(&bars->full[stage]);
                 if (!mbar_wait_bounded(smem_addr(&bars->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
                     raise_abort(bars, p, kWhereProducerEmpty);
@@ -254,7 +223,8 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t phase = 0;
         int it = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++it) {
+        Work w;
+        for (int item = 0; ok && work_at(p, item, w); ++item, ++it) {
             const int buf = it & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
             if (!mbar_wait_bounded(smem_addr(&bars->acc_empty[buf]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -263,8 +233,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
-            int t, tm, tn, ks, ns, kb0, kb1;
-            decode_unit(p, u, t, tm, tn, ks, ns, kb0, kb1);
+            const int kb0 = w.kb0, kb1 = w.kb1;
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait_bounded(smem_addr(&bars->full[stage]), phase, abort_flag, p.timeout_ns)) {
                     raise_abort(bars, p, kWhereMmaEmpty);
@@ -297,7 +266,8 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ---- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 ----
         const int quarter = warp & 3;
         int it = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++it) {
+        Work w;
+        for (int item = 0; work_at(p, item, w); ++item, ++it) {
             const int buf = it & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
             bool ok = mbar_wait_bounded(smem_addr(&bars->acc_full[buf]), acc_phase, abort_flag, p.timeout_ns);
@@ -307,16 +277,14 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 break;
             }
             tc_fence_after_sync();
-            int t, tm, tn, ks, ns, kb0, kb1;
-            decode_unit(p, u, t, tm, tn, ks, ns, kb0, kb1);
-            const int row = tm * BM + quarter * 32 + lane;
+            const int row = w.tm * BM + quarter * 32 + lane;
+            const int tn = w.tn;
             const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-            if (ns > 1) {
-                // Tail slice: the raw partial tile, tile-packed (rows and columns past
-                // M and N hold sums of the copy engine's zero fill); the tail
-                // reduction adds the slices in order and applies alpha / beta.
-                float *wrow = p.W + (static_cast<long long>(t - p.n_full) * p.tail_splits + ks) * (BM * BN) +
-                              (quarter * 32 + lane) * BN;
+            if (w.dest == kToPartial) {
+                // Stream-K piece: the raw partial tile, tile-packed (rows and columns
+                // past M and N hold sums of the copy engine's zero fill); the
+                // stream-K reduction adds the pieces in k order and applies alpha / beta.
+                float *wrow = p.W + static_cast<long long>(w.idx) * (BM * BN) + (quarter * 32 + lane) * BN;
                 if (p.kblocks <= kShortK)
                     store_partial_row<4>(t_row, wrow);
                 else

@@ -83,22 +83,20 @@ typedef struct sgemm_plan_s {
     int splits;              /* split-K factor S (1 = fused epilogue) */
     int tiles_m, tiles_n;    /* output tiles */
     int units;               /* work units: tiles_m * tiles_n * splits; with stream-K the whole
-                                tiles before the stream-K span; TF32 tail split: whole tiles plus
-                                tail_tiles * tail_splits K slices */
+                                tiles before the stream-K span */
     int grid;                /* CTAs launched (persistent: min(units, SMs * ctas_per_sm)) */
     int repack_a, repack_b;  /* operand first copied to a 16-byte-aligned workspace copy */
     int vec_c;               /* 1: C read/written with 16-byte accesses */
     int math_mode;           /* sgemm_math_mode_t */
     int launches;            /* kernels one sgemm_run launches for this plan */
     long long workspace_bytes; /* device workspace the handle holds for it */
-    int tail_tiles;          /* TF32 mode: tiles of the last, partial round of the persistent grid
-                                that are split along K to even out the waves (0 = none) */
-    int tail_splits;         /* TF32 mode: K slices per tail tile (partials reduced in order) */
     int transpose_a;         /* 1: A is first transposed into the workspace (K x M, M contiguous)
                                 and the FP32 mainloop reads A^T; 0: it reads A as given */
-    int sk_tiles;            /* FP32 mode, stream-K: the last sk_tiles tiles (after `units` whole
-                                tiles) form one span of k-blocks cut evenly over the grid's CTAs;
-                                tiles shared by two or more CTAs are reduced in k order (0 = none) */
+    int sk_tiles;            /* stream-K (both modes): the last sk_tiles tiles (after `units`
+                                whole tiles) form one span of k-blocks cut evenly over the grid's
+                                CTAs; tiles shared by two or more CTAs are reduced in k order
+                                (0 = none) */
+    int sk_grid;             /* CTAs sharing the stream-K span (the first sk_grid of the grid) */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */
@@ -115,8 +113,8 @@ typedef enum sgemm_option {
                                      before it releases a slab; |value| <= 100000, 0 = off */
     SGEMM_OPT_FORCE_TRANSPOSE_A = 7,/* FP32 path: -1 = automatic (the default), 0 = read A as given,
                                      1 = always transpose A first (same results either way) */
-    SGEMM_OPT_FORCE_STREAMK = 8   /* FP32 path: -1 = automatic (the default), 0 = never, 1 = whenever
-                                     the last round of tiles is partial (ignored with forced splits) */
+    SGEMM_OPT_FORCE_STREAMK = 8   /* -1 = automatic (the default), 0 = never, 1 = whenever the last
+                                     round of tiles is partial (ignored with forced splits) */
 } sgemm_option_t;
 
 /*

@@ -84,7 +84,6 @@ def test_plan_square_4096(lib):
     slots = 152 * p.ctas_per_sm
     assert p.sk_tiles == tiles - (tiles // slots) * slots == 112
     assert p.units == tiles - p.sk_tiles == 912 and p.grid == 152
-    assert p.tail_tiles == 0 and p.tail_splits == 0
     # A is transposed first (A^T mainloop): transpose + mainloop + stream-K reduction
     assert p.transpose_a == 1 and p.launches == 3
     assert p.workspace_bytes >= 2 * 152 * p.bm * p.bn * 4 + 4096 * 4096 * 4
@@ -160,11 +159,11 @@ def test_plan_invariants_random_shapes(lib):
         kb = -(-K // 32)
         assert 1 <= p.splits <= min(kb, 16)
         slots = sms * p.ctas_per_sm
-        assert p.tail_tiles == 0 and p.tail_splits == 0  # the TF32 mode's tail split
         if p.sk_tiles > 0:
             assert p.splits == 1 and 0 < p.sk_tiles < slots
             assert p.units == tiles - p.sk_tiles and p.units % slots == 0
             assert p.grid == (slots if p.units > 0 else min(slots, p.sk_tiles * kb))
+            assert p.sk_grid == min(slots, p.sk_tiles * kb) <= p.grid
             assert p.workspace_bytes >= 2 * p.grid * p.bm * p.bn * 4
         else:
             assert p.units == tiles * p.splits
@@ -185,8 +184,9 @@ def test_tf32_plan(lib):
     p = sg.plan(4096, 4096, 4096, math_mode=sg.MATH_TF32)
     assert p.kernel == sg.KERNEL_TF32 and (p.bm, p.bn, p.bk) == (128, 256, 32)
     assert p.repack_b == 1 and p.grid == 152 and p.transpose_a == 0
-    # 512 tiles on 152 SMs: 3 whole rounds, then the 56 remaining tiles in 2 K slices
-    assert p.tail_tiles == 56 and p.tail_splits == 2 and p.units == 456 + 112
-    assert p.launches == 3  # B transpose, mainloop, tail reduction
-    assert p.workspace_bytes >= 4096 * 4096 * 4 + 56 * 2 * 128 * 256 * 4
+    # 512 tiles on 152 SMs: 3 whole rounds, then the 56 remaining tiles as a stream-K span
+    assert p.units == 456 and p.sk_tiles == 56
+    assert p.sk_grid == 112  # 2 equal K slices per span tile, one per CTA
+    assert p.launches == 3  # B transpose, mainloop, stream-K reduction
+    assert p.workspace_bytes >= 4096 * 4096 * 4 + 2 * 152 * 128 * 256 * 4
     assert p.workspace_bytes >= 4096 * 4096 * 4  # B transposed to K-major

@@ -116,18 +116,25 @@ def test_mode_switch_back_to_fp32(h):
         h.set_math_mode(sg.MATH_TF32)
 
 
-@pytest.mark.parametrize("shape", [(4096, 4000, 2048), (512, 512, 512), (77, 1000, 517)])
-def test_tail_split(h, shape):
-    """The last partial round's tiles are cut along K (single rounds too): partial tiles
-    are added in slice order by the reduction; exact on integers, tight bound on reals,
-    and bitwise repeatable."""
+@pytest.mark.parametrize("shape", [(4096, 4000, 2048), (512, 512, 512), (77, 1000, 517), (300, 700, 1000)])
+def test_stream_k(h, shape):
+    """The last partial round's tiles form a stream-K span (the whole problem when it is
+    a single round): partial tiles are added in k order by the reduction; exact on
+    integers, tight bound on reals, and bitwise repeatable."""
+    h.set_option(sg.OPT_FORCE_STREAMK, 1)
+    try:
+        _stream_k_case(h, shape)
+    finally:
+        h.set_option(sg.OPT_FORCE_STREAMK, -1)
+
+
+def _stream_k_case(h, shape):
     M, N, K = shape
     A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=M + K, dist=("int", "int", "int"))
     got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
     assert st == sg.SGEMM_OK and guards
     plan = h.last_plan()
-    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert plan.tail_splits > 1 and plan.tail_tiles > 0 and plan.launches == 3 + plan.repack_a, plan.as_dict()
+    assert plan.kernel == sg.KERNEL_TF32 and plan.sk_tiles > 0 and plan.launches == 3 + plan.repack_a, plan.as_dict()
     rows = sample_rows(M) if M > 1024 else None
     _check(got, A, B, C, 1.5, 0.5, rows=rows, exact=True)
     Ar, Br, Cr = inputs.problem_operands(M=M, N=N, K=K, seed=M + K + 1, dist=("normal", "uniform", "uniform"))
