@@ -1,6 +1,6 @@
 // FP32 FFMA SGEMM mainloop for sm_103a, plus the operand layout kernels
 // (A / B transposition, repack of unaligned operands), the split-K and
-// tail-split reductions and the beta-only scaling kernel.
+// stream-K reductions and the beta-only scaling kernel.
 //
 // C = alpha * A * B + beta * C, row-major ("SGEMM CUDA kernel (First Half)",
 // opening definition). The structure follows the tiling ladder of the pages —

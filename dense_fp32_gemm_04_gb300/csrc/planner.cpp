@@ -82,7 +82,7 @@ bool transpose_pays(const Problem &q, double t_main)
 // spread over all CTAs, as on the FP32 path, gives two partials per CTA: the
 // TF32 epilogue writes those slower than it saves, 4096^3 219 -> 237 us.)
 // Rates: the mainloop's measured ~650 TFLOP/s, ~5.5 TB/s for the reduction.
-int choose_tail_tf32(int M, int N, int K, int num_sms, bool beta_read)
+int choose_slices_tf32(int M, int N, int K, int num_sms, bool beta_read)
 {
     const double flops_per_sm = 650e12 / 152.0;
     const double hbm = 5.5e12;
@@ -98,10 +98,10 @@ int choose_tail_tf32(int M, int N, int K, int num_sms, bool beta_read)
     double best_gain = 0.01 * static_cast<double>(rounds) * t_last;
     int best = 0;
     for (int st = 2; st <= 8 && st <= kb; ++st) {
-        const double t_tail = static_cast<double>(ceil_div(rem * st, slots)) *
+        const double t_span_round = static_cast<double>(ceil_div(rem * st, slots)) *
                               (static_cast<double>(ceil_div(kb, st)) + 1.5) * t_kb;
         const double bytes = (2.0 * st + (beta_read ? 2.0 : 1.0)) * 4.0 * static_cast<double>(rem) * tile_elems;
-        const double gain = t_last - t_tail - bytes / hbm - 2.5e-6;
+        const double gain = t_last - t_span_round - bytes / hbm - 2.5e-6;
         if (gain > best_gain) {
             best_gain = gain;
             best = st;
@@ -214,7 +214,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
             const long long n_full = (ceil_div(units, slots) - 1) * slots;
             const long long rem = units - n_full;
             const long long kb = ceil_div(q.K, sgemm_cfg::kTf32BK);
-            long long st = choose_tail_tf32(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
+            long long st = choose_slices_tf32(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
             if (st < 2 && ov.force_streamk == 1) st = std::min(kb, slots / rem);  // forced: fill the idle CTAs
             st = std::min(st, slots / rem);  // one slice per CTA: rem * st CTAs at most `slots`
             if (st >= 2 && rem < slots) {

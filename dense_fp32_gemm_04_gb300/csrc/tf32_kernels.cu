@@ -3,7 +3,9 @@
 // bits), products are accumulated in FP32 in tensor memory (TMEM). It is never
 // used unless the caller selects it, and is held to its own, looser bound.
 //
-// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
+// Structure (one CTA per SM, persistent over 128 x 256 output tiles, walking
+// the work sequence of schedule.cuh: whole tiles, then the CTA's K slice of
+// a stream-K span whose partial tiles sk_reduce_kernel adds in k order):
 //   warp 0      TMA producer: A box (32 k x 128 rows) and B^T box (32 k x 256
 //               columns), both with the 128-byte swizzle, into a 4-stage ring.
 //   warp 1      MMA issuer: one thread issues 4 tcgen05.mma (K = 8 each) per

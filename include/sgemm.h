@@ -123,7 +123,7 @@ typedef enum sgemm_option {
  * Returns SGEMM_ERR_ARCH unless the device is compute capability 10.3,
  * SGEMM_ERR_ALLOC if its small device status word cannot be allocated.
  * The handle owns a lazily grown device workspace (the transposed copy of A,
- * aligned operand copies, split-K and tail-split partials) and, for
+ * aligned operand copies, split-K and stream-K partials) and, for
  * sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
