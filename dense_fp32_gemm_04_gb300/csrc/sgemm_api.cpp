@@ -80,14 +80,17 @@ int ensure_workspace(sgemm_handle_t h, size_t bytes)
         h->workspace = nullptr;
         h->ws_bytes = 0;
     }
-    const size_t grow = bytes + bytes / 4;
-    if (cudaMalloc(&h->workspace, grow) != cudaSuccess) {
+    // 25 % headroom so that slowly growing problems do not reallocate every call;
+    // exactly `bytes` when the headroom does not fit.
+    for (size_t size : {bytes + bytes / 4, bytes}) {
+        if (cudaMalloc(&h->workspace, size) == cudaSuccess) {
+            h->ws_bytes = size;
+            return SGEMM_OK;
+        }
         cudaGetLastError();
         h->workspace = nullptr;
-        return SGEMM_ERR_ALLOC;
     }
-    h->ws_bytes = grow;
-    return SGEMM_OK;
+    return SGEMM_ERR_ALLOC;
 }
 
 // 2-D FP32 tensor map over a row-major (outer x inner) matrix with row stride ld.
@@ -254,14 +257,26 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     sgemm_plan_t plan;
     int rc = make_plan(q, h->ov, &plan);
     if (rc != SGEMM_OK) return rc;
+    if (plan.kernel == SGEMM_KERNEL_NONE || plan.kernel == SGEMM_KERNEL_SCALE) {
+        if (h->log) log_plan(plan, M, N, K);
+        h->last = plan;
+        if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;
+        return launch_scale(M, N, beta, C, ldc, h->num_sms, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
+
+    Workspace w = workspace_layout(q, plan);
+    rc = ensure_workspace(h, static_cast<size_t>(w.total));
+    if (rc == SGEMM_ERR_ALLOC && plan.transpose_a && h->ov.force_transpose_a < 0) {
+        // No room for A^T (a very large A): read A as given instead, same results.
+        Overrides ov = h->ov;
+        ov.force_transpose_a = 0;
+        if ((rc = make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
+        w = workspace_layout(q, plan);
+        rc = ensure_workspace(h, static_cast<size_t>(w.total));
+    }
     if (h->log) log_plan(plan, M, N, K);
     h->last = plan;
-    if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;
-    if (plan.kernel == SGEMM_KERNEL_SCALE)
-        return launch_scale(M, N, beta, C, ldc, h->num_sms, stream) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
-
-    const Workspace w = workspace_layout(q, plan);
-    if ((rc = ensure_workspace(h, static_cast<size_t>(w.total))) != SGEMM_OK) return rc;
+    if (rc != SGEMM_OK) return rc;
     char *ws = static_cast<char *>(h->workspace);
 
     const float *a_src = A;
