@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 namespace sgemm_dev {
 
@@ -81,6 +82,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if (static_cast<long long>(global_timer_ns() - t0) > timeout_ns) return false;
     }
 }
+
+// Programmatic dependent launch (kernels of one library call). pdl_wait: block
+// until the grid this one was launched after has completed and its writes are
+// visible (returns at once for a grid launched the ordinary way). pdl_trigger:
+// let the next grid of the call, launched with the programmatic-serialization
+// attribute, become resident early; it still waits in pdl_wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
@@ -205,6 +214,26 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
 {
     return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Launch `kernel`; with `dependent`, as a programmatic dependent of the kernel
+// launched before it on `stream` (used only between kernels of one call, so a
+// grid never waits on a previous call's kernels beyond their completion).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(bool dependent, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
 }  // namespace sgemm_dev

@@ -88,6 +88,7 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
     uint32_t issued = 0, issued_parity = 0;  // per stage: has a copy outstanding, and its phase parity
     int seq = 0;
     bool ok = true;
+    pdl_wait();  // the operands written by this call's transpose / repack are complete
     Work w;
     for (int item = 0; ok && work_at(p, item, w); ++item) {
         const int tm = w.tm, tn = w.tn;
@@ -121,6 +122,7 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
             }
         }
     }
+    pdl_trigger();  // every copy is issued: the call's reduction may become resident
     // No copy of ours may still be writing this CTA's shared memory when it exits.
     for (int s = 0; s < T::STAGES; ++s) {
         if (issued >> s & 1u) {
@@ -434,13 +436,13 @@ cudaError_t set_attr()
 
 template <class T>
 cudaError_t launch(bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
-                   cudaStream_t stream)
+                   cudaStream_t stream, bool dependent)
 {
     if (a_mmajor)
-        ffma_sgemm_kernel<T, true><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tmA, tmB, p);
-    else
-        ffma_sgemm_kernel<T, false><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tmA, tmB, p);
-    return cudaGetLastError();
+        return launch_kernel(dependent, ffma_sgemm_kernel<T, true>, dim3(grid), dim3(T::THREADS), T::SMEM_BYTES,
+                             stream, tmA, tmB, p);
+    return launch_kernel(dependent, ffma_sgemm_kernel<T, false>, dim3(grid), dim3(T::THREADS), T::SMEM_BYTES, stream,
+                         tmA, tmB, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -451,6 +453,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, long long ldw,
                                      int M, int N, float alpha, float beta, float *__restrict__ C, long long ldc,
                                      int vec_c)
 {
+    pdl_wait();  // the mainloop's slices are complete and visible
     const int n4 = (N + 3) >> 2;
     const long long total = static_cast<long long>(M) * n4;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -493,6 +496,7 @@ constexpr int kSkMaxShared = 64;  // covering CTAs whose offsets are kept in sha
 __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int bm, int bn)
 {
     __shared__ long long off[kSkMaxShared];
+    pdl_wait();  // the mainloop's partial tiles are complete and visible
     const long long S = static_cast<long long>(p.sk_tiles) * p.kblocks;
     const long long G = p.sk_grid;
     const int rel = blockIdx.y;
@@ -551,6 +555,7 @@ __global__ void scale_kernel(int M, int N, float beta, float *__restrict__ C, lo
 __global__ void repack_kernel(const float *__restrict__ src, long long lds, float *__restrict__ dst, long long ldd,
                               int rows, int cols)
 {
+    pdl_trigger();  // the call's mainloop may become resident; it waits for this grid to finish
     const long long total = static_cast<long long>(rows) * cols;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -571,6 +576,7 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
                                                         float *__restrict__ XT, long long ldxt, int rows, int cols)
 {
     __shared__ float tile[64][65];
+    pdl_trigger();  // the call's mainloop may become resident; it waits for this grid to finish
     const int c0 = blockIdx.x * 64;
     const int t = threadIdx.x;
     for (long long r0l = blockIdx.y * 64LL; r0l < rows; r0l += gridDim.y * 64LL) {
@@ -628,13 +634,13 @@ cudaError_t ffma_set_attributes()
 }
 
 cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const FfmaParams &p, int grid, cudaStream_t stream)
+                        const FfmaParams &p, int grid, cudaStream_t stream, bool dependent)
 {
     switch (config) {
-    case 0: return launch<Cfg0>(a_mmajor, tmA, tmB, p, grid, stream);
-    case 1: return launch<Cfg1>(a_mmajor, tmA, tmB, p, grid, stream);
-    case 2: return launch<Cfg2>(a_mmajor, tmA, tmB, p, grid, stream);
-    case 3: return launch<Cfg3>(a_mmajor, tmA, tmB, p, grid, stream);
+    case 0: return launch<Cfg0>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
+    case 1: return launch<Cfg1>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
+    case 2: return launch<Cfg2>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
+    case 3: return launch<Cfg3>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -644,17 +650,15 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
                                  cudaStream_t stream)
 {
     const long long work = static_cast<long long>(M) * ((N + 3) / 4);
-    splitk_reduce_kernel<<<elementwise_grid(work, 256, num_sms), 256, 0, stream>>>(W, ldw, wstride, splits, M, N,
-                                                                                   alpha, beta, C, ldc, vec_c);
-    return cudaGetLastError();
+    return launch_kernel(true, splitk_reduce_kernel, dim3(elementwise_grid(work, 256, num_sms)), dim3(256), 0, stream,
+                         W, ldw, wstride, splits, M, N, alpha, beta, C, ldc, vec_c);
 }
 
 cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)
 {
     (void)num_sms;
     const dim3 grid((bm * (bn / 4) + 255) / 256, p.sk_tiles);  // sk_tiles < SMs * CTAs per SM
-    sk_reduce_kernel<<<grid, 256, 0, stream>>>(p, bm, bn);
-    return cudaGetLastError();
+    return launch_kernel(true, sk_reduce_kernel, grid, dim3(256), 0, stream, p, bm, bn);
 }
 
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms, cudaStream_t stream)

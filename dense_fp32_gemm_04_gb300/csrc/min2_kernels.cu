@@ -15,10 +15,13 @@
 #include <climits>
 #include <cstdint>
 
+#include "device_ptx.cuh"
 #include "sgemm_internal.h"
 
 namespace sgemm_impl {
 namespace {
+
+using namespace sgemm_dev;
 
 constexpr int kThreads = 256;
 
@@ -86,6 +89,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(kThreads) min2_pass1(const float *__restrict__ C, long long ldc, int M, int N,
                                                        Top2 *__restrict__ cand)
 {
+    pdl_wait();     // C is complete (the call's GEMM kernels)
+    pdl_trigger();  // the merge may become resident; it waits for this grid to finish
     Top2 t = empty_top2();
     for (int row = blockIdx.x; row < M; row += gridDim.x) {
         const float *crow = C + static_cast<long long>(row) * ldc;
@@ -123,6 +128,7 @@ __global__ void __launch_bounds__(kThreads) min2_pass1(const float *__restrict__
 __global__ void __launch_bounds__(kThreads) min2_pass2(const Top2 *__restrict__ cand, int n, int N,
                                                        float *__restrict__ vals, int *__restrict__ ij)
 {
+    pdl_wait();  // every candidate pair is written
     Top2 t = empty_top2();
     for (int i = threadIdx.x; i < n; i += kThreads) merge(t, cand[i]);
     t = block_reduce(t);
@@ -145,12 +151,14 @@ cudaError_t launch_min2(const float *C, long long ldc, int M, int N, void *cand,
 {
     const int g = M < blocks ? (M > 0 ? M : 1) : blocks;
     const bool vec = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && ldc % 4 == 0;
-    if (vec)
-        min2_pass1<true><<<g, kThreads, 0, stream>>>(C, ldc, M, N, static_cast<Top2 *>(cand));
-    else
-        min2_pass1<false><<<g, kThreads, 0, stream>>>(C, ldc, M, N, static_cast<Top2 *>(cand));
-    min2_pass2<<<1, kThreads, 0, stream>>>(static_cast<const Top2 *>(cand), g, N, vals, ij);
-    return cudaGetLastError();
+    // Both run as programmatic dependents of the kernel before them (the call's GEMM,
+    // then pass 1); with nothing launched by the GEMM they simply follow the stream.
+    Top2 *c = static_cast<Top2 *>(cand);
+    cudaError_t e = vec ? launch_kernel(true, min2_pass1<true>, dim3(g), dim3(kThreads), 0, stream, C, ldc, M, N, c)
+                        : launch_kernel(true, min2_pass1<false>, dim3(g), dim3(kThreads), 0, stream, C, ldc, M, N, c);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(true, min2_pass2, dim3(1), dim3(kThreads), 0, stream, static_cast<const Top2 *>(c), g, N,
+                         vals, ij);
 }
 
 }  // namespace sgemm_impl

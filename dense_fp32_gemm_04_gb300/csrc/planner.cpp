@@ -57,10 +57,12 @@ double model_time_sk(const sgemm_cfg::TileConfig &c, int M, int N, int K, int nu
     const double t_kb = static_cast<double>(c.bm) * c.bn * sgemm_cfg::kFfmaBK * c.ctas_per_sm / fma_per_sm * c.rel_cost;
     double t = static_cast<double>(rounds - 1) * (static_cast<double>(kb) + 1.5) * t_kb +
                (static_cast<double>(ceil_div(span, G)) + 3.0) * t_kb + 2.0e-6;
+    // Partial tiles (written, then read by the reduction) mostly stay in L2: counted
+    // at twice the HBM rate; C at the HBM rate.
     const double tile_bytes = 4.0 * c.bm * c.bn;
-    const double bytes = (2.0 * static_cast<double>(G + rem) + (beta_read ? 2.0 : 1.0) * static_cast<double>(rem)) *
-                         tile_bytes;
-    return t + bytes / hbm + 2.5e-6;
+    const double part_bytes = 2.0 * static_cast<double>(G + rem) * tile_bytes;
+    const double c_bytes = (beta_read ? 2.0 : 1.0) * static_cast<double>(rem) * tile_bytes;
+    return t + part_bytes / (2.0 * hbm) + c_bytes / hbm + 2.5e-6;
 }
 
 // Transposing A first pays when its copy (read + write of A, one more launch)
@@ -266,10 +268,14 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
 
     // A^T: the mainloop's FFMA2 form with A pairs along M runs ~10 % faster;
     // transposing A costs one read and one write of A.
-    if (ov.force_transpose_a >= 0)
+    if (ov.force_transpose_a >= 0) {
         out->transpose_a = ov.force_transpose_a;
-    else
-        out->transpose_a = transpose_pays(q, model_time(c, q.M, q.N, q.K, S, q.num_sms, q.beta != 0.0f)) ? 1 : 0;
+    } else {
+        const bool beta_read = q.beta != 0.0f;
+        const double t_main = out->sk_tiles > 0 ? model_time_sk(c, q.M, q.N, q.K, q.num_sms, beta_read)
+                                                : model_time(c, q.M, q.N, q.K, S, q.num_sms, beta_read);
+        out->transpose_a = transpose_pays(q, t_main) ? 1 : 0;
+    }
     if (out->transpose_a) out->repack_a = 0;  // the transposed copy is aligned whatever A was
 
     const Workspace w = workspace_layout(q, *out);

@@ -338,7 +338,9 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         p.sk_tiles = plan.sk_tiles;
         p.sk_grid = plan.sk_grid;
     }
-    if (launch_ffma(plan.config, plan.transpose_a != 0, tmA, tmB, p, plan.grid, stream) != cudaSuccess)
+    // Right after this call's transpose / repack: launched as its programmatic dependent.
+    const bool after_copy = plan.transpose_a || plan.repack_a || plan.repack_b;
+    if (launch_ffma(plan.config, plan.transpose_a != 0, tmA, tmB, p, plan.grid, stream, after_copy) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.sk_tiles > 0 && launch_sk_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;

@@ -72,8 +72,10 @@ struct Tf32Params {
 // error of the launch (cudaSuccess when it was enqueued).
 cudaError_t ffma_set_attributes();  // opt in to large dynamic shared memory (current device)
 // a_mmajor: tmA maps A^T (K rows of M, M contiguous) instead of A (M rows of K).
+// dependent: launched as a programmatic dependent of the call's previous kernel
+// (transpose / repack), whose completion its copy issue waits for.
 cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const FfmaParams &p, int grid, cudaStream_t stream);
+                        const FfmaParams &p, int grid, cudaStream_t stream, bool dependent);
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
                                  int vec_c, int num_sms, cudaStream_t stream);

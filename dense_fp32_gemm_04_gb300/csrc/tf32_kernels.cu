@@ -193,6 +193,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
+        pdl_wait();  // B^T (and a repacked A) written by this call's previous kernels are complete
         Work w;
         for (int item = 0; ok && work_at(p, item, w); ++item) {
             const int tm = w.tm, tn = w.tn;
@@ -213,6 +214,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
+        pdl_trigger();  // every copy is issued: the call's reduction may become resident
         for (int s = 0; s < STAGES; ++s) {
             const int rec = bars->issued[s];
             if ((rec & 2) && !mbar_wait_bounded(smem_addr(&bars->full[s]), static_cast<uint32_t>(rec & 1), nullptr,
@@ -326,8 +328,9 @@ cudaError_t tf32_set_attributes()
 cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
                         cudaStream_t stream)
 {
-    tf32_sgemm_kernel<<<grid, THREADS, sgemm_cfg::tf32_smem_bytes(), stream>>>(tmA, tmBt, p);
-    return cudaGetLastError();
+    // always right after this call's B transposition: launched as its programmatic dependent
+    return launch_kernel(true, tf32_sgemm_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_smem_bytes(), stream,
+                         tmA, tmBt, p);
 }
 
 }  // namespace sgemm_impl
