@@ -381,8 +381,12 @@ def measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, device, st
     achieved = gemm_flops(M, N, K) / (ms * 1e-3) / 1e12
     bf16, basis = measured_bf16_peak()
     peak = bf16 * (1.1 / 2.25)  # nominal dense tf32 : bf16 ratio
+    kernel = ("tf32_pair_kernel (CTA pairs, tcgen05 .cta_group::2, 256 x 256 tiles)" if plan.config == 1
+              else "tf32_sgemm_kernel (one CTA per 128 x 256 tile)")
     return {"value": achieved, "unit": "TFLOP/s", "ms_per_call": ms, "steps": steps, "status": st,
-            "launches_per_call": plan.launches,
+            "launches_per_call": plan.launches, "kernel": kernel,
+            "plan": {k: plan.as_dict()[k] for k in ("config", "bm", "bn", "stages", "grid", "units", "sk_tiles",
+                                                    "sk_grid")},
             "note": "flagged SGEMM_MATH_TF32 (TF32 inputs, FP32 accumulate); per-call time includes the B transpose",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,

@@ -41,6 +41,7 @@ OPT_LOG = 5
 OPT_SKEW_NS = 6
 OPT_FORCE_TRANSPOSE_A = 7
 OPT_FORCE_STREAMK = 8
+OPT_FORCE_TF32_KERNEL = 9
 
 
 class Plan(ctypes.Structure):

@@ -76,32 +76,38 @@ bool transpose_pays(const Problem &q, double t_main)
     return t_copy < kAtGain * t_main;
 }
 
-// Stream-K span of the TF32 mode (one 128 x 256 tile per SM per round), cut into
-// equal K slices: the span's rem tiles go to rem * St CTAs, so that every CTA
-// range is slice s of one tile (k-blocks [s kb / St, (s + 1) kb / St)) and each
-// writes one partial tile. St <= 8 with at least one 32-deep block per slice,
-// chosen when the modelled time saved exceeds the partial-tile reduction. (A span
-// spread over all CTAs, as on the FP32 path, gives two partials per CTA: the
-// TF32 epilogue writes those slower than it saves, 4096^3 219 -> 237 us.)
-// Rates: the mainloop's measured ~650 TFLOP/s, ~5.5 TB/s for the reduction.
-int choose_slices_tf32(int M, int N, int K, int num_sms, bool beta_read)
+// TF32 mode, one kernel (one CTA per 128 x 256 tile on `slots` SMs, or one CTA
+// pair per 256 x 256 tile on `slots` pairs): modelled time of the persistent
+// grid, and the stream-K slicing of its last partial round. The span's rem tiles
+// go to rem * St workers in equal K slices, so that every worker's range is
+// slice s of one tile (k-blocks [s kb / St, (s + 1) kb / St)) and each writes
+// one partial tile; St <= 8 with at least one 32-deep block per slice, taken
+// when the modelled time saved exceeds the partial-tile reduction by 1 % of the
+// call. (A span spread over all workers, as on the FP32 path, gives two partials
+// per worker: the TF32 epilogue writes those slower than it saves, 4096^3 219 ->
+// 237 us with one CTA per tile.) Rates: FLOP/s per worker as measured for each
+// kernel; ~5.5 TB/s for the reduction.
+struct Tf32Model {
+    double time;
+    int slices;  // St, 0 = no stream-K
+};
+
+Tf32Model model_tf32(int M, int N, int K, int bm, int bn, long long slots, double flops_per_worker, bool beta_read)
 {
-    const double flops_per_sm = 650e12 / 152.0;
     const double hbm = 5.5e12;
     const long long kb = ceil_div(K, sgemm_cfg::kTf32BK);
-    const long long tiles = ceil_div(M, sgemm_cfg::kTf32BM) * ceil_div(N, sgemm_cfg::kTf32BN);
-    const long long slots = num_sms;
+    const long long tiles = ceil_div(M, bm) * ceil_div(N, bn);
     const long long rounds = ceil_div(tiles, slots);
     const long long rem = tiles - (rounds - 1) * slots;
-    if (rem >= slots) return 0;
-    const double tile_elems = static_cast<double>(sgemm_cfg::kTf32BM) * sgemm_cfg::kTf32BN;
-    const double t_kb = tile_elems * sgemm_cfg::kTf32BK * 2.0 / flops_per_sm;
+    const double tile_elems = static_cast<double>(bm) * bn;
+    const double t_kb = tile_elems * sgemm_cfg::kTf32BK * 2.0 / flops_per_worker;
     const double t_last = (static_cast<double>(kb) + 1.5) * t_kb;
-    double best_gain = 0.01 * static_cast<double>(rounds) * t_last;
+    const double base = static_cast<double>(rounds) * t_last + 2.0e-6;
+    if (rem >= slots) return {base, 0};
+    double best_gain = 0.01 * base;
     int best = 0;
-    for (int st = 2; st <= 8 && st <= kb; ++st) {
-        const double t_span_round = static_cast<double>(ceil_div(rem * st, slots)) *
-                              (static_cast<double>(ceil_div(kb, st)) + 1.5) * t_kb;
+    for (int st = 2; st <= 8 && st <= kb && rem * st <= slots; ++st) {
+        const double t_span_round = (static_cast<double>(ceil_div(kb, st)) + 1.5) * t_kb;
         const double bytes = (2.0 * st + (beta_read ? 2.0 : 1.0)) * 4.0 * static_cast<double>(rem) * tile_elems;
         const double gain = t_last - t_span_round - bytes / hbm - 2.5e-6;
         if (gain > best_gain) {
@@ -109,8 +115,14 @@ int choose_slices_tf32(int M, int N, int K, int num_sms, bool beta_read)
             best = st;
         }
     }
-    return best;
+    return {best > 0 ? base - best_gain : base, best};
 }
+
+// Measured mainloop rates (4096^3, GB300): one CTA per tile ~650 TFLOP/s on
+// 152 SMs.
+constexpr double kTf32FlopsPerSm = 650e12 / 152.0;
+// CTA pair: per pair, relative to two SMs of the one-CTA kernel.
+constexpr double kTf32PairGain = 1.30;
 
 }  // namespace
 
@@ -196,11 +208,29 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     if (q.math_mode == SGEMM_MATH_TF32) {
         // B always goes through the workspace: transposed to K-major (N x roundup(K, 4)).
         if (q.K > 65535LL * 64) return SGEMM_ERR_NOT_SUPPORTED;
+        const long long pairs = q.num_pairs > 0 ? q.num_pairs : (q.num_pairs == 0 ? q.num_sms / 2 : 0);
+        const bool beta_read = q.beta != 0.0f;
+        const Tf32Model one = model_tf32(q.M, q.N, q.K, sgemm_cfg::kTf32BM, sgemm_cfg::kTf32BN, q.num_sms,
+                                         kTf32FlopsPerSm, beta_read);
+        Tf32Model two{INFINITY, 0};
+        if (pairs > 0)
+            two = model_tf32(q.M, q.N, q.K, sgemm_cfg::kTf32PairBM, sgemm_cfg::kTf32PairBN, pairs,
+                             2.0 * kTf32FlopsPerSm * kTf32PairGain, beta_read);
+        bool use_pair = two.time < one.time;
+        if (ov.force_tf32_kernel == 0) use_pair = false;
+        if (ov.force_tf32_kernel == 1) {
+            if (pairs <= 0) return SGEMM_ERR_NOT_SUPPORTED;
+            use_pair = true;
+        }
+        const Tf32Model &m = use_pair ? two : one;
+        const long long slots = use_pair ? pairs : q.num_sms;  // workers
+        const int cluster = use_pair ? 2 : 1;                  // CTAs per worker
         out->kernel = SGEMM_KERNEL_TF32;
-        out->bm = sgemm_cfg::kTf32BM;
-        out->bn = sgemm_cfg::kTf32BN;
+        out->config = use_pair ? 1 : 0;
+        out->bm = use_pair ? sgemm_cfg::kTf32PairBM : sgemm_cfg::kTf32BM;
+        out->bn = use_pair ? sgemm_cfg::kTf32PairBN : sgemm_cfg::kTf32BN;
         out->bk = sgemm_cfg::kTf32BK;
-        out->stages = sgemm_cfg::kTf32Stages;
+        out->stages = use_pair ? sgemm_cfg::kTf32PairStages : sgemm_cfg::kTf32Stages;
         out->threads = sgemm_cfg::kTf32Threads;
         out->ctas_per_sm = 1;
         out->splits = 1;
@@ -208,22 +238,21 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         out->tiles_m = static_cast<int>(ceil_div(q.M, out->bm));
         out->tiles_n = static_cast<int>(ceil_div(q.N, out->bn));
         const long long units = static_cast<long long>(out->tiles_m) * out->tiles_n;
-        if (units > INT_MAX) return SGEMM_ERR_NOT_SUPPORTED;
+        if (units > INT_MAX / 2) return SGEMM_ERR_NOT_SUPPORTED;
         out->units = static_cast<int>(units);
-        out->grid = static_cast<int>(std::min<long long>(units, q.num_sms));
+        out->grid = static_cast<int>(cluster * std::min<long long>(units, slots));
         if (ov.force_splits == 0 && ov.force_streamk != 0) {
-            const long long slots = q.num_sms;
             const long long n_full = (ceil_div(units, slots) - 1) * slots;
             const long long rem = units - n_full;
             const long long kb = ceil_div(q.K, sgemm_cfg::kTf32BK);
-            long long st = choose_slices_tf32(q.M, q.N, q.K, q.num_sms, q.beta != 0.0f);
-            if (st < 2 && ov.force_streamk == 1) st = std::min(kb, slots / rem);  // forced: fill the idle CTAs
-            st = std::min(st, slots / rem);  // one slice per CTA: rem * st CTAs at most `slots`
+            long long st = m.slices;
+            if (st < 2 && ov.force_streamk == 1 && rem < slots) st = std::min(kb, slots / rem);  // forced: fill idle workers
+            st = std::min(st, slots / rem);  // one slice per worker: rem * st workers at most `slots`
             if (st >= 2 && rem < slots) {
                 out->units = static_cast<int>(n_full);
                 out->sk_tiles = static_cast<int>(rem);
                 out->sk_grid = static_cast<int>(rem * st);
-                out->grid = static_cast<int>(n_full > 0 ? slots : std::min(slots, rem * st));
+                out->grid = static_cast<int>(cluster * (n_full > 0 ? slots : std::min(slots, rem * st)));
             }
         }
         out->workspace_bytes = workspace_layout(q, *out).total;
@@ -308,9 +337,9 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
         off += round_up(static_cast<long long>(q.K) * w.ldb * 4, 256);
     }
     if (p.sk_tiles > 0) {
-        // two partial tiles per CTA of the stream-K grid
+        // two partial tiles per worker (CTA, or CTA pair) of the stream-K span
         w.w_off = off;
-        off += round_up(2LL * p.grid * p.bm * p.bn * 4, 256);
+        off += round_up(2LL * p.sk_grid * p.bm * p.bn * 4, 256);
     } else if (p.splits > 1) {
         w.ldw = round_up(q.N, 4);
         w.wstride = static_cast<long long>(q.M) * w.ldw;

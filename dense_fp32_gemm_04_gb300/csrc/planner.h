@@ -16,6 +16,7 @@ struct Problem {
     int num_sms;
     int math_mode;
     float alpha, beta;
+    int num_pairs = 0;  // TF32 CTA pairs resident at once (0: num_sms / 2; < 0: none)
 };
 
 struct Overrides {
@@ -23,6 +24,7 @@ struct Overrides {
     int force_splits = 0;   // 0 automatic
     int force_transpose_a = -1;  // -1 automatic, 0 never, 1 always (FFMA kernel)
     int force_streamk = -1;      // -1 automatic, 0 never, 1 whenever the last round is partial
+    int force_tf32_kernel = -1;  // -1 automatic, 0 one CTA per tile, 1 CTA pairs
 };
 
 // Offsets (bytes) into the handle's workspace and the strides used there.

@@ -1,16 +1,17 @@
 // Tile scheduling shared by the persistent FFMA and TF32 kernels: the grouped
-// tile raster, and the sequence of work items of one CTA (data-parallel units,
-// then its share of a stream-K span).
+// tile raster, and the sequence of work items of one worker (data-parallel
+// units, then its share of a stream-K span). A worker is a CTA, or a CTA pair
+// working on the two halves of one tile (the TF32 pair kernel).
 //
 // Params (FfmaParams or Tf32Params) provide: tiles_m, tiles_n, units, splits,
 // kblocks, sk_tiles, sk_grid. Units [0, units) are u = tile * splits + slice;
 // tiles [units / splits, units / splits + sk_tiles) form the stream-K span of
-// S = sk_tiles * kblocks k-blocks, of which CTA g (< sk_grid) takes
-// [g S / G, (g + 1) S / G). A tile inside one CTA's range is finished by it;
-// a tile shared by several CTAs gets one tile-packed partial from each, at
-// slot 2g for the CTA's first span tile and 2g + 1 for its last, which the
-// stream-K reduction adds in CTA (= k) order. The covering CTAs of span tile t
-// are ((t kb + 1) G - 1) / S .. ((t + 1) kb G - 1) / S.
+// S = sk_tiles * kblocks k-blocks, of which worker g (< sk_grid = G) takes
+// [g S / G, (g + 1) S / G). A tile inside one worker's range is finished by
+// it; a tile shared by several workers gets one tile-packed partial from each,
+// at slot 2g for the worker's first span tile and 2g + 1 for its last, which
+// the stream-K reduction adds in worker (= k) order. The covering workers of
+// span tile t are ((t kb + 1) G - 1) / S .. ((t + 1) kb G - 1) / S.
 #pragma once
 
 namespace sgemm_impl {
@@ -39,15 +40,15 @@ struct Work {
     int t, tm, tn, kb0, kb1, dest, idx;
 };
 
-// Item i of this CTA's work: first its units (u = blockIdx.x + i * gridDim.x),
+// Item i of worker g's work (of G workers): first its units (u = g + i * G),
 // then the pieces of its stream-K range, one per tile the range touches.
 // Computed from i alone, so callers keep only i live across a mainloop, and
 // every role of a CTA (copy issue, compute, epilogue) walks the same sequence.
-// Returns false past the end.
+// A worker is a CTA, or a CTA pair that shares its tiles. Returns false past
+// the end.
 template <class P>
-__device__ __forceinline__ bool work_at(const P &p, int i, Work &w)
+__device__ __forceinline__ bool work_at_g(const P &p, int i, Work &w, int g, int G)
 {
-    const int g = blockIdx.x, G = gridDim.x;
     const int n_units = g < p.units ? (p.units - g + G - 1) / G : 0;
     if (i < n_units) {
         const int u = g + i * G;
@@ -78,6 +79,13 @@ __device__ __forceinline__ bool work_at(const P &p, int i, Work &w)
     w.dest = (w.kb0 == 0 && w.kb1 == p.kblocks) ? kToC : kToPartial;
     w.idx = 2 * g + (j == 0 ? 0 : 1);
     return true;
+}
+
+// Worker = this CTA.
+template <class P>
+__device__ __forceinline__ bool work_at(const P &p, int i, Work &w)
+{
+    return work_at_g(p, i, w, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
 }
 
 }  // namespace sgemm_impl

@@ -23,6 +23,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 struct sgemm_handle_s {
     int device = 0;
     int num_sms = 0;
+    int tf32_pairs = -1;  // CTA pairs of the TF32 pair kernel resident at once (-1: none fit)
     int math_mode = SGEMM_MATH_FP32;
     int *d_status = nullptr;
     void *workspace = nullptr;
@@ -130,7 +131,8 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
                  p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.sk_tiles);
 }
 
-// TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop.
+// TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop
+// (one CTA per 128 x 256 tile, or a CTA pair per 256 x 256 tile) [-> stream-K reduction].
 int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int M, int N, int K, float alpha,
              const float *A, int lda, const float *B, int ldb, float beta, float *C, int ldc, cudaStream_t stream)
 {
@@ -147,10 +149,13 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     if (launch_transpose(B, ldb, bt, w.ldb, K, N, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
     CUtensorMap tmA, tmBt;
     int rc;
-    if ((rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kTf32BK, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+    // Boxes: a CTA's rows of the tile (the pair kernel's CTAs stage half of A's and half of B's rows each).
+    const bool pair = plan.config == 1;
+    const int box_a = pair ? plan.bm / 2 : plan.bm, box_b = pair ? plan.bn / 2 : plan.bn;
+    if ((rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kTf32BK, box_a, CU_TENSOR_MAP_SWIZZLE_128B)) !=
         SGEMM_OK)
         return rc;
-    if ((rc = make_tmap(h, &tmBt, bt, K, N, w.ldb, sgemm_cfg::kTf32BK, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+    if ((rc = make_tmap(h, &tmBt, bt, K, N, w.ldb, sgemm_cfg::kTf32BK, box_b, CU_TENSOR_MAP_SWIZZLE_128B)) !=
         SGEMM_OK)
         return rc;
     Tf32Params p{};
@@ -174,7 +179,9 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         p.sk_tiles = plan.sk_tiles;
         p.sk_grid = plan.sk_grid;
     }
-    if (launch_tf32(tmA, tmBt, p, plan.grid, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    const cudaError_t le =
+        pair ? launch_tf32_pair(tmA, tmBt, p, plan.grid, stream) : launch_tf32(tmA, tmBt, p, plan.grid, stream);
+    if (le != cudaSuccess) return SGEMM_ERR_LAUNCH;
     if (plan.sk_tiles > 0) {
         // Same raster and tile-packed partial layout as the FP32 stream-K span.
         FfmaParams r{};
@@ -254,6 +261,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
 {
     const int align = (aligned16(A) ? 1 : 0) | (aligned16(B) ? 2 : 0) | (aligned16(C) ? 4 : 0);
     Problem q{M, N, K, lda, ldb, ldc, align, h->num_sms, h->math_mode, alpha, beta};
+    q.num_pairs = h->tf32_pairs;
     sgemm_plan_t plan;
     int rc = make_plan(q, h->ov, &plan);
     if (rc != SGEMM_OK) return rc;
@@ -406,6 +414,10 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
         delete h;
         return SGEMM_ERR_CUDA;
     }
+    {
+        const int pairs = tf32_pair_max_pairs();
+        h->tf32_pairs = pairs > 0 ? std::min(pairs, sms / 2) : -1;
+    }
     if (cudaMalloc(&h->d_status, 256) != cudaSuccess || cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
         cudaGetLastError();
         if (h->d_status) cudaFree(h->d_status);
@@ -430,6 +442,10 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
     if (const char *fk = std::getenv("SGEMM_FORCE_STREAMK")) {
         const long v = std::strtol(fk, nullptr, 10);
         if (v >= -1 && v <= 1) h->ov.force_streamk = static_cast<int>(v);
+    }
+    if (const char *fp = std::getenv("SGEMM_FORCE_TF32_KERNEL")) {
+        const long v = std::strtol(fp, nullptr, 10);
+        if (v >= -1 && v <= 1) h->ov.force_tf32_kernel = static_cast<int>(v);
     }
     *out = h;
     return SGEMM_OK;
@@ -643,6 +659,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
     case SGEMM_OPT_FORCE_STREAMK:
         if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
         h->ov.force_streamk = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_FORCE_TF32_KERNEL:
+        if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.force_tf32_kernel = static_cast<int>(value);
         return SGEMM_OK;
     default:
         return SGEMM_ERR_INVALID_VALUE;

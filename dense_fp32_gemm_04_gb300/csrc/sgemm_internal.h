@@ -17,7 +17,8 @@ enum : int {
     kWhereDrain = 3,         // waiting for this CTA's own copies in flight ran out
     kWhereMmaEmpty = 4,      // TF32: the MMA issuer's wait for a filled stage ran out
     kWhereAccum = 5,         // TF32: the epilogue's wait for the accumulator ran out
-    kWhereTmemAlloc = 6      // TF32: TMEM allocation failed
+    kWhereTmemAlloc = 6,     // TF32: TMEM allocation failed
+    kWherePairLayout = 7     // TF32 pair: the two CTAs' shared-memory layouts differ (no work done)
 };
 
 // Everything the FFMA mainloop needs besides the two tensor maps.
@@ -48,8 +49,9 @@ struct FfmaParams {
     int skew_ns;
 };
 
-// Everything the TF32 tcgen05 mainloop needs besides the two tensor maps
-// (A: M x K, and B^T: N x K, both K-major).
+// Everything the TF32 tcgen05 mainloops need besides the two tensor maps
+// (A: M x K, and B^T: N x K, both K-major). Tiles are 128 x 256 for the
+// one-CTA kernel and 256 x 256 for the pair kernel.
 struct Tf32Params {
     int M, N, K;
     float alpha, beta;
@@ -90,6 +92,12 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int 
 cudaError_t tf32_set_attributes();
 cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
                         cudaStream_t stream);
+// CTA-pair kernel: p in units of 256 x 256 pair tiles (W slots of 256 x 256);
+// tmA box 32 x 128 rows, tmBt box 32 x 128 rows; grid = 2 x pairs.
+cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
+                             cudaStream_t stream);
+// CTA pairs of the pair kernel that fit on the current device at once (0: none).
+int tf32_pair_max_pairs();
 // XT (cols x ldxt) = X^T for X (rows x cols, row stride ldx); ldxt % 4 == 0.
 cudaError_t launch_transpose(const float *X, long long ldx, float *XT, long long ldxt, int rows, int cols,
                              cudaStream_t stream);

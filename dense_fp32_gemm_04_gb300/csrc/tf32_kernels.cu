@@ -317,12 +317,279 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel (tcgen05 .cta_group::2). A cluster of two CTAs on two SMs
+// computes 256 x 256 tiles: rank r stages rows [128 r, 128 r + 128) of the A
+// slab and rows [128 r, 128 r + 128) of the B^T slab (columns of B), both at
+// the same shared-memory offsets in the two CTAs, and holds rows
+// [128 r, 128 r + 128) of the accumulator in its own TMEM. One thread of rank 0
+// issues M = 256, N = 256 MMAs that read both CTAs' stages and write both
+// TMEMs. Barriers:
+//   full[s]      rank 0 only: both CTAs' copies of stage s complete_tx on it
+//                (rank 0 expects the bytes of both).
+//   empty[s]     both CTAs: the MMAs that read stage s committed to both.
+//   acc_full[b]  both CTAs: accumulator b holds a finished tile.
+//   acc_empty[b] rank 0 only: the 4 epilogue warps of each CTA have read
+//                accumulator b (8 arrivals, the peer's from the other SM).
+// Every wait is bounded; a CTA whose wait runs out records SGEMM_ERR_TIMEOUT
+// and stops; the two CTAs leave only through one final cluster barrier, after
+// rank 0 saw its MMAs and both CTAs' copies finish (bounded), so no CTA exits
+// while the other may still touch its shared memory or TMEM.
+constexpr int PBM = sgemm_cfg::kTf32PairBM;
+constexpr int PBN = sgemm_cfg::kTf32PairBN;
+constexpr int PHALF_M = PBM / 2, PHALF_N = PBN / 2;
+constexpr int PSTAGES = sgemm_cfg::kTf32PairStages;
+constexpr int PA_BYTES = PHALF_M * BK * 4;
+constexpr int PB_BYTES = PHALF_N * BK * 4;
+constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr uint32_t PIDESC = idesc_tf32(PBM, PBN);
+constexpr int kLayoutCode = 7 << 16;  // SGEMM_ERR_NOT_SUPPORTED << 16
+static_assert(PBN == BN, "the pair kernel's accumulator rows share the one-CTA epilogue (BN columns)");
+static_assert(sgemm_cfg::tf32_pair_smem_bytes() == 1024 + PSTAGES * PSTAGE_BYTES + 256 + sgemm_cfg::kTf32PairSlack,
+              "smem layout");
+
+struct PairBars {
+    uint64_t full[PSTAGES];
+    uint64_t empty[PSTAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t ring_offset;  // this CTA's stage-ring address, compared with the peer's
+    int abort_flag;
+    int issued[PSTAGES];
+};
+static_assert(sizeof(PairBars) <= 256, "barrier block");
+
+__device__ __forceinline__ void raise_abort_pair(PairBars *b, const Tf32Params &p, int code)
+{
+    volatile int *f = &b->abort_flag;
+    if (!*f) {
+        *f = 1;
+        report_status(p.status, code);
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBt,
+                 const Tf32Params p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t a_base = smem_addr(smem);
+    const uint32_t b_base = a_base + PSTAGES * PA_BYTES;
+    PairBars *bars = reinterpret_cast<PairBars *>(smem + PSTAGES * PSTAGE_BYTES);
+    volatile int *abort_flag = &bars->abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = static_cast<int>(cluster_id_x());
+    const int pairs = static_cast<int>(cluster_count_x());
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(smem_addr(&bars->full[s]), 1);
+            mbar_init(smem_addr(&bars->empty[s]), 1);
+            bars->issued[s] = 0;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&bars->acc_full[b]), 1);
+            mbar_init(smem_addr(&bars->acc_empty[b]), 8);
+        }
+        mbar_init(smem_addr(&bars->mma_done), 1);
+        bars->abort_flag = 0;
+        bars->ring_offset = a_base;
+        fence_barrier_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmBt);
+    }
+    if (warp == 0) {
+        tmem_alloc_pair(smem_addr(&bars->tmem_base), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any copy or arrive targets them
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    // The MMAs address both CTAs' stages by rank 0's offsets, which must therefore
+    // agree. Compared on the address bits a shared-memory descriptor holds (the
+    // offset inside the CTA's shared memory; higher bits of a shared::cta address
+    // can differ between the CTAs of a cluster).
+    constexpr uint32_t kDescAddrMask = 0x3FFFFu;
+    const uint32_t peer_ring = ld_shared_cluster_u32(mapa_shared(smem_addr(&bars->ring_offset), rank ^ 1u));
+    const bool same_layout = ((peer_ring ^ a_base) & kDescAddrMask) == 0;
+    if (!same_layout && threadIdx.x == 0) raise_abort_pair(bars, p, kLayoutCode | kWherePairLayout);
+
+    if (!same_layout) {
+        // both CTAs see the mismatch: no copies, no MMAs
+    } else if (warp == 0 && lane == 0) {
+        // ---- TMA producer (both CTAs): this CTA's halves of each stage ----
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        pdl_wait();  // B^T (and a repacked A) written by this call's previous kernels are complete
+        Work w;
+        for (int item = 0; ok && work_at_g(p, item, w, pair, pairs); ++item) {
+            const int row_a = w.tm * PBM + static_cast<int>(rank) * PHALF_M;
+            const int row_b = w.tn * PBN + static_cast<int>(rank) * PHALF_N;
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                if (!mbar_wait_bounded(smem_addr(&bars->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
+                    raise_abort_pair(bars, p, kTimeoutCode | kWhereProducerEmpty);
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = mapa_shared(smem_addr(&bars->full[stage]), 0);  // rank 0's barrier
+                if (rank == 0) mbar_arrive_expect_tx(smem_addr(&bars->full[stage]), 2 * PSTAGE_BYTES);
+                tma_load_2d_pair(a_base + stage * PA_BYTES, &tmA, full, kb * BK, row_a);
+                tma_load_2d_pair(b_base + stage * PB_BYTES, &tmBt, full, kb * BK, row_b);
+                bars->issued[stage] = 2 | static_cast<int>(phase);
+                if (++stage == PSTAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        pdl_trigger();  // every copy is issued: the call's reduction may become resident
+        // Drain. Rank 0: both CTAs' copies of every issued stage have landed (they
+        // complete on its full barriers). Both: unless aborted, the MMAs that read
+        // them have committed to this CTA's empty barriers.
+        for (int s = 0; s < PSTAGES; ++s) {
+            const int rec = bars->issued[s];
+            if (!(rec & 2)) continue;
+            const uint32_t par = static_cast<uint32_t>(rec & 1);
+            if (rank == 0 && !mbar_wait_cluster_bounded(smem_addr(&bars->full[s]), par, nullptr, p.timeout_ns)) {
+                report_status(p.status, kTimeoutCode | kWhereDrain);
+                break;
+            }
+            if (!*abort_flag && !mbar_wait_bounded(smem_addr(&bars->empty[s]), par, abort_flag, p.timeout_ns)) {
+                report_status(p.status, kTimeoutCode | kWhereDrain);
+                break;
+            }
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---- MMA issuer (rank 0 only) ----
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        Work w;
+        for (int item = 0; ok && work_at_g(p, item, w, pair, pairs); ++item, ++it) {
+            const int buf = it & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
+            if (!mbar_wait_cluster_bounded(smem_addr(&bars->acc_empty[buf]), acc_phase ^ 1u, abort_flag,
+                                           p.timeout_ns)) {
+                raise_abort_pair(bars, p, kTimeoutCode | kWhereAccum);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * PBN);
+            const int kb0 = w.kb0, kb1 = w.kb1;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_cluster_bounded(smem_addr(&bars->full[stage]), phase, abort_flag, p.timeout_ns)) {
+                    raise_abort_pair(bars, p, kTimeoutCode | kWhereMmaEmpty);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t a_s = a_base + stage * PA_BYTES;
+                const uint32_t b_s = b_base + stage * PB_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / MMA_K; ++k)
+                    mma_tf32_pair(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4),
+                                  smem_desc_k_sw128(b_s + k * MMA_K * 4), PIDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+                mma_commit_pair_both(smem_addr(&bars->empty[stage]));  // stage free in both CTAs
+                if (++stage == PSTAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mma_commit_pair_both(smem_addr(&bars->acc_full[buf]));
+        }
+        // Every MMA (they write both CTAs' TMEM) is finished before either CTA frees it.
+        mma_commit_pair_local(smem_addr(&bars->mma_done));
+        if (!mbar_wait_bounded(smem_addr(&bars->mma_done), 0u, nullptr, p.timeout_ns))
+            report_status(p.status, kTimeoutCode | kWhereDrain);
+    } else if (warp >= 2) {
+        // ---- epilogue (both CTAs): warp w reads TMEM lanes 32 * (w % 4) .. + 31 ----
+        const int quarter = warp & 3;
+        const int half_row = static_cast<int>(rank) * PHALF_M + quarter * 32 + lane;
+        int it = 0;
+        Work w;
+        for (int item = 0; work_at_g(p, item, w, pair, pairs); ++item, ++it) {
+            const int buf = it & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
+            bool ok = mbar_wait_cluster_bounded(smem_addr(&bars->acc_full[buf]), acc_phase, abort_flag, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) raise_abort_pair(bars, p, kTimeoutCode | kWhereAccum);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * PBN);
+            if (w.dest == kToPartial) {
+                // this CTA's rows of the pair's tile-packed 256 x 256 partial
+                float *wrow = p.W + static_cast<long long>(w.idx) * (PBM * PBN) + static_cast<long long>(half_row) * PBN;
+                if (p.kblocks <= kShortK)
+                    store_partial_row<4>(t_row, wrow);
+                else
+                    store_partial_row<1>(t_row, wrow);
+            } else {
+                const int row = w.tm * PBM + half_row;
+                if (p.kblocks <= kShortK)
+                    store_c_row<4>(p, t_row, row, w.tn);
+                else
+                    store_c_row<1>(p, t_row, row, w.tn);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&bars->acc_empty[buf]), 0));  // rank 0's
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still use its barriers, stages or TMEM
+    tc_fence_after_sync();
+    if (warp == 0) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
 }  // namespace
 
 cudaError_t tf32_set_attributes()
 {
-    return cudaFuncSetAttribute(tf32_sgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                sgemm_cfg::tf32_smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(tf32_sgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         sgemm_cfg::tf32_smem_bytes());
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tf32_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                sgemm_cfg::tf32_pair_smem_bytes());
+}
+
+int tf32_pair_max_pairs()
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = sgemm_cfg::tf32_pair_smem_bytes();
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, tf32_pair_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return clusters;
+}
+
+cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
+                             cudaStream_t stream)
+{
+    // grid = 2 x pairs; clusters of two come from the kernel's __cluster_dims__
+    return launch_kernel(true, tf32_pair_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_pair_smem_bytes(), stream,
+                         tmA, tmBt, p);
 }
 
 cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,

@@ -56,4 +56,20 @@ constexpr int tf32_smem_bytes()
     return 1024 + kTf32Stages * (kTf32BM + kTf32BN) * kTf32BK * 4 + 256;
 }
 
+// TF32 on CTA pairs (tcgen05 .cta_group::2): a pair of CTAs on two SMs computes
+// a 256 x 256 tile (M = 256, N = 256 per MMA); each CTA stages 128 rows of A
+// and 128 columns of B (32 KiB per stage, 6 stages) and holds its 128 rows of
+// the accumulator, so per SM the tensor core reads a third less shared memory
+// per FMA than with one CTA per 128 x 256 tile.
+constexpr int kTf32PairBM = 256, kTf32PairBN = 256, kTf32PairStages = 6;
+// 1 KiB for aligning the ring, the ring, the barrier block, and one B half-stage
+// (16 KiB) of slack that no instruction writes: any read past the last stage by
+// an operand larger than intended stays inside the CTA's shared memory.
+constexpr int kTf32PairSlack = (kTf32PairBN / 2) * kTf32BK * 4;
+constexpr int tf32_pair_smem_bytes()
+{
+    return 1024 + kTf32PairStages * (kTf32PairBM / 2 + kTf32PairBN / 2) * kTf32BK * 4 + 256 + kTf32PairSlack;
+}
+static_assert(tf32_pair_smem_bytes() <= 227 * 1024, "shared memory per CTA");
+
 }  // namespace sgemm_cfg

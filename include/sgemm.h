@@ -76,7 +76,9 @@ typedef enum sgemm_kernel_kind {
 /* What sgemm_run does for one problem (filled by sgemm_plan / sgemm_last_plan). */
 typedef struct sgemm_plan_s {
     int kernel;              /* sgemm_kernel_kind_t */
-    int config;              /* row of the tile-config table, -1 if none */
+    int config;              /* FFMA: row of the tile-config table; TF32: 0 = one CTA per 128 x 256
+                                tile, 1 = CTA pair per 256 x 256 tile (grid counts CTAs, sk_grid
+                                pairs); -1 if none */
     int bm, bn, bk, stages;  /* CTA tile and pipeline depth */
     int threads;             /* threads per CTA */
     int ctas_per_sm;         /* resident CTAs per SM the grid is sized for */
@@ -96,7 +98,8 @@ typedef struct sgemm_plan_s {
                                 whole tiles) form one span of k-blocks cut evenly over the grid's
                                 CTAs; tiles shared by two or more CTAs are reduced in k order
                                 (0 = none) */
-    int sk_grid;             /* CTAs sharing the stream-K span (the first sk_grid of the grid) */
+    int sk_grid;             /* workers sharing the stream-K span (the first sk_grid CTAs, or CTA
+                                pairs for the TF32 pair kernel) */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */
@@ -113,8 +116,12 @@ typedef enum sgemm_option {
                                      before it releases a slab; |value| <= 100000, 0 = off */
     SGEMM_OPT_FORCE_TRANSPOSE_A = 7,/* FP32 path: -1 = automatic (the default), 0 = read A as given,
                                      1 = always transpose A first (same results either way) */
-    SGEMM_OPT_FORCE_STREAMK = 8   /* -1 = automatic (the default), 0 = never, 1 = whenever the last
+    SGEMM_OPT_FORCE_STREAMK = 8,  /* -1 = automatic (the default), 0 = never, 1 = whenever the last
                                      round of tiles is partial (ignored with forced splits) */
+    SGEMM_OPT_FORCE_TF32_KERNEL = 9 /* TF32 mode: -1 = automatic (the default), 0 = one CTA per
+                                     128 x 256 tile, 1 = a CTA pair (cluster of two, tcgen05
+                                     .cta_group::2) per 256 x 256 tile; 1 fails with
+                                     SGEMM_ERR_NOT_SUPPORTED where no pair fits */
 } sgemm_option_t;
 
 /*
@@ -127,8 +134,9 @@ typedef enum sgemm_option {
  * sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
- * SGEMM_FORCE_SPLITS=<S>, SGEMM_FORCE_TRANSPOSE_A=<-1|0|1> and
- * SGEMM_FORCE_STREAMK=<-1|0|1> preset the planner overrides of sgemm_set_option.
+ * SGEMM_FORCE_SPLITS=<S>, SGEMM_FORCE_TRANSPOSE_A=<-1|0|1>,
+ * SGEMM_FORCE_STREAMK=<-1|0|1> and SGEMM_FORCE_TF32_KERNEL=<-1|0|1> preset the
+ * planner overrides of sgemm_set_option.
  */
 int sgemm_create(sgemm_handle_t *out);
 

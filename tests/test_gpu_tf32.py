@@ -7,7 +7,8 @@ TF32 (relative error below 2^-10, so a product is off by below 2^-9 + 2^-20),
 then K products are summed in FP32 (depth K + 2 with alpha/beta):
 |err| <= (2^-9 + 2^-20 + (K + 2) * 2^-24) * magnitude. A wrong descriptor or
 layout would fail the tight bound by orders of magnitude. Integer operands in
-{-2..2} are exact in TF32, so those runs must be bit-exact.
+{-2..2} are exact in TF32, so those runs must be bit-exact. Every case runs on
+both TF32 kernels (one CTA per tile, and CTA pairs).
 """
 
 import numpy as np
@@ -22,8 +23,10 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.fixture(scope="module")
-def h():
+@pytest.fixture(scope="module", params=[0, 1], ids=["one_cta", "cta_pair"])
+def h(request):
+    """A TF32-mode handle forced to one kernel: 0 = one CTA per 128 x 256 tile,
+    1 = a CTA pair (cluster of two, tcgen05 .cta_group::2) per 256 x 256 tile."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from dense_fp32_gemm_04_gb300 import _build
@@ -31,8 +34,17 @@ def h():
     _build.build()
     handle = sg.Sgemm(0)
     handle.set_math_mode(sg.MATH_TF32)
+    handle.set_option(sg.OPT_FORCE_TF32_KERNEL, request.param)
+    handle.tf32_kernel = request.param
     yield handle
     handle.close()
+
+
+def _assert_kernel(h):
+    plan = h.last_plan()
+    assert plan.kernel == sg.KERNEL_TF32 and plan.config == h.tf32_kernel, plan.as_dict()
+    if plan.config == 1:
+        assert (plan.bm, plan.bn) == (256, 256) and plan.grid % 2 == 0
 
 
 def _check(got, A, B, C, alpha, beta, rows=None, exact=False):
@@ -50,14 +62,13 @@ def _check(got, A, B, C, alpha, beta, rows=None, exact=False):
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (128, 256, 32), (129, 257, 33), (256, 256, 256), (300, 500, 200),
-                                   (77, 1000, 517)])
+                                   (77, 1000, 517), (520, 1030, 96)])
 def test_integer_exact(h, shape):
     M, N, K = shape
     A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=M + N + K, dist=("int", "int", "int"))
     got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
     assert st == sg.SGEMM_OK and guards
-    plan = h.last_plan()
-    assert plan.kernel == sg.KERNEL_TF32
+    _assert_kernel(h)
     assert h.check_device_status() == (sg.SGEMM_OK, 0)
     _check(got, A, B, C, 1.5, 0.5, exact=True)
 
@@ -93,6 +104,7 @@ def test_square4096(h, name):
     A, B, C = inputs.problem_operands(name)
     got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
     assert st == sg.SGEMM_OK and guards
+    _assert_kernel(h)
     assert h.check_device_status() == (sg.SGEMM_OK, 0)
     _check(got, A, B, C, p["alpha"], p["beta"], rows=sample_rows(p["M"]), exact=name.endswith("_int"))
 
@@ -134,7 +146,8 @@ def _stream_k_case(h, shape):
     got, guards, st = run_gemm(torch, h, A, B, C, 1.5, 0.5)
     assert st == sg.SGEMM_OK and guards
     plan = h.last_plan()
-    assert plan.kernel == sg.KERNEL_TF32 and plan.sk_tiles > 0 and plan.launches == 3 + plan.repack_a, plan.as_dict()
+    _assert_kernel(h)
+    assert plan.sk_tiles > 0 and plan.launches == 3 + plan.repack_a, plan.as_dict()
     rows = sample_rows(M) if M > 1024 else None
     _check(got, A, B, C, 1.5, 0.5, rows=rows, exact=True)
     Ar, Br, Cr = inputs.problem_operands(M=M, N=N, K=K, seed=M + K + 1, dist=("normal", "uniform", "uniform"))
