@@ -207,12 +207,31 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_byte_addr)
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma .kind::tf32: D format F32 (bits 4-5 = 1),
-// A and B format TF32 (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
+// Shared-memory matrix descriptor of an MN-major TF32 operand tile (MN
+// contiguous), written by TMA in boxes of 32 MN x 32 K with the 128-byte
+// swizzle of 32-byte chunks (the swizzle this operand form takes): a box is 32
+// K-rows of 128 bytes; boxes along MN are `lbo` bytes apart (leading byte
+// offset). The stride byte offset between K-row groups is 512 bytes: the rows
+// are contiguous, so that holds for groups of 4 rows, and a K = 8 MMA stays
+// inside one group of 8. Version 1, layout type 1 = 128-byte swizzle with
+// 32-byte atoms.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128_32b(uint32_t smem_byte_addr, uint32_t lbo)
 {
-    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+    uint64_t d = static_cast<uint64_t>((smem_byte_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(512 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(1) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma .kind::tf32: D format F32 (bits 4-5 = 1),
+// A and B format TF32 (bits 7-9 and 10-12 = 2), A K-major (bit 15 = 0), B K-major
+// (bit 16 = 0) or MN-major (bit 16 = 1, b_mn), N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn = false)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 

@@ -206,8 +206,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     out->repack_b = b_ok ? 0 : 1;
     out->vec_c = ((q.align_flags & 4) && q.ldc % 4 == 0) ? 1 : 0;
     if (q.math_mode == SGEMM_MATH_TF32) {
-        // B always goes through the workspace: transposed to K-major (N x roundup(K, 4)).
-        if (q.K > 65535LL * 64) return SGEMM_ERR_NOT_SUPPORTED;
+        // A is read K-major and B MN-major as stored (repacked only when not 16-byte aligned).
         const long long pairs = q.num_pairs > 0 ? q.num_pairs : (q.num_pairs == 0 ? q.num_sms / 2 : 0);
         const bool beta_read = q.beta != 0.0f;
         const Tf32Model one = model_tf32(q.M, q.N, q.K, sgemm_cfg::kTf32BM, sgemm_cfg::kTf32BN, q.num_sms,
@@ -234,7 +233,6 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         out->threads = sgemm_cfg::kTf32Threads;
         out->ctas_per_sm = 1;
         out->splits = 1;
-        out->repack_b = 1;
         out->tiles_m = static_cast<int>(ceil_div(q.M, out->bm));
         out->tiles_n = static_cast<int>(ceil_div(q.N, out->bn));
         const long long units = static_cast<long long>(out->tiles_m) * out->tiles_n;
@@ -256,7 +254,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
             }
         }
         out->workspace_bytes = workspace_layout(q, *out).total;
-        out->launches = 1 + out->repack_a + 1 + (out->sk_tiles > 0 ? 1 : 0);
+        out->launches = out->repack_a + out->repack_b + 1 + (out->sk_tiles > 0 ? 1 : 0);
         return SGEMM_OK;
     }
 
@@ -326,12 +324,7 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
         w.a_off = off;
         off += round_up(static_cast<long long>(q.M) * w.lda * 4, 256);
     }
-    if (p.kernel == SGEMM_KERNEL_TF32) {
-        // B^T, K-major: N rows of roundup(K, 4) floats.
-        w.ldb = round_up(q.K, 4);
-        w.b_off = off;
-        off += round_up(static_cast<long long>(q.N) * w.ldb * 4, 256);
-    } else if (p.repack_b) {
+    if (p.repack_b) {
         w.ldb = round_up(q.N, 4);
         w.b_off = off;
         off += round_up(static_cast<long long>(q.K) * w.ldb * 4, 256);

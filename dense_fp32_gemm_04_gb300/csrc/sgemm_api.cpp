@@ -131,31 +131,37 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
                  p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.sk_tiles);
 }
 
-// TF32 tensor-core path: [repack A] -> transpose B to K-major -> tcgen05 mainloop
-// (one CTA per 128 x 256 tile, or a CTA pair per 256 x 256 tile) [-> stream-K reduction].
+// TF32 tensor-core path: [repack A] [repack B] -> tcgen05 mainloop (one CTA per
+// 128 x 256 tile, or a CTA pair per 256 x 256 tile) [-> stream-K reduction].
 int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int M, int N, int K, float alpha,
              const float *A, int lda, const float *B, int ldb, float beta, float *C, int ldc, cudaStream_t stream)
 {
     char *ws = static_cast<char *>(h->workspace);
-    const float *a_src = A;
-    long long a_ld = lda;
+    const float *a_src = A, *b_src = B;
+    long long a_ld = lda, b_ld = ldb;
     if (plan.repack_a) {
         float *dst = reinterpret_cast<float *>(ws + w.a_off);
         if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_src = dst;
         a_ld = w.lda;
     }
-    float *bt = reinterpret_cast<float *>(ws + w.b_off);
-    if (launch_transpose(B, ldb, bt, w.ldb, K, N, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    CUtensorMap tmA, tmBt;
+    if (plan.repack_b) {
+        float *dst = reinterpret_cast<float *>(ws + w.b_off);
+        if (launch_repack(B, ldb, dst, w.ldb, K, N, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        b_src = dst;
+        b_ld = w.ldb;
+    }
+    CUtensorMap tmA, tmB;
     int rc;
-    // Boxes: a CTA's rows of the tile (the pair kernel's CTAs stage half of A's and half of B's rows each).
+    // A box: a CTA's rows of the tile (the pair kernel's CTAs stage 128 rows each);
+    // B box: 32 columns x 32 k, read MN-major with the 128-byte swizzle of 32-byte
+    // chunks (the kernels issue one per 32 columns).
     const bool pair = plan.config == 1;
-    const int box_a = pair ? plan.bm / 2 : plan.bm, box_b = pair ? plan.bn / 2 : plan.bn;
+    const int box_a = pair ? plan.bm / 2 : plan.bm;
     if ((rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kTf32BK, box_a, CU_TENSOR_MAP_SWIZZLE_128B)) !=
         SGEMM_OK)
         return rc;
-    if ((rc = make_tmap(h, &tmBt, bt, K, N, w.ldb, sgemm_cfg::kTf32BK, box_b, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+    if ((rc = make_tmap(h, &tmB, b_src, N, K, b_ld, 32, sgemm_cfg::kTf32BK, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) !=
         SGEMM_OK)
         return rc;
     Tf32Params p{};
@@ -179,8 +185,9 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         p.sk_tiles = plan.sk_tiles;
         p.sk_grid = plan.sk_grid;
     }
-    const cudaError_t le =
-        pair ? launch_tf32_pair(tmA, tmBt, p, plan.grid, stream) : launch_tf32(tmA, tmBt, p, plan.grid, stream);
+    const bool dependent = plan.repack_a || plan.repack_b;
+    const cudaError_t le = pair ? launch_tf32_pair(tmA, tmB, p, plan.grid, stream, dependent)
+                                : launch_tf32(tmA, tmB, p, plan.grid, stream, dependent);
     if (le != cudaSuccess) return SGEMM_ERR_LAUNCH;
     if (plan.sk_tiles > 0) {
         // Same raster and tile-packed partial layout as the FP32 stream-K span.

@@ -50,8 +50,8 @@ struct FfmaParams {
 };
 
 // Everything the TF32 tcgen05 mainloops need besides the two tensor maps
-// (A: M x K, and B^T: N x K, both K-major). Tiles are 128 x 256 for the
-// one-CTA kernel and 256 x 256 for the pair kernel.
+// (A: M rows of K, read K-major; B: K rows of N, read MN-major). Tiles are
+// 128 x 256 for the one-CTA kernel and 256 x 256 for the pair kernel.
 struct Tf32Params {
     int M, N, K;
     float alpha, beta;
@@ -90,12 +90,15 @@ cudaError_t launch_min2(const float *C, long long ldc, int M, int N, void *cand,
 cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int num_sms,
                          cudaStream_t stream);
 cudaError_t tf32_set_attributes();
-cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
-                        cudaStream_t stream);
+// tmA: box 32 k x 128 rows (128-byte swizzle); tmB: box 32 n x 32 k (128-byte
+// swizzle). dependent: launched as a programmatic dependent of the call's
+// previous kernel (an operand repack).
+cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
+                        cudaStream_t stream, bool dependent);
 // CTA-pair kernel: p in units of 256 x 256 pair tiles (W slots of 256 x 256);
-// tmA box 32 x 128 rows, tmBt box 32 x 128 rows; grid = 2 x pairs.
-cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
-                             cudaStream_t stream);
+// same tensor maps; grid = 2 x pairs.
+cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
+                             cudaStream_t stream, bool dependent);
 // CTA pairs of the pair kernel that fit on the current device at once (0: none).
 int tf32_pair_max_pairs();
 // XT (cols x ldxt) = X^T for X (rows x cols, row stride ldx); ldxt % 4 == 0.

@@ -6,8 +6,9 @@
 // Structure (one CTA per SM, persistent over 128 x 256 output tiles, walking
 // the work sequence of schedule.cuh: whole tiles, then the CTA's K slice of
 // a stream-K span whose partial tiles sk_reduce_kernel adds in k order):
-//   warp 0      TMA producer: A box (32 k x 128 rows) and B^T box (32 k x 256
-//               columns), both with the 128-byte swizzle, into a 4-stage ring.
+//   warp 0      TMA producer: A box (32 k x 128 rows, K-major, 128-byte
+//               swizzle) and eight B boxes (32 n x 32 k each, MN-major: B as
+//               stored, 128-byte swizzle of 32-byte chunks) into a 4-stage ring.
 //   warp 1      MMA issuer: one thread issues 4 tcgen05.mma (K = 8 each) per
 //               stage into one of two TMEM accumulators (128 lanes x 256
 //               columns each), commits the stage back to the producer, and
@@ -16,9 +17,9 @@
 //               accumulator, alpha/beta, stores to C; then hand the
 //               accumulator back so the next tile's MMAs overlap this one's
 //               stores.
-// Both operands must be K-major for this instruction form: A (row-major M x K)
-// already is; B (row-major K x N) is first transposed into the handle's
-// workspace (transpose_kernel, ffma_kernels.cu).
+// A (row-major M x K) is read K-major, B (row-major K x N) MN-major, both as the
+// caller stores them (an operand whose base or row stride is not 16-byte
+// aligned is first repacked into the handle's workspace).
 //
 // All waits are bounded; on expiry the CTA records SGEMM_ERR_TIMEOUT, lets its
 // copies and MMAs in flight finish (bounded), frees its TMEM and returns.
@@ -44,7 +45,11 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = sgemm_cfg::kTf32Threads;
 constexpr int MMA_K = 8;                  // K of one tcgen05.mma .kind::tf32
 constexpr uint32_t TMEM_COLS = 2 * BN;    // two accumulators
-constexpr uint32_t IDESC = idesc_tf32(BM, BN);
+constexpr uint32_t IDESC = idesc_tf32(BM, BN, true);
+// B is staged MN-major in boxes of 32 n x 32 k (4 KiB, 128-byte swizzle of 32-byte
+// chunks), boxes along n 4 KiB apart.
+constexpr int kBoxN = 32;
+constexpr int B_BOX_BYTES = kBoxN * BK * 4;
 static_assert(sgemm_cfg::tf32_smem_bytes() == 1024 + STAGES * STAGE_BYTES + 256, "smem layout");
 static_assert(TMEM_COLS == 512, "two 128 x 256 FP32 accumulators fill TMEM");
 
@@ -150,7 +155,7 @@ __device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row,
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBt,
+tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const Tf32Params p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -177,7 +182,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         bars->abort_flag = 0;
         fence_barrier_init();
         prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmBt);
+        prefetch_tensormap(&tmB);
     }
     if (warp == 0) {
         tmem_alloc(smem_addr(&bars->tmem_base), TMEM_COLS);
@@ -193,7 +198,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        pdl_wait();  // B^T (and a repacked A) written by this call's previous kernels are complete
+        pdl_wait();  // operands repacked by this call's previous kernel are complete
         Work w;
         for (int item = 0; ok && work_at(p, item, w); ++item) {
             const int tm = w.tm, tn = w.tn;
@@ -206,7 +211,9 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 mbar_arrive_expect_tx(full, STAGE_BYTES);
                 tma_load_2d(a_base + stage * A_BYTES, &tmA, full, kb * BK, tm * BM);
-                tma_load_2d(b_base + stage * B_BYTES, &tmBt, full, kb * BK, tn * BN);
+#pragma unroll
+                for (int j = 0; j < BN / kBoxN; ++j)
+                    tma_load_2d(b_base + stage * B_BYTES + j * B_BOX_BYTES, &tmB, full, tn * BN + j * kBoxN, kb * BK);
                 bars->issued[stage] = 2 | static_cast<int>(phase);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -249,9 +256,10 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t b_s = b_base + stage * B_BYTES;
 #pragma unroll
                 for (int k = 0; k < BK / MMA_K; ++k) {
-                    // K advances 8 TF32 = 32 bytes inside the 128-byte swizzle atom.
-                    mma_tf32(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4), smem_desc_k_sw128(b_s + k * MMA_K * 4),
-                             IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+                    // A: K advances 8 TF32 = 32 bytes inside the 128-byte swizzle atom;
+                    // B: one 8-row (8 k) group = 1024 bytes.
+                    mma_tf32(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4),
+                             smem_desc_mn_sw128_32b(b_s + k * 1024, B_BOX_BYTES), IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
                 }
                 mma_commit(smem_addr(&bars->empty[stage]));  // stage free once these MMAs are done
                 if (++stage == STAGES) {
@@ -320,8 +328,9 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 // ---------------------------------------------------------------------------
 // CTA-pair kernel (tcgen05 .cta_group::2). A cluster of two CTAs on two SMs
 // computes 256 x 256 tiles: rank r stages rows [128 r, 128 r + 128) of the A
-// slab and rows [128 r, 128 r + 128) of the B^T slab (columns of B), both at
-// the same shared-memory offsets in the two CTAs, and holds rows
+// slab (K-major) and columns [128 r, 128 r + 128) of the B slab (MN-major, four
+// 32 n x 32 k boxes), both at the same shared-memory offsets in the two CTAs,
+// and holds rows
 // [128 r, 128 r + 128) of the accumulator in its own TMEM. One thread of rank 0
 // issues M = 256, N = 256 MMAs that read both CTAs' stages and write both
 // TMEMs. Barriers:
@@ -342,7 +351,7 @@ constexpr int PSTAGES = sgemm_cfg::kTf32PairStages;
 constexpr int PA_BYTES = PHALF_M * BK * 4;
 constexpr int PB_BYTES = PHALF_N * BK * 4;
 constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
-constexpr uint32_t PIDESC = idesc_tf32(PBM, PBN);
+constexpr uint32_t PIDESC = idesc_tf32(PBM, PBN, true);
 constexpr int kLayoutCode = 7 << 16;  // SGEMM_ERR_NOT_SUPPORTED << 16
 static_assert(PBN == BN, "the pair kernel's accumulator rows share the one-CTA epilogue (BN columns)");
 static_assert(sgemm_cfg::tf32_pair_smem_bytes() == 1024 + PSTAGES * PSTAGE_BYTES + 256 + sgemm_cfg::kTf32PairSlack,
@@ -371,7 +380,7 @@ __device__ __forceinline__ void raise_abort_pair(PairBars *b, const Tf32Params &
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBt,
+tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const Tf32Params p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -402,7 +411,7 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         bars->ring_offset = a_base;
         fence_barrier_init();
         prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmBt);
+        prefetch_tensormap(&tmB);
     }
     if (warp == 0) {
         tmem_alloc_pair(smem_addr(&bars->tmem_base), TMEM_COLS);
@@ -429,11 +438,11 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        pdl_wait();  // B^T (and a repacked A) written by this call's previous kernels are complete
+        pdl_wait();  // operands repacked by this call's previous kernel are complete
         Work w;
         for (int item = 0; ok && work_at_g(p, item, w, pair, pairs); ++item) {
             const int row_a = w.tm * PBM + static_cast<int>(rank) * PHALF_M;
-            const int row_b = w.tn * PBN + static_cast<int>(rank) * PHALF_N;
+            const int col_b = w.tn * PBN + static_cast<int>(rank) * PHALF_N;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!mbar_wait_bounded(smem_addr(&bars->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
                     raise_abort_pair(bars, p, kTimeoutCode | kWhereProducerEmpty);
@@ -443,7 +452,10 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const uint32_t full = mapa_shared(smem_addr(&bars->full[stage]), 0);  // rank 0's barrier
                 if (rank == 0) mbar_arrive_expect_tx(smem_addr(&bars->full[stage]), 2 * PSTAGE_BYTES);
                 tma_load_2d_pair(a_base + stage * PA_BYTES, &tmA, full, kb * BK, row_a);
-                tma_load_2d_pair(b_base + stage * PB_BYTES, &tmBt, full, kb * BK, row_b);
+#pragma unroll
+                for (int j = 0; j < PHALF_N / kBoxN; ++j)
+                    tma_load_2d_pair(b_base + stage * PB_BYTES + j * B_BOX_BYTES, &tmB, full, col_b + j * kBoxN,
+                                     kb * BK);
                 bars->issued[stage] = 2 | static_cast<int>(phase);
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -498,7 +510,8 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                 for (int k = 0; k < BK / MMA_K; ++k)
                     mma_tf32_pair(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4),
-                                  smem_desc_k_sw128(b_s + k * MMA_K * 4), PIDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+                                  smem_desc_mn_sw128_32b(b_s + k * 1024, B_BOX_BYTES), PIDESC,
+                                  (kb != kb0 || k != 0) ? 1u : 0u);
                 mma_commit_pair_both(smem_addr(&bars->empty[stage]));  // stage free in both CTAs
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -584,20 +597,19 @@ int tf32_pair_max_pairs()
     return clusters;
 }
 
-cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
-                             cudaStream_t stream)
+cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
+                             cudaStream_t stream, bool dependent)
 {
     // grid = 2 x pairs; clusters of two come from the kernel's __cluster_dims__
-    return launch_kernel(true, tf32_pair_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_pair_smem_bytes(), stream,
-                         tmA, tmBt, p);
+    return launch_kernel(dependent, tf32_pair_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_pair_smem_bytes(),
+                         stream, tmA, tmB, p);
 }
 
-cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmBt, const Tf32Params &p, int grid,
-                        cudaStream_t stream)
+cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
+                        cudaStream_t stream, bool dependent)
 {
-    // always right after this call's B transposition: launched as its programmatic dependent
-    return launch_kernel(true, tf32_sgemm_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_smem_bytes(), stream,
-                         tmA, tmBt, p);
+    return launch_kernel(dependent, tf32_sgemm_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_smem_bytes(),
+                         stream, tmA, tmB, p);
 }
 
 }  // namespace sgemm_impl

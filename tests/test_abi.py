@@ -184,12 +184,16 @@ def test_tf32_plan(lib):
     p = sg.plan(4096, 4096, 4096, math_mode=sg.MATH_TF32)
     # CTA pairs: 256 x 256 tiles, 76 pairs on 152 SMs
     assert p.kernel == sg.KERNEL_TF32 and p.config == 1 and (p.bm, p.bn, p.bk) == (256, 256, 32)
-    assert p.repack_b == 1 and p.grid == 152 and p.transpose_a == 0
+    # A read K-major and B MN-major as stored: no operand copy
+    assert p.repack_a == 0 and p.repack_b == 0 and p.grid == 152 and p.transpose_a == 0
     # 256 tiles on 76 pairs: 3 whole rounds, then the 28 remaining tiles as a stream-K span
     assert p.units == 228 and p.sk_tiles == 28
     assert p.sk_grid == 56  # 2 equal K slices per span tile, one per pair
-    assert p.launches == 3  # B transpose, mainloop, stream-K reduction
-    assert p.workspace_bytes >= 4096 * 4096 * 4 + 2 * 56 * 256 * 256 * 4
+    assert p.launches == 2  # mainloop, stream-K reduction
+    assert p.workspace_bytes == 2 * 56 * 256 * 256 * 4
+    # an unaligned B (ldb not a multiple of 4) is repacked first
+    p = sg.plan(4096, 4095, 4096, ldb=4095, ldc=4096, math_mode=sg.MATH_TF32)
+    assert p.repack_b == 1 and p.launches == p.repack_a + 2 + (1 if p.sk_tiles else 0)
     # an odd SM count: pairs = floor(SMs / 2), the grid is whole pairs
     p = sg.plan(4096, 4096, 4096, num_sms=151, math_mode=sg.MATH_TF32)
     assert p.config == 1 and p.grid == 150
@@ -202,4 +206,4 @@ def test_tf32_single_cta_plan(lib):
     assert p.tiles_m == 1 and p.tiles_n == 16
     assert p.units + p.sk_tiles == 16 and p.grid <= 152
     if p.sk_tiles:
-        assert p.grid == p.sk_grid and p.workspace_bytes >= 4096 * 4096 * 4 + 2 * p.sk_grid * 128 * 256 * 4
+        assert p.grid == p.sk_grid and p.workspace_bytes >= 2 * p.sk_grid * 128 * 256 * 4
