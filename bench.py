@@ -31,7 +31,7 @@ METRIC = "SGEMM TFLOP/s at M=N=K=4096 FP32 and % of GB300 FP32 FFMA peak"
 WORKLOAD = "square4096"
 L2_BYTES = 126 * 2**20  # GB300 L2 (nvidia-smi reports ~126 MiB)
 KERNEL_SOURCES = ["dense_fp32_gemm_04_gb300/csrc/ffma_kernels.cu", "dense_fp32_gemm_04_gb300/csrc/device_ptx.cuh",
-                  "dense_fp32_gemm_04_gb300/csrc/tile_table.h"]
+                  "dense_fp32_gemm_04_gb300/csrc/schedule.cuh", "dense_fp32_gemm_04_gb300/csrc/tile_table.h"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "ffma_sgemm_4096_traffic.md")
 
 

@@ -86,7 +86,8 @@ bool transpose_pays(const Problem &q, double t_main)
 // call. (A span spread over all workers, as on the FP32 path, gives two partials
 // per worker: the TF32 epilogue writes those slower than it saves, 4096^3 219 ->
 // 237 us with one CTA per tile.) Rates: FLOP/s per worker as measured for each
-// kernel; ~5.5 TB/s for the reduction.
+// kernel; C at ~5.5 TB/s, the partial tiles (written, then read back within
+// microseconds, mostly from L2) at twice that.
 struct Tf32Model {
     double time;
     int slices;  // St, 0 = no stream-K
@@ -108,8 +109,9 @@ Tf32Model model_tf32(int M, int N, int K, int bm, int bn, long long slots, doubl
     int best = 0;
     for (int st = 2; st <= 8 && st <= kb && rem * st <= slots; ++st) {
         const double t_span_round = (static_cast<double>(ceil_div(kb, st)) + 1.5) * t_kb;
-        const double bytes = (2.0 * st + (beta_read ? 2.0 : 1.0)) * 4.0 * static_cast<double>(rem) * tile_elems;
-        const double gain = t_last - t_span_round - bytes / hbm - 2.5e-6;
+        const double part_bytes = 2.0 * st * 4.0 * static_cast<double>(rem) * tile_elems;
+        const double c_bytes = (beta_read ? 2.0 : 1.0) * 4.0 * static_cast<double>(rem) * tile_elems;
+        const double gain = t_last - t_span_round - part_bytes / (2.0 * hbm) - c_bytes / hbm - 2.5e-6;
         if (gain > best_gain) {
             best_gain = gain;
             best = st;
@@ -118,11 +120,11 @@ Tf32Model model_tf32(int M, int N, int K, int bm, int bn, long long slots, doubl
     return {best > 0 ? base - best_gain : base, best};
 }
 
-// Measured mainloop rates (4096^3, GB300): one CTA per tile ~650 TFLOP/s on
-// 152 SMs.
+// Measured mainloop rates (GB300, 6144^3 and 8192^3 without stream-K): one CTA
+// per tile ~660 TFLOP/s on 152 SMs; a CTA pair does 1.33-1.34x the work of two
+// SMs of the one-CTA kernel (a third less shared-memory traffic per FMA).
 constexpr double kTf32FlopsPerSm = 650e12 / 152.0;
-// CTA pair: per pair, relative to two SMs of the one-CTA kernel.
-constexpr double kTf32PairGain = 1.30;
+constexpr double kTf32PairGain = 1.33;
 
 }  // namespace
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include "../../include/sgemm.h"
+#include "tf32_tiles.h"
 #include "tile_table.h"
 
 namespace sgemm_impl {

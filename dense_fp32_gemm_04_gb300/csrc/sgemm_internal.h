@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "tf32_tiles.h"
 #include "tile_table.h"
 
 namespace sgemm_impl {

@@ -28,6 +28,7 @@
 #include <cstdint>
 
 #include "device_ptx.cuh"
+#include "tcgen05_ptx.cuh"
 #include "schedule.cuh"
 #include "sgemm_internal.h"
 
@@ -141,13 +142,20 @@ __device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row,
                 *reinterpret_cast<float4 *>(crow + colb + 4 * q) = out;
             }
         } else {
-            // N edge or C not 16-byte accessible: element by element
+            // N edge or C not 16-byte accessible: element by element, every C load of
+            // the step issued before any use (one memory latency per step, not one per
+            // element)
+            float c[16 * NB];
+            if (p.beta != 0.0f) {
+#pragma unroll
+                for (int q = 0; q < 16 * NB; ++q) c[q] = colb + q < p.N ? crow[colb + q] : 0.0f;
+            }
 #pragma unroll
             for (int q = 0; q < 16 * NB; ++q) {
                 const int col = colb + q;
                 if (col < p.N) {
                     const float a = __uint_as_float(v[q >> 4][q & 15]);
-                    crow[col] = (p.beta != 0.0f) ? fmaf(p.alpha, a, p.beta * crow[col]) : p.alpha * a;
+                    crow[col] = (p.beta != 0.0f) ? fmaf(p.alpha, a, p.beta * c[q]) : p.alpha * a;
                 }
             }
         }
@@ -354,8 +362,7 @@ constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr uint32_t PIDESC = idesc_tf32(PBM, PBN, true);
 constexpr int kLayoutCode = 7 << 16;  // SGEMM_ERR_NOT_SUPPORTED << 16
 static_assert(PBN == BN, "the pair kernel's accumulator rows share the one-CTA epilogue (BN columns)");
-static_assert(sgemm_cfg::tf32_pair_smem_bytes() == 1024 + PSTAGES * PSTAGE_BYTES + 256 + sgemm_cfg::kTf32PairSlack,
-              "smem layout");
+static_assert(sgemm_cfg::tf32_pair_smem_bytes() == 1024 + PSTAGES * PSTAGE_BYTES + 256, "smem layout");
 
 struct PairBars {
     uint64_t full[PSTAGES];

@@ -1,4 +1,4 @@
-// The tile-config table: every CTA shape the library instantiates. The
+// The tile-config table: every FFMA CTA shape the library instantiates. The
 // planner (planner.cpp) picks a row and a split-K factor per problem; the
 // kernels (ffma_kernels.cu) instantiate exactly these rows, in this order,
 // and static_assert that their shared-memory sizes match.
@@ -47,29 +47,5 @@ constexpr TileConfig kFfmaConfigs[] = {
     make_ffma(64, 64, 4, 3, 1.430f),    // 3: tiny problems (1.5 consumer warps per scheduler)
 };
 constexpr int kNumFfmaConfigs = sizeof(kFfmaConfigs) / sizeof(kFfmaConfigs[0]);
-
-// The flagged TF32 tensor-core mode: one CTA per SM computes 128 x 256 tiles
-// (tcgen05.mma M = 128, N = 256) from 32-deep K slabs in a 4-stage ring.
-constexpr int kTf32BM = 128, kTf32BN = 256, kTf32BK = 32, kTf32Stages = 4, kTf32Threads = 192;
-constexpr int tf32_smem_bytes()
-{
-    return 1024 + kTf32Stages * (kTf32BM + kTf32BN) * kTf32BK * 4 + 256;
-}
-
-// TF32 on CTA pairs (tcgen05 .cta_group::2): a pair of CTAs on two SMs computes
-// a 256 x 256 tile (M = 256, N = 256 per MMA); each CTA stages 128 rows of A
-// and 128 columns of B (32 KiB per stage, 6 stages) and holds its 128 rows of
-// the accumulator, so per SM the tensor core reads a third less shared memory
-// per FMA than with one CTA per 128 x 256 tile.
-constexpr int kTf32PairBM = 256, kTf32PairBN = 256, kTf32PairStages = 6;
-// 1 KiB for aligning the ring, the ring, the barrier block, and one B half-stage
-// (16 KiB) of slack that no instruction writes: any read past the last stage by
-// an operand larger than intended stays inside the CTA's shared memory.
-constexpr int kTf32PairSlack = (kTf32PairBN / 2) * kTf32BK * 4;
-constexpr int tf32_pair_smem_bytes()
-{
-    return 1024 + kTf32PairStages * (kTf32PairBM / 2 + kTf32PairBN / 2) * kTf32BK * 4 + 256 + kTf32PairSlack;
-}
-static_assert(tf32_pair_smem_bytes() <= 227 * 1024, "shared memory per CTA");
 
 }  // namespace sgemm_cfg
