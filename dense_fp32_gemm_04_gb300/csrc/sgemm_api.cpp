@@ -39,14 +39,17 @@ struct sgemm_handle_s {
     EncodeTiledFn encode = nullptr;
     // sgemm_run_host pipeline: copy-in and copy-out streams and their events.
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_end = nullptr;
-    cudaEvent_t ev_in[8] = {}, ev_done[8] = {};
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+    cudaEvent_t ev_in[12] = {}, ev_done[12] = {};  // one pair per pipeline step
     void *min2_cand = nullptr;  // sgemm_run_min2 per-block candidates
 };
 
 namespace {
 
 constexpr int kMaxHostPanels = 8;
+constexpr int kMaxColBlocks = 4;
+constexpr int kMaxHostSteps = kMaxHostPanels - 1 + kMaxColBlocks;
+static_assert(kMaxHostSteps <= 12, "events per pipeline step");
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -219,9 +222,8 @@ int ensure_host_pipeline(sgemm_handle_t h)
     bool ok = cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&h->ev_b, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&h->ev_end, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < kMaxHostPanels; ++i)
+    for (int i = 0; ok && i < kMaxHostSteps; ++i)
         ok = cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
@@ -231,36 +233,59 @@ int ensure_host_pipeline(sgemm_handle_t h)
     return SGEMM_OK;
 }
 
-// Row panels for sgemm_run_host, as start rows (start[P] = M). The first and
-// last panels are about M / 8 rows so that the copy-in before the first GEMM
-// and the copy-out after the last one are short; the rows between them are
-// split evenly into panels of at least two rounds of 128 x 128 tiles (at most
-// 4), whose copies overlap the GEMMs of their neighbours. Problems with less
-// than two such rounds between the edges are one panel. The edge panels and
-// all middle panels but the last have a multiple of 128 rows.
-int host_panel_starts(sgemm_handle_t h, int M, int N, int K, int *start)
+// Pipeline schedule of sgemm_run_host: row panels of A and C (start rows,
+// start[panels] = M) and the column blocks of B (col[blocks] = N) in which B is
+// copied in and panel 0 is computed.
+//
+// Copy-in runs at ~200 GB/s on the host link; with B resident a row of C costs
+// about three times longer to compute (2NK / ~70 TFLOP/s) than its A and C rows
+// take to copy (4 (K + N) bytes at 200 GB/s, at 4096^3), so only the start of the
+// pipeline is copy-bound: nothing can be computed before B has arrived. So B is
+// copied in column blocks (up to 4, multiples of 128 columns), and panel 0 (about
+// M / 8 rows) is computed block by block as they arrive. Then panels grow, each
+// at most three times its predecessor, so its copy-in finishes while the previous
+// panel computes; the last panel is again about M / 8 rows, so the copy-out after
+// the last GEMM is short. Problems with less than two rounds of 128 x 128 tiles
+// outside the edge panels are one panel and one block. All panels but the last
+// have a multiple of 128 rows. (M = N = K = 4096: panels 512 (4 blocks of 1024
+// columns), 512, 1536, 1024, 512.)
+struct HostSchedule {
+    int panels = 1;
+    int start[kMaxHostPanels + 1] = {};
+    int blocks = 1;
+    int col[kMaxColBlocks + 1] = {};
+};
+
+HostSchedule host_schedule(const sgemm_handle_s *h, int M, int N, int K, bool split_b)
 {
-    start[0] = 0;
-    if (static_cast<double>(M) * N * K < 1.0e9 || M < 1024) {
-        start[1] = M;
-        return 1;
-    }
+    HostSchedule sc;
+    sc.start[1] = M;
+    sc.col[1] = N;
+    if (static_cast<double>(M) * N * K < 1.0e9 || M < 1024) return sc;
     const int edge = std::max(128, M / 8 / 128 * 128);
-    const int mid = M - 2 * edge;
-    const long long mid_tiles = static_cast<long long>((mid + 127) / 128) * ((N + 127) / 128);
-    if (mid_tiles < 2LL * h->num_sms) {  // too little work to hide the copies behind
-        start[1] = M;
-        return 1;
+    const long long mid_tiles = static_cast<long long>((M - 2 * edge + 127) / 128) * ((N + 127) / 128);
+    if (mid_tiles < 2LL * h->num_sms) return sc;
+    int P = 0, r = 0, size = edge;
+    for (int i = 0;; ++i) {
+        const int left = M - r;
+        int take = i < 2 ? edge : 3 * size;
+        take = std::min(take, left - edge) / 128 * 128;  // leave at least `edge` rows for the last panel
+        if (left <= edge || P == kMaxHostPanels - 1 || take <= 0) {
+            sc.start[++P] = M;
+            break;
+        }
+        r += take;
+        sc.start[++P] = r;
+        size = take;
     }
-    long long nmid = mid_tiles / (2LL * h->num_sms);
-    nmid = std::max(1LL, std::min({nmid, 4LL, static_cast<long long>(mid / 128)}));
-    const int mid_rows = ((mid + static_cast<int>(nmid) - 1) / static_cast<int>(nmid) + 127) / 128 * 128;
-    int P = 0;
-    start[++P] = edge;
-    for (int i = 0; i < nmid - 1 && start[P] + mid_rows < M - edge; ++i) start[P + 1] = start[P] + mid_rows, ++P;
-    start[++P] = M - edge;
-    start[++P] = M;
-    return P;
+    sc.panels = P;
+    if (split_b) {
+        const int nb = N >= 1024 ? kMaxColBlocks : (N >= 512 ? 2 : 1);
+        const int w = ((N + nb - 1) / nb + 127) / 128 * 128;
+        sc.blocks = (N + w - 1) / w;
+        for (int j = 0; j <= sc.blocks; ++j) sc.col[j] = std::min(N, j * w);
+    }
+    return sc;
 }
 
 int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
@@ -468,9 +493,9 @@ int sgemm_destroy(sgemm_handle_t h)
     if (h->min2_cand) cudaFree(h->min2_cand);
     if (h->h2d) cudaStreamDestroy(h->h2d);
     if (h->d2h) cudaStreamDestroy(h->d2h);
-    for (cudaEvent_t e : {h->ev_start, h->ev_b, h->ev_end})
+    for (cudaEvent_t e : {h->ev_start, h->ev_end})
         if (e) cudaEventDestroy(e);
-    for (int i = 0; i < kMaxHostPanels; ++i) {
+    for (int i = 0; i < kMaxHostSteps; ++i) {
         if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
         if (h->ev_done[i]) cudaEventDestroy(h->ev_done[i]);
     }
@@ -524,46 +549,53 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     int rc = ensure_host_pipeline(h);
     if (rc != SGEMM_OK) return rc;
 
-    // Pipeline over row panels of A and C: B and panel 0 go in first on the
-    // copy-in stream; panel p computes on `stream` once its rows are in, while
-    // panel p + 1 is copied in and panel p - 1 is copied out on the copy-out
-    // stream. Every panel is an ordinary device call on the staged copies.
+    // Pipeline (host_schedule): on the copy-in stream, B block by block with panel
+    // 0's A rows and its C block beside each, then each later panel's A and C rows;
+    // every GEMM runs on `stream` once its copies are in (events), and its C rows
+    // are copied back on the copy-out stream while later GEMMs compute. Every GEMM
+    // is an ordinary device call on the staged copies.
     cudaStream_t s = stream;
-    int start[kMaxHostPanels + 1];
-    const int P = host_panel_starts(h, M, N, K, start);
+    const HostSchedule sc = host_schedule(h, M, N, K, need_ab);
     const bool copy_c_in = beta != 0.0f;
     bool ok = cudaEventRecord(h->ev_start, s) == cudaSuccess && cudaStreamWaitEvent(h->h2d, h->ev_start, 0) == cudaSuccess &&
               cudaStreamWaitEvent(h->d2h, h->ev_start, 0) == cudaSuccess;
-    if (ok && need_ab)
-        ok = cudaMemcpy2DAsync(dB, dldb * 4, B, static_cast<size_t>(ldb) * 4, static_cast<size_t>(N) * 4, K,
-                               cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
-    ok = ok && cudaEventRecord(h->ev_b, h->h2d) == cudaSuccess && cudaStreamWaitEvent(s, h->ev_b, 0) == cudaSuccess;
-    int panels = 0;
-    bool c_changed = true;
-    for (int p = 0; ok && p < P; ++p) {
-        const int r0 = start[p];
-        const int mp = start[p + 1] - r0;
+    int step = 0;
+    for (int p = 0; ok && p < sc.panels; ++p) {
+        const int r0 = sc.start[p];
+        const int mp = sc.start[p + 1] - r0;
         const float *hA = A + static_cast<long long>(r0) * lda;
         float *hC = C + static_cast<long long>(r0) * ldc;
         float *pA = dA + static_cast<long long>(r0) * dlda;
         float *pC = dC + static_cast<long long>(r0) * dldc;
-        if (need_ab)
-            ok = cudaMemcpy2DAsync(pA, dlda * 4, hA, static_cast<size_t>(lda) * 4, static_cast<size_t>(K) * 4, mp,
-                                   cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
-        if (ok && copy_c_in)
-            ok = cudaMemcpy2DAsync(pC, dldc * 4, hC, static_cast<size_t>(ldc) * 4, static_cast<size_t>(N) * 4, mp,
-                                   cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
-        ok = ok && cudaEventRecord(h->ev_in[p], h->h2d) == cudaSuccess && cudaStreamWaitEvent(s, h->ev_in[p], 0) == cudaSuccess;
-        if (!ok) break;
-        rc = run_device(h, mp, N, K, alpha, need_ab ? pA : nullptr, static_cast<int>(dlda > 0 ? dlda : 1),
-                        need_ab ? dB : nullptr, static_cast<int>(dldb), beta, pC, static_cast<int>(dldc), s);
+        // panel 0 in B's column blocks; later panels whole (all of B is in by then)
+        const int nblk = p == 0 ? sc.blocks : 1;
+        for (int j = 0; ok && j < nblk; ++j) {
+            const int c0 = p == 0 ? sc.col[j] : 0;
+            const int nc = p == 0 ? sc.col[j + 1] - c0 : N;
+            if (p == 0 && need_ab)
+                ok = cudaMemcpy2DAsync(dB + c0, dldb * 4, B + c0, static_cast<size_t>(ldb) * 4,
+                                       static_cast<size_t>(nc) * 4, K, cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+            if (ok && j == 0 && need_ab)
+                ok = cudaMemcpy2DAsync(pA, dlda * 4, hA, static_cast<size_t>(lda) * 4, static_cast<size_t>(K) * 4, mp,
+                                       cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+            if (ok && copy_c_in)
+                ok = cudaMemcpy2DAsync(pC + c0, dldc * 4, hC + c0, static_cast<size_t>(ldc) * 4,
+                                       static_cast<size_t>(nc) * 4, mp, cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+            ok = ok && cudaEventRecord(h->ev_in[step], h->h2d) == cudaSuccess &&
+                 cudaStreamWaitEvent(s, h->ev_in[step], 0) == cudaSuccess;
+            if (!ok) break;
+            rc = run_device(h, mp, nc, K, alpha, need_ab ? pA : nullptr, static_cast<int>(dlda > 0 ? dlda : 1),
+                            need_ab ? dB + c0 : nullptr, static_cast<int>(dldb), beta, pC + c0, static_cast<int>(dldc), s);
+            if (rc != SGEMM_OK) break;
+            const bool c_changed = h->last.kernel != SGEMM_KERNEL_NONE;  // alpha == 0 / K == 0 with beta == 1
+            ok = cudaEventRecord(h->ev_done[step], s) == cudaSuccess &&
+                 cudaStreamWaitEvent(h->d2h, h->ev_done[step], 0) == cudaSuccess;
+            if (ok && c_changed)
+                ok = cudaMemcpy2DAsync(hC + c0, static_cast<size_t>(ldc) * 4, pC + c0, dldc * 4,
+                                       static_cast<size_t>(nc) * 4, mp, cudaMemcpyDeviceToHost, h->d2h) == cudaSuccess;
+            ++step;
+        }
         if (rc != SGEMM_OK) break;
-        c_changed = h->last.kernel != SGEMM_KERNEL_NONE;  // alpha == 0 / K == 0 with beta == 1: C unchanged
-        ok = cudaEventRecord(h->ev_done[p], s) == cudaSuccess && cudaStreamWaitEvent(h->d2h, h->ev_done[p], 0) == cudaSuccess;
-        if (ok && c_changed)
-            ok = cudaMemcpy2DAsync(hC, static_cast<size_t>(ldc) * 4, pC, dldc * 4, static_cast<size_t>(N) * 4, mp,
-                                   cudaMemcpyDeviceToHost, h->d2h) == cudaSuccess;
-        ++panels;
     }
     // Join the copy streams back into `stream` and wait: on success and on
     // failure alike no copy into the caller's host buffers is left in flight.
@@ -577,7 +609,6 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
         cudaGetLastError();
         return SGEMM_ERR_CUDA;
     }
-    (void)panels;
     return SGEMM_OK;
 }
 
