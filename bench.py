@@ -387,7 +387,7 @@ def measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, device, st
             "launches_per_call": plan.launches, "kernel": kernel,
             "plan": {k: plan.as_dict()[k] for k in ("config", "bm", "bn", "stages", "grid", "units", "sk_tiles",
                                                     "sk_grid")},
-            "note": "flagged SGEMM_MATH_TF32 (TF32 inputs, FP32 accumulate); per-call time includes the B transpose",
+            "note": "flagged SGEMM_MATH_TF32 (TF32 inputs, FP32 accumulate); per-call time includes the stream-K reduction",
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak,
                          "peak_basis": f"{basis} bf16 {bf16} TFLOP/s x 1.1/2.25 (nominal tf32:bf16 dense ratio)"}}

@@ -165,10 +165,16 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K,
 
 /*
  * Same operation with HOST operands: copies A, B (and C when beta != 0) to
- * handle-owned device buffers on `stream`, runs sgemm_run, copies C back and
- * synchronizes `stream` before returning. Pinned (page-locked) host memory
- * gives asynchronous, full-bandwidth copies; pageable memory also works.
- * Same argument rules as sgemm_run (pointers are host pointers).
+ * handle-owned device buffers, computes C there and copies it back, then
+ * synchronizes `stream` before returning. Large problems are pipelined over
+ * row panels of A and C (the first panel also over column blocks of B, in
+ * which B is copied in), each panel or block one device GEMM on `stream`
+ * while the next one's copy-in and the previous one's copy-out run on the
+ * handle's own copy streams; the panels depend only on M, N, K and the SM
+ * count, so results are reproducible and satisfy the sgemm_run bound. Pinned
+ * (page-locked) host memory gives asynchronous, full-bandwidth copies;
+ * pageable memory also works. Same argument rules as sgemm_run (pointers are
+ * host pointers).
  */
 int sgemm_run_host(sgemm_handle_t h, int M, int N, int K,
                    float alpha, const float *A, int lda,
