@@ -381,8 +381,8 @@ def measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, device, st
     achieved = gemm_flops(M, N, K) / (ms * 1e-3) / 1e12
     bf16, basis = measured_bf16_peak()
     peak = bf16 * (1.1 / 2.25)  # nominal dense tf32 : bf16 ratio
-    kernel = ("tf32_pair_kernel (CTA pairs, tcgen05 .cta_group::2, 256 x 256 tiles)" if plan.config == 1
-              else "tf32_sgemm_kernel (one CTA per 128 x 256 tile)")
+    kernel = ("tf32_kernel<true> (CTA pairs, tcgen05 .cta_group::2, 256 x 256 tiles)" if plan.config == 1
+              else "tf32_kernel<false> (one CTA per 128 x 256 tile)")
     return {"value": achieved, "unit": "TFLOP/s", "ms_per_call": ms, "steps": steps, "status": st,
             "launches_per_call": plan.launches, "kernel": kernel,
             "plan": {k: plan.as_dict()[k] for k in ("config", "bm", "bn", "stages", "grid", "units", "sk_tiles",

@@ -139,6 +139,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
+// CTAs in this CTA's cluster (1 when the kernel was not launched with clusters).
+__device__ __forceinline__ uint32_t cluster_size()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_id_x()
 {
     uint32_t r;

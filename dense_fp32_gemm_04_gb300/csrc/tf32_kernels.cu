@@ -3,34 +3,57 @@
 // bits), products are accumulated in FP32 in tensor memory (TMEM). It is never
 // used unless the caller selects it, and is held to its own, looser bound.
 //
-// Structure (one CTA per SM, persistent over 128 x 256 output tiles, walking
-// the work sequence of schedule.cuh: whole tiles, then the CTA's K slice of
-// a stream-K span whose partial tiles sk_reduce_kernel adds in k order):
-//   warp 0      TMA producer: A box (32 k x 128 rows, K-major, 128-byte
-//               swizzle) and eight B boxes (32 n x 32 k each, MN-major: B as
-//               stored, 128-byte swizzle of 32-byte chunks) into a 4-stage ring.
-//   warp 1      MMA issuer: one thread issues 4 tcgen05.mma (K = 8 each) per
-//               stage into one of two TMEM accumulators (128 lanes x 256
-//               columns each), commits the stage back to the producer, and
-//               commits a finished accumulator to the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter of the
-//               accumulator, alpha/beta, stores to C; then hand the
-//               accumulator back so the next tile's MMAs overlap this one's
-//               stores.
+// One kernel, two forms (the PAIR template flag), both persistent with one CTA
+// per SM, walking the work sequence of schedule.cuh (whole tiles, then the
+// worker's K slice of a stream-K span whose partial tiles sk_reduce_kernel adds
+// in k order):
+//   one CTA     a worker is a CTA computing 128 x 256 tiles with
+//               tcgen05.mma.cta_group::1 (M = 128, N = 256, K = 8).
+//   CTA pair    a worker is a cluster of two CTAs on two SMs computing 256 x 256
+//               tiles with tcgen05.mma.cta_group::2 (M = 256, N = 256): rank r
+//               stages rows [128 r, 128 r + 128) of the A slab and columns
+//               [128 r, 128 r + 128) of the B slab at the same shared-memory
+//               offsets in both CTAs and holds rows [128 r, 128 r + 128) of the
+//               accumulator in its own TMEM; rank 0's MMAs read both CTAs'
+//               stages and write both TMEMs. Per FMA each SM's shared memory
+//               then carries a third less traffic than with one CTA per tile.
+// Warps of every CTA:
+//   warp 0      TMA producer: the CTA's A box (32 k x 128 rows, K-major,
+//               128-byte swizzle) and B boxes (32 n x 32 k each, MN-major: B as
+//               stored, 128-byte swizzle of 32-byte chunks) into the stage ring.
+//   warp 1      MMA issuer (rank 0 only): one thread issues 4 tcgen05.mma
+//               (K = 8 each) per stage into one of two TMEM accumulators (128
+//               lanes x 256 columns each), commits the stage back to the
+//               producers, and commits a finished accumulator to the epilogues.
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter of the CTA's
+//               accumulator, alpha/beta, stores to C; then hand the accumulator
+//               back so the next tile's MMAs overlap this one's stores.
+// Barriers (in each CTA; for the pair, the MMA issuer's are rank 0's):
+//   full[s]      both CTAs' copies of stage s complete_tx on rank 0's (rank 0
+//                expects the bytes of both).
+//   empty[s]     every CTA: the MMAs that read stage s committed (multicast to
+//                both CTAs of a pair).
+//   acc_full[b]  every CTA: accumulator b holds a finished tile (multicast).
+//   acc_empty[b] rank 0: the epilogue warps of every CTA of the worker have read
+//                accumulator b (4 or 8 arrivals, a peer's through its cluster
+//                address).
 // A (row-major M x K) is read K-major, B (row-major K x N) MN-major, both as the
 // caller stores them (an operand whose base or row stride is not 16-byte
 // aligned is first repacked into the handle's workspace).
 //
-// All waits are bounded; on expiry the CTA records SGEMM_ERR_TIMEOUT, lets its
-// copies and MMAs in flight finish (bounded), frees its TMEM and returns.
+// All waits are bounded; on expiry the CTA records SGEMM_ERR_TIMEOUT and stops.
+// A CTA leaves only after its copies have landed and the MMAs reading its
+// stages have committed (bounded waits), and the two CTAs of a pair only
+// through one final cluster barrier, after rank 0 saw its MMAs finish, so no
+// CTA exits while the other may still touch its shared memory or TMEM.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "device_ptx.cuh"
-#include "tcgen05_ptx.cuh"
 #include "schedule.cuh"
 #include "sgemm_internal.h"
+#include "tcgen05_ptx.cuh"
 
 namespace sgemm_impl {
 namespace {
@@ -38,40 +61,58 @@ namespace {
 using namespace sgemm_dev;
 
 constexpr int kTimeoutCode = 5 << 16;  // SGEMM_ERR_TIMEOUT << 16
-constexpr int BM = sgemm_cfg::kTf32BM, BN = sgemm_cfg::kTf32BN, BK = sgemm_cfg::kTf32BK;
-constexpr int STAGES = sgemm_cfg::kTf32Stages;
-constexpr int A_BYTES = BM * BK * 4;
-constexpr int B_BYTES = BN * BK * 4;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kLayoutCode = 7 << 16;   // SGEMM_ERR_NOT_SUPPORTED << 16
+constexpr int BK = sgemm_cfg::kTf32BK;
+constexpr int BN = sgemm_cfg::kTf32BN;    // columns of a tile and of a CTA's accumulator (both forms)
 constexpr int THREADS = sgemm_cfg::kTf32Threads;
 constexpr int MMA_K = 8;                  // K of one tcgen05.mma .kind::tf32
 constexpr uint32_t TMEM_COLS = 2 * BN;    // two accumulators
-constexpr uint32_t IDESC = idesc_tf32(BM, BN, true);
 // B is staged MN-major in boxes of 32 n x 32 k (4 KiB, 128-byte swizzle of 32-byte
 // chunks), boxes along n 4 KiB apart.
 constexpr int kBoxN = 32;
 constexpr int B_BOX_BYTES = kBoxN * BK * 4;
-static_assert(sgemm_cfg::tf32_smem_bytes() == 1024 + STAGES * STAGE_BYTES + 256, "smem layout");
 static_assert(TMEM_COLS == 512, "two 128 x 256 FP32 accumulators fill TMEM");
+static_assert(sgemm_cfg::kTf32PairBN == BN, "both forms keep 256 accumulator columns per CTA");
 
-struct Bars {
+template <bool PAIR>
+struct Tf32Shape {
+    static constexpr int CTAS = PAIR ? 2 : 1;  // CTAs per worker
+    static constexpr int BM = PAIR ? sgemm_cfg::kTf32PairBM : sgemm_cfg::kTf32BM;  // tile rows
+    static constexpr int CTA_M = BM / CTAS;    // rows of A and of the accumulator per CTA
+    static constexpr int CTA_N = BN / CTAS;    // columns of B staged per CTA
+    static constexpr int STAGES = PAIR ? sgemm_cfg::kTf32PairStages : sgemm_cfg::kTf32Stages;
+    static constexpr int A_BYTES = CTA_M * BK * 4;
+    static constexpr int B_BYTES = CTA_N * BK * 4;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t IDESC = idesc_tf32(BM, BN, true);
+    static constexpr int SMEM = PAIR ? sgemm_cfg::tf32_pair_smem_bytes() : sgemm_cfg::tf32_smem_bytes();
+    static_assert(CTA_M == 128, "an accumulator holds 128 TMEM lanes");
+    static_assert(CTA_N % kBoxN == 0, "whole B boxes");
+    static_assert(SMEM == 1024 + STAGES * STAGE_BYTES + 256, "smem layout");
+};
+
+template <int STAGES>
+struct Tf32Bars {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
+    uint32_t ring_offset;  // this CTA's stage-ring address, compared with the peer's
     int abort_flag;
     int issued[STAGES];
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Tf32Bars<sgemm_cfg::kTf32PairStages>) <= 256, "barrier block");
+static_assert(sizeof(Tf32Bars<sgemm_cfg::kTf32Stages>) <= 256, "barrier block");
 
-__device__ __forceinline__ void raise_abort(Bars *b, const Tf32Params &p, int where)
+template <int STAGES>
+__device__ __forceinline__ void raise_abort(Tf32Bars<STAGES> *b, const Tf32Params &p, int code)
 {
     volatile int *f = &b->abort_flag;
     if (!*f) {
         *f = 1;
-        report_status(p.status, kTimeoutCode | where);
+        report_status(p.status, code);
     }
 }
 
@@ -162,19 +203,29 @@ __device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row,
     }
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
-tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const Tf32Params p)
+tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Tf32Params p)
 {
+    using S = Tf32Shape<PAIR>;
+    constexpr int STAGES = S::STAGES;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t a_base = smem_addr(smem);
-    const uint32_t b_base = a_base + STAGES * A_BYTES;
-    Bars *bars = reinterpret_cast<Bars *>(smem + STAGES * STAGE_BYTES);
+    const uint32_t b_base = a_base + STAGES * S::A_BYTES;
+    Tf32Bars<STAGES> *bars = reinterpret_cast<Tf32Bars<STAGES> *>(smem + STAGES * S::STAGE_BYTES);
     volatile int *abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (PAIR && cluster_size() != 2) {
+        // not launched as clusters of two: no barrier, copy or tensor-core operation is issued
+        if (threadIdx.x == 0) report_status(p.status, kLayoutCode | kWherePairLayout);
+        return;
+    }
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int worker = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int workers = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -184,234 +235,7 @@ tf32_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_addr(&bars->acc_full[b]), 1);
-            mbar_init(smem_addr(&bars->acc_empty[b]), 4);
-        }
-        mbar_init(smem_addr(&bars->mma_done), 1);
-        bars->abort_flag = 0;
-        fence_barrier_init();
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
-    }
-    if (warp == 0) {
-        tmem_alloc(smem_addr(&bars->tmem_base), TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = bars->tmem_base;
-
-    if (warp == 0 && lane == 0) {
-        // ---- TMA producer ----
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        pdl_wait();  // operands repacked by this call's previous kernel are complete
-        Work w;
-        for (int item = 0; ok && work_at(p, item, w); ++item) {
-            const int tm = w.tm, tn = w.tn;
-            for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                const uint32_t full = smem_addr(&bars->full[stage]);
-                if (!mbar_wait_bounded(smem_addr(&bars->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
-                    raise_abort(bars, p, kWhereProducerEmpty);
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(full, STAGE_BYTES);
-                tma_load_2d(a_base + stage * A_BYTES, &tmA, full, kb * BK, tm * BM);
-#pragma unroll
-                for (int j = 0; j < BN / kBoxN; ++j)
-                    tma_load_2d(b_base + stage * B_BYTES + j * B_BOX_BYTES, &tmB, full, tn * BN + j * kBoxN, kb * BK);
-                bars->issued[stage] = 2 | static_cast<int>(phase);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        pdl_trigger();  // every copy is issued: the call's reduction may become resident
-        for (int s = 0; s < STAGES; ++s) {
-            const int rec = bars->issued[s];
-            if ((rec & 2) && !mbar_wait_bounded(smem_addr(&bars->full[s]), static_cast<uint32_t>(rec & 1), nullptr,
-                                                p.timeout_ns))
-                report_status(p.status, kTimeoutCode | kWhereDrain);
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----
-        int stage = 0;
-        uint32_t phase = 0;
-        int it = 0;
-        bool ok = true;
-        Work w;
-        for (int item = 0; ok && work_at(p, item, w); ++item, ++it) {
-            const int buf = it & 1;
-            const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
-            if (!mbar_wait_bounded(smem_addr(&bars->acc_empty[buf]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
-                raise_abort(bars, p, kWhereAccum);
-                break;
-            }
-            tc_fence_after_sync();
-            const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
-            const int kb0 = w.kb0, kb1 = w.kb1;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(smem_addr(&bars->full[stage]), phase, abort_flag, p.timeout_ns)) {
-                    raise_abort(bars, p, kWhereMmaEmpty);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t a_s = a_base + stage * A_BYTES;
-                const uint32_t b_s = b_base + stage * B_BYTES;
-#pragma unroll
-                for (int k = 0; k < BK / MMA_K; ++k) {
-                    // A: K advances 8 TF32 = 32 bytes inside the 128-byte swizzle atom;
-                    // B: one 8-row (8 k) group = 1024 bytes.
-                    mma_tf32(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4),
-                             smem_desc_mn_sw128_32b(b_s + k * 1024, B_BOX_BYTES), IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
-                }
-                mma_commit(smem_addr(&bars->empty[stage]));  // stage free once these MMAs are done
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!ok) break;
-            mma_commit(smem_addr(&bars->acc_full[buf]));
-        }
-        // Every MMA of ours must be finished before TMEM is released.
-        mma_commit(smem_addr(&bars->mma_done));
-        if (!mbar_wait_bounded(smem_addr(&bars->mma_done), 0u, nullptr, p.timeout_ns))
-            report_status(p.status, kTimeoutCode | kWhereDrain);
-    } else if (warp >= 2) {
-        // ---- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 ----
-        const int quarter = warp & 3;
-        int it = 0;
-        Work w;
-        for (int item = 0; work_at(p, item, w); ++item, ++it) {
-            const int buf = it & 1;
-            const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
-            bool ok = mbar_wait_bounded(smem_addr(&bars->acc_full[buf]), acc_phase, abort_flag, p.timeout_ns);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) raise_abort(bars, p, kWhereAccum);
-                break;
-            }
-            tc_fence_after_sync();
-            const int row = w.tm * BM + quarter * 32 + lane;
-            const int tn = w.tn;
-            const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-            if (w.dest == kToPartial) {
-                // Stream-K piece: the raw partial tile, tile-packed (rows and columns
-                // past M and N hold sums of the copy engine's zero fill); the
-                // stream-K reduction adds the pieces in k order and applies alpha / beta.
-                float *wrow = p.W + static_cast<long long>(w.idx) * (BM * BN) + (quarter * 32 + lane) * BN;
-                if (p.kblocks <= kShortK)
-                    store_partial_row<4>(t_row, wrow);
-                else
-                    store_partial_row<1>(t_row, wrow);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&bars->acc_empty[buf]));
-                continue;
-            }
-            if (p.kblocks <= kShortK)
-                store_c_row<4>(p, t_row, row, tn);
-            else
-                store_c_row<1>(p, t_row, row, tn);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars->acc_empty[buf]));
-        }
-    }
-
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    if (warp == 0) {
-        __syncwarp();
-        tmem_dealloc(tmem, TMEM_COLS);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// CTA-pair kernel (tcgen05 .cta_group::2). A cluster of two CTAs on two SMs
-// computes 256 x 256 tiles: rank r stages rows [128 r, 128 r + 128) of the A
-// slab (K-major) and columns [128 r, 128 r + 128) of the B slab (MN-major, four
-// 32 n x 32 k boxes), both at the same shared-memory offsets in the two CTAs,
-// and holds rows
-// [128 r, 128 r + 128) of the accumulator in its own TMEM. One thread of rank 0
-// issues M = 256, N = 256 MMAs that read both CTAs' stages and write both
-// TMEMs. Barriers:
-//   full[s]      rank 0 only: both CTAs' copies of stage s complete_tx on it
-//                (rank 0 expects the bytes of both).
-//   empty[s]     both CTAs: the MMAs that read stage s committed to both.
-//   acc_full[b]  both CTAs: accumulator b holds a finished tile.
-//   acc_empty[b] rank 0 only: the 4 epilogue warps of each CTA have read
-//                accumulator b (8 arrivals, the peer's from the other SM).
-// Every wait is bounded; a CTA whose wait runs out records SGEMM_ERR_TIMEOUT
-// and stops; the two CTAs leave only through one final cluster barrier, after
-// rank 0 saw its MMAs and both CTAs' copies finish (bounded), so no CTA exits
-// while the other may still touch its shared memory or TMEM.
-constexpr int PBM = sgemm_cfg::kTf32PairBM;
-constexpr int PBN = sgemm_cfg::kTf32PairBN;
-constexpr int PHALF_M = PBM / 2, PHALF_N = PBN / 2;
-constexpr int PSTAGES = sgemm_cfg::kTf32PairStages;
-constexpr int PA_BYTES = PHALF_M * BK * 4;
-constexpr int PB_BYTES = PHALF_N * BK * 4;
-constexpr int PSTAGE_BYTES = PA_BYTES + PB_BYTES;
-constexpr uint32_t PIDESC = idesc_tf32(PBM, PBN, true);
-constexpr int kLayoutCode = 7 << 16;  // SGEMM_ERR_NOT_SUPPORTED << 16
-static_assert(PBN == BN, "the pair kernel's accumulator rows share the one-CTA epilogue (BN columns)");
-static_assert(sgemm_cfg::tf32_pair_smem_bytes() == 1024 + PSTAGES * PSTAGE_BYTES + 256, "smem layout");
-
-struct PairBars {
-    uint64_t full[PSTAGES];
-    uint64_t empty[PSTAGES];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
-    uint64_t mma_done;
-    uint32_t tmem_base;
-    uint32_t ring_offset;  // this CTA's stage-ring address, compared with the peer's
-    int abort_flag;
-    int issued[PSTAGES];
-};
-static_assert(sizeof(PairBars) <= 256, "barrier block");
-
-__device__ __forceinline__ void raise_abort_pair(PairBars *b, const Tf32Params &p, int code)
-{
-    volatile int *f = &b->abort_flag;
-    if (!*f) {
-        *f = 1;
-        report_status(p.status, code);
-    }
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const Tf32Params p)
-{
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const uint32_t raw = smem_addr(smem_raw);
-    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    const uint32_t a_base = smem_addr(smem);
-    const uint32_t b_base = a_base + PSTAGES * PA_BYTES;
-    PairBars *bars = reinterpret_cast<PairBars *>(smem + PSTAGES * PSTAGE_BYTES);
-    volatile int *abort_flag = &bars->abort_flag;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const int pair = static_cast<int>(cluster_id_x());
-    const int pairs = static_cast<int>(cluster_count_x());
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < PSTAGES; ++s) {
-            mbar_init(smem_addr(&bars->full[s]), 1);
-            mbar_init(smem_addr(&bars->empty[s]), 1);
-            bars->issued[s] = 0;
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_addr(&bars->acc_full[b]), 1);
-            mbar_init(smem_addr(&bars->acc_empty[b]), 8);
+            mbar_init(smem_addr(&bars->acc_empty[b]), 4 * S::CTAS);
         }
         mbar_init(smem_addr(&bars->mma_done), 1);
         bars->abort_flag = 0;
@@ -421,60 +245,77 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         prefetch_tensormap(&tmB);
     }
     if (warp == 0) {
-        tmem_alloc_pair(smem_addr(&bars->tmem_base), TMEM_COLS);
-        tmem_relinquish_pair();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_addr(&bars->tmem_base), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_addr(&bars->tmem_base), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // both CTAs' barriers are initialised before any copy or arrive targets them
+    if constexpr (PAIR) cluster_sync();  // both CTAs' barriers are initialised before any copy or arrive targets them
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
-    // The MMAs address both CTAs' stages by rank 0's offsets, which must therefore
-    // agree. Compared on the address bits a shared-memory descriptor holds (the
-    // offset inside the CTA's shared memory; higher bits of a shared::cta address
-    // can differ between the CTAs of a cluster).
-    constexpr uint32_t kDescAddrMask = 0x3FFFFu;
-    const uint32_t peer_ring = ld_shared_cluster_u32(mapa_shared(smem_addr(&bars->ring_offset), rank ^ 1u));
-    const bool same_layout = ((peer_ring ^ a_base) & kDescAddrMask) == 0;
-    if (!same_layout && threadIdx.x == 0) raise_abort_pair(bars, p, kLayoutCode | kWherePairLayout);
+    bool same_layout = true;
+    if constexpr (PAIR) {
+        // Rank 0's MMAs address both CTAs' stages by its own offsets, which must
+        // therefore agree; compared on the address bits a shared-memory descriptor
+        // holds (the offset inside the CTA; higher bits of a shared::cta address
+        // differ between the CTAs of a cluster).
+        constexpr uint32_t kDescAddrMask = 0x3FFFFu;
+        const uint32_t peer_ring = ld_shared_cluster_u32(mapa_shared(smem_addr(&bars->ring_offset), rank ^ 1u));
+        same_layout = ((peer_ring ^ a_base) & kDescAddrMask) == 0;
+        if (!same_layout && threadIdx.x == 0) raise_abort(bars, p, kLayoutCode | kWherePairLayout);
+    }
 
     if (!same_layout) {
-        // both CTAs see the mismatch: no copies, no MMAs
+        // both CTAs of the pair see the mismatch: no copies, no MMAs
     } else if (warp == 0 && lane == 0) {
-        // ---- TMA producer (both CTAs): this CTA's halves of each stage ----
+        // ---- TMA producer: this CTA's part of each stage ----
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         pdl_wait();  // operands repacked by this call's previous kernel are complete
         Work w;
-        for (int item = 0; ok && work_at_g(p, item, w, pair, pairs); ++item) {
-            const int row_a = w.tm * PBM + static_cast<int>(rank) * PHALF_M;
-            const int col_b = w.tn * PBN + static_cast<int>(rank) * PHALF_N;
+        for (int item = 0; ok && work_at_g(p, item, w, worker, workers); ++item) {
+            const int row_a = w.tm * S::BM + static_cast<int>(rank) * S::CTA_M;
+            const int col_b = w.tn * BN + static_cast<int>(rank) * S::CTA_N;
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!mbar_wait_bounded(smem_addr(&bars->empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
-                    raise_abort_pair(bars, p, kTimeoutCode | kWhereProducerEmpty);
+                    raise_abort(bars, p, kTimeoutCode | kWhereProducerEmpty);
                     ok = false;
                     break;
                 }
-                const uint32_t full = mapa_shared(smem_addr(&bars->full[stage]), 0);  // rank 0's barrier
-                if (rank == 0) mbar_arrive_expect_tx(smem_addr(&bars->full[stage]), 2 * PSTAGE_BYTES);
-                tma_load_2d_pair(a_base + stage * PA_BYTES, &tmA, full, kb * BK, row_a);
+                const uint32_t a_dst = a_base + stage * S::A_BYTES;
+                const uint32_t b_dst = b_base + stage * S::B_BYTES;
+                if (rank == 0) mbar_arrive_expect_tx(smem_addr(&bars->full[stage]), S::CTAS * S::STAGE_BYTES);
+                if constexpr (PAIR) {
+                    const uint32_t full = mapa_shared(smem_addr(&bars->full[stage]), 0);  // rank 0's barrier
+                    tma_load_2d_pair(a_dst, &tmA, full, kb * BK, row_a);
 #pragma unroll
-                for (int j = 0; j < PHALF_N / kBoxN; ++j)
-                    tma_load_2d_pair(b_base + stage * PB_BYTES + j * B_BOX_BYTES, &tmB, full, col_b + j * kBoxN,
-                                     kb * BK);
+                    for (int j = 0; j < S::CTA_N / kBoxN; ++j)
+                        tma_load_2d_pair(b_dst + j * B_BOX_BYTES, &tmB, full, col_b + j * kBoxN, kb * BK);
+                } else {
+                    const uint32_t full = smem_addr(&bars->full[stage]);
+                    tma_load_2d(a_dst, &tmA, full, kb * BK, row_a);
+#pragma unroll
+                    for (int j = 0; j < S::CTA_N / kBoxN; ++j)
+                        tma_load_2d(b_dst + j * B_BOX_BYTES, &tmB, full, col_b + j * kBoxN, kb * BK);
+                }
                 bars->issued[stage] = 2 | static_cast<int>(phase);
-                if (++stage == PSTAGES) {
+                if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
         }
         pdl_trigger();  // every copy is issued: the call's reduction may become resident
-        // Drain. Rank 0: both CTAs' copies of every issued stage have landed (they
-        // complete on its full barriers). Both: unless aborted, the MMAs that read
-        // them have committed to this CTA's empty barriers.
-        for (int s = 0; s < PSTAGES; ++s) {
+        // Drain. Rank 0: every issued stage's copies (of both CTAs of a pair) have
+        // landed, as they complete on its full barriers. Every CTA: unless aborted,
+        // the MMAs that read them have committed to this CTA's empty barriers.
+        for (int s = 0; s < STAGES; ++s) {
             const int rec = bars->issued[s];
             if (!(rec & 2)) continue;
             const uint32_t par = static_cast<uint32_t>(rec & 1);
@@ -488,76 +329,96 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
         }
     } else if (warp == 1 && lane == 0 && rank == 0) {
-        // ---- MMA issuer (rank 0 only) ----
+        // ---- MMA issuer (rank 0) ----
         int stage = 0;
         uint32_t phase = 0;
         int it = 0;
         bool ok = true;
         Work w;
-        for (int item = 0; ok && work_at_g(p, item, w, pair, pairs); ++item, ++it) {
+        for (int item = 0; ok && work_at_g(p, item, w, worker, workers); ++item, ++it) {
             const int buf = it & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
             if (!mbar_wait_cluster_bounded(smem_addr(&bars->acc_empty[buf]), acc_phase ^ 1u, abort_flag,
                                            p.timeout_ns)) {
-                raise_abort_pair(bars, p, kTimeoutCode | kWhereAccum);
+                raise_abort(bars, p, kTimeoutCode | kWhereAccum);
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * PBN);
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
             const int kb0 = w.kb0, kb1 = w.kb1;
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait_cluster_bounded(smem_addr(&bars->full[stage]), phase, abort_flag, p.timeout_ns)) {
-                    raise_abort_pair(bars, p, kTimeoutCode | kWhereMmaEmpty);
+                    raise_abort(bars, p, kTimeoutCode | kWhereMmaEmpty);
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t a_s = a_base + stage * PA_BYTES;
-                const uint32_t b_s = b_base + stage * PB_BYTES;
+                const uint32_t a_s = a_base + stage * S::A_BYTES;
+                const uint32_t b_s = b_base + stage * S::B_BYTES;
 #pragma unroll
-                for (int k = 0; k < BK / MMA_K; ++k)
-                    mma_tf32_pair(d_tmem, smem_desc_k_sw128(a_s + k * MMA_K * 4),
-                                  smem_desc_mn_sw128_32b(b_s + k * 1024, B_BOX_BYTES), PIDESC,
-                                  (kb != kb0 || k != 0) ? 1u : 0u);
-                mma_commit_pair_both(smem_addr(&bars->empty[stage]));  // stage free in both CTAs
-                if (++stage == PSTAGES) {
+                for (int k = 0; k < BK / MMA_K; ++k) {
+                    // A: K advances 8 TF32 = 32 bytes inside the 128-byte swizzle atom;
+                    // B: one 8-row (8 k) group = 1024 bytes.
+                    const uint64_t a_desc = smem_desc_k_sw128(a_s + k * MMA_K * 4);
+                    const uint64_t b_desc = smem_desc_mn_sw128_32b(b_s + k * 1024, B_BOX_BYTES);
+                    const uint32_t acc = (kb != kb0 || k != 0) ? 1u : 0u;
+                    if constexpr (PAIR)
+                        mma_tf32_pair(d_tmem, a_desc, b_desc, S::IDESC, acc);
+                    else
+                        mma_tf32(d_tmem, a_desc, b_desc, S::IDESC, acc);
+                }
+                // the stage is free (in both CTAs of a pair) once these MMAs are done
+                if constexpr (PAIR)
+                    mma_commit_pair_both(smem_addr(&bars->empty[stage]));
+                else
+                    mma_commit(smem_addr(&bars->empty[stage]));
+                if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            mma_commit_pair_both(smem_addr(&bars->acc_full[buf]));
+            if constexpr (PAIR)
+                mma_commit_pair_both(smem_addr(&bars->acc_full[buf]));
+            else
+                mma_commit(smem_addr(&bars->acc_full[buf]));
         }
-        // Every MMA (they write both CTAs' TMEM) is finished before either CTA frees it.
-        mma_commit_pair_local(smem_addr(&bars->mma_done));
+        // Every MMA (for a pair they write both CTAs' TMEM) is finished before TMEM is freed.
+        if constexpr (PAIR)
+            mma_commit_pair_local(smem_addr(&bars->mma_done));
+        else
+            mma_commit(smem_addr(&bars->mma_done));
         if (!mbar_wait_bounded(smem_addr(&bars->mma_done), 0u, nullptr, p.timeout_ns))
             report_status(p.status, kTimeoutCode | kWhereDrain);
     } else if (warp >= 2) {
-        // ---- epilogue (both CTAs): warp w reads TMEM lanes 32 * (w % 4) .. + 31 ----
+        // ---- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 of this CTA ----
         const int quarter = warp & 3;
-        const int half_row = static_cast<int>(rank) * PHALF_M + quarter * 32 + lane;
+        const int cta_row = static_cast<int>(rank) * S::CTA_M + quarter * 32 + lane;  // row within the tile
         int it = 0;
         Work w;
-        for (int item = 0; work_at_g(p, item, w, pair, pairs); ++item, ++it) {
+        for (int item = 0; work_at_g(p, item, w, worker, workers); ++item, ++it) {
             const int buf = it & 1;
             const uint32_t acc_phase = static_cast<uint32_t>(it >> 1) & 1u;
             bool ok = mbar_wait_cluster_bounded(smem_addr(&bars->acc_full[buf]), acc_phase, abort_flag, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
-                if (lane == 0) raise_abort_pair(bars, p, kTimeoutCode | kWhereAccum);
+                if (lane == 0) raise_abort(bars, p, kTimeoutCode | kWhereAccum);
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * PBN);
+            const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
             if (w.dest == kToPartial) {
-                // this CTA's rows of the pair's tile-packed 256 x 256 partial
-                float *wrow = p.W + static_cast<long long>(w.idx) * (PBM * PBN) + static_cast<long long>(half_row) * PBN;
+                // Stream-K piece: this CTA's rows of the raw, tile-packed partial tile
+                // (rows and columns past M and N hold sums of the copy engine's zero
+                // fill); the stream-K reduction adds the pieces in k order and
+                // applies alpha / beta.
+                float *wrow = p.W + static_cast<long long>(w.idx) * (S::BM * BN) + static_cast<long long>(cta_row) * BN;
                 if (p.kblocks <= kShortK)
                     store_partial_row<4>(t_row, wrow);
                 else
                     store_partial_row<1>(t_row, wrow);
             } else {
-                const int row = w.tm * PBM + half_row;
+                const int row = w.tm * S::BM + cta_row;
                 if (p.kblocks <= kShortK)
                     store_c_row<4>(p, t_row, row, w.tn);
                 else
@@ -565,17 +426,25 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&bars->acc_empty[buf]), 0));  // rank 0's
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&bars->acc_empty[buf]), 0));  // rank 0's
+                else
+                    mbar_arrive(smem_addr(&bars->acc_empty[buf]));
+            }
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();  // neither CTA leaves while the other may still use its barriers, stages or TMEM
+    if constexpr (PAIR) cluster_sync();  // neither CTA leaves while the other may still use its barriers, stages or TMEM
     tc_fence_after_sync();
     if (warp == 0) {
         __syncwarp();
-        tmem_dealloc_pair(tmem, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem, TMEM_COLS);
+        else
+            tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -583,11 +452,11 @@ tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
 cudaError_t tf32_set_attributes()
 {
-    cudaError_t e = cudaFuncSetAttribute(tf32_sgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         sgemm_cfg::tf32_smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(tf32_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tf32Shape<false>::SMEM);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(tf32_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                sgemm_cfg::tf32_pair_smem_bytes());
+    return cudaFuncSetAttribute(tf32_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Tf32Shape<true>::SMEM);
 }
 
 int tf32_pair_max_pairs()
@@ -595,28 +464,35 @@ int tf32_pair_max_pairs()
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = sgemm_cfg::tf32_pair_smem_bytes();
+    cfg.dynamicSmemBytes = Tf32Shape<true>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, tf32_pair_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, tf32_kernel<true>, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
     return clusters;
 }
 
-cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
-                             cudaStream_t stream, bool dependent)
-{
-    // grid = 2 x pairs; clusters of two come from the kernel's __cluster_dims__
-    return launch_kernel(dependent, tf32_pair_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_pair_smem_bytes(),
-                         stream, tmA, tmB, p);
-}
-
 cudaError_t launch_tf32(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
                         cudaStream_t stream, bool dependent)
 {
-    return launch_kernel(dependent, tf32_sgemm_kernel, dim3(grid), dim3(THREADS), sgemm_cfg::tf32_smem_bytes(),
-                         stream, tmA, tmB, p);
+    return launch_kernel(dependent, tf32_kernel<false>, dim3(grid), dim3(THREADS), Tf32Shape<false>::SMEM, stream,
+                         tmA, tmB, p);
+}
+
+cudaError_t launch_tf32_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const Tf32Params &p, int grid,
+                             cudaStream_t stream, bool dependent)
+{
+    // grid = 2 x pairs, launched as clusters of two
+    return launch_kernel_cluster(dependent, 2, tf32_kernel<true>, dim3(grid), dim3(THREADS), Tf32Shape<true>::SMEM,
+                                 stream, tmA, tmB, p);
 }
 
 }  // namespace sgemm_impl
