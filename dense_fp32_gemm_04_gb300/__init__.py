@@ -79,6 +79,7 @@ _SIGNATURES = {
     "sgemm_check_device_status": ([_P, _P, ctypes.POINTER(_I)], _I),
     "sgemm_plan": ([_I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(Plan)], _I),
     "sgemm_last_plan": ([_P, ctypes.POINTER(Plan)], _I),
+    "sgemm_reserve": ([_P, _LL], _I),
     "sgemm_config_count": ([], _I),
     "sgemm_config_info": ([_I, ctypes.POINTER(Plan)], _I),
     "sgemm_status_string": ([_I], ctypes.c_char_p),
@@ -300,6 +301,10 @@ class Sgemm:
         code = ctypes.c_int()
         st = library().sgemm_check_device_status(self._h, self._stream(stream), ctypes.byref(code))
         return st, code.value
+
+    def reserve(self, workspace_bytes: int):
+        """Grow the device workspace now (so that later calls can be captured into a CUDA graph)."""
+        _check(library().sgemm_reserve(self._h, int(workspace_bytes)), "sgemm_reserve")
 
     def last_plan(self) -> Plan:
         p = Plan()

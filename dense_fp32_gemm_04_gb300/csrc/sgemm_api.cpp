@@ -74,9 +74,19 @@ struct DeviceGuard {
     }
 };
 
-int ensure_workspace(sgemm_handle_t h, size_t bytes)
+// Grow the handle's workspace to at least `bytes`. Growing synchronizes the
+// device and reallocates, which a stream capture forbids: while `stream` is being
+// captured, a workspace that is too small is SGEMM_ERR_NOT_SUPPORTED and nothing
+// is called (size it first, with sgemm_reserve or an uncaptured call).
+int ensure_workspace(sgemm_handle_t h, size_t bytes, cudaStream_t stream)
 {
     if (bytes <= h->ws_bytes) return SGEMM_OK;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return SGEMM_ERR_NOT_SUPPORTED;
     if (h->workspace) {
         // Earlier launches on any stream may still read the old buffer.
         if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
@@ -305,14 +315,14 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     }
 
     Workspace w = workspace_layout(q, plan);
-    rc = ensure_workspace(h, static_cast<size_t>(w.total));
+    rc = ensure_workspace(h, static_cast<size_t>(w.total), stream);
     if (rc == SGEMM_ERR_ALLOC && plan.transpose_a && h->ov.force_transpose_a < 0) {
         // No room for A^T (a very large A): read A as given instead, same results.
         Overrides ov = h->ov;
         ov.force_transpose_a = 0;
         if ((rc = make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
         w = workspace_layout(q, plan);
-        rc = ensure_workspace(h, static_cast<size_t>(w.total));
+        rc = ensure_workspace(h, static_cast<size_t>(w.total), stream);
     }
     if (h->log) log_plan(plan, M, N, K);
     h->last = plan;
@@ -450,9 +460,11 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
         const int pairs = tf32_pair_max_pairs();
         h->tf32_pairs = pairs > 0 ? std::min(pairs, sms / 2) : -1;
     }
-    if (cudaMalloc(&h->d_status, 256) != cudaSuccess || cudaMemset(h->d_status, 0, 256) != cudaSuccess) {
+    if (cudaMalloc(&h->d_status, 256) != cudaSuccess || cudaMemset(h->d_status, 0, 256) != cudaSuccess ||
+        cudaMalloc(&h->min2_cand, min2_candidate_bytes(8 * sms)) != cudaSuccess) {
         cudaGetLastError();
         if (h->d_status) cudaFree(h->d_status);
+        if (h->min2_cand) cudaFree(h->min2_cand);
         delete h;
         return SGEMM_ERR_ALLOC;
     }
@@ -622,12 +634,7 @@ int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     if (!g.ok) return SGEMM_ERR_CUDA;
     int rc = run_device(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
     if (rc != SGEMM_OK) return rc;
-    const int blocks = 8 * h->num_sms;
-    if (h->min2_cand == nullptr && cudaMalloc(&h->min2_cand, min2_candidate_bytes(blocks)) != cudaSuccess) {
-        cudaGetLastError();
-        h->min2_cand = nullptr;
-        return SGEMM_ERR_ALLOC;
-    }
+    const int blocks = 8 * h->num_sms;  // the candidate buffer is sized for this at handle creation
     return launch_min2(C, ldc, M, N, h->min2_cand, blocks, min_vals, min_ij, stream) == cudaSuccess
                ? SGEMM_OK
                : SGEMM_ERR_LAUNCH;
@@ -726,6 +733,14 @@ int sgemm_plan(int M, int N, int K, int lda, int ldb, int ldc, int align_flags, 
     if (out == nullptr) return SGEMM_ERR_INVALID_VALUE;
     Problem q{M, N, K, lda, ldb, ldc, align_flags, num_sms, math_mode, 1.0f, 1.0f};
     return make_plan(q, Overrides{}, out);
+}
+
+int sgemm_reserve(sgemm_handle_t h, long long workspace_bytes)
+{
+    if (h == nullptr || workspace_bytes < 0) return SGEMM_ERR_INVALID_VALUE;
+    DeviceGuard g(h->device);
+    if (!g.ok) return SGEMM_ERR_CUDA;
+    return ensure_workspace(h, static_cast<size_t>(workspace_bytes), nullptr);
 }
 
 int sgemm_last_plan(sgemm_handle_t h, sgemm_plan_t *out)

@@ -268,6 +268,22 @@ int sgemm_plan(int M, int N, int K, int lda, int ldb, int ldc, int align_flags,
 /* The plan used by the handle's most recent sgemm_run / sgemm_run_host. */
 int sgemm_last_plan(sgemm_handle_t h, sgemm_plan_t *out);
 
+/*
+ * Grow the handle's device workspace to at least workspace_bytes now (e.g. the
+ * workspace_bytes of sgemm_plan for the problems to come). Growing synchronizes
+ * the device. SGEMM_ERR_ALLOC if the memory cannot be had.
+ *
+ * CUDA graphs: sgemm_run and sgemm_run_min2 may be captured into a CUDA graph
+ * (stream capture) once the workspace holds their plan's workspace_bytes (this
+ * call, or an earlier uncaptured run of a problem at least as large): they then
+ * only launch kernels and encode tensor maps on the host. A captured call whose
+ * workspace would have to grow returns SGEMM_ERR_NOT_SUPPORTED and calls
+ * nothing on the stream. sgemm_run_host synchronizes and cannot be captured.
+ * Graph replays reuse the workspace: replays of graphs holding calls of one
+ * handle must not overlap.
+ */
+int sgemm_reserve(sgemm_handle_t h, long long workspace_bytes);
+
 /* Number of rows in the tile-config table, and row `index` (as a plan whose
  * problem-dependent fields are zero). Needs no GPU. */
 int sgemm_config_count(void);
