@@ -21,6 +21,7 @@ import statistics
 import subprocess
 import sys
 import threading
+import traceback
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -502,6 +503,17 @@ def measured_hbm_gbs():
 
 
 # ---------------------------------------------------------------- our arm
+def optional(name, fn, *a, **kw):
+    """Run an optional section of the line (min2, configs, context, TF32, CPU baseline):
+    a failure there becomes {"error": ...} in its key (traceback on stderr) instead of
+    costing the headline measurement."""
+    try:
+        return fn(*a, **kw)
+    except Exception as e:  # noqa: BLE001 - reported in the JSON line and on stderr
+        traceback.print_exc(file=sys.stderr)
+        return {"error": f"{name}: {type(e).__name__}: {e}"}
+
+
 def run_ours(args, world):
     import numpy as np
     import torch
@@ -577,12 +589,14 @@ def run_ours(args, world):
     e2e_t = world.max(time.perf_counter() - t0)
     e2e_value = flops * e2e_steps * world.size / e2e_t / 1e12
 
-    min2 = measure_min2(torch, sg, h, dA, dB, dC, M, N, K, alpha, beta, stream, ms_per_call=elapsed / args.steps * 1e3)
-    configs = (measure_configs(torch, sg, h, dev, stream, measured_hbm_gbs())
+    min2 = optional("min2", measure_min2, torch, sg, h, dA, dB, dC, M, N, K, alpha, beta, stream,
+                    ms_per_call=elapsed / args.steps * 1e3)
+    configs = (optional("configs", measure_configs, torch, sg, h, dev, stream, measured_hbm_gbs())
                if world.size == 1 and not args.no_configs else None)
-    library = (measure_library_context(torch, dA, dB, dC, alpha, beta, flops)
+    library = (optional("library_context", measure_library_context, torch, dA, dB, dC, alpha, beta, flops)
                if world.size == 1 and not args.no_context else None)
-    tf32 = (measure_tf32(torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream, world.local_rank, args.tf32_steps)
+    tf32 = (optional("tf32_mode", measure_tf32, torch, sg, dA, dB, dC, M, N, K, alpha, beta, stream,
+                     world.local_rank, args.tf32_steps)
             if args.tf32_steps > 0 else None)
 
     clocks = sampler.summary(t_wall0, t_wall1)
@@ -624,10 +638,11 @@ def run_ours(args, world):
         "library_context": library,
     }
     if world.rank == 0 and world.size == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(args.workload, args.cpu_seconds, A, B, C)
-        if not args.no_configs:
-            line["cpu_baseline"]["configs"] = cpu_oracle_configs(min(2.0, args.cpu_seconds / 4),
-                                                                 (A, B, C) if args.workload == "square4096" else None)
+        line["cpu_baseline"] = optional("cpu_baseline", cpu_oracle_sample, args.workload, args.cpu_seconds, A, B, C)
+        if not args.no_configs and "error" not in line["cpu_baseline"]:
+            line["cpu_baseline"]["configs"] = optional(
+                "cpu_baseline.configs", cpu_oracle_configs, min(2.0, args.cpu_seconds / 4),
+                (A, B, C) if args.workload == "square4096" else None)
     if world.rank == 0:
         print(json.dumps(line), flush=True)
     h.close()

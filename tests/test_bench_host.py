@@ -110,3 +110,12 @@ def test_kernel_hash_ignores_comments():
     assert bench.strip_comments("a  =\n b;") == bench.strip_comments("a = b;".replace(" b", "\n  b"))
     assert bench.strip_comments("x = 1; // a") == bench.strip_comments("x = 1; // b")
     assert bench.strip_comments("x = 1;") != bench.strip_comments("x = 2;")
+
+
+def test_optional_sections_report_failures_instead_of_raising(capsys):
+    def boom():
+        raise ValueError("no TF32 today")
+
+    assert bench.optional("tf32_mode", boom) == {"error": "tf32_mode: ValueError: no TF32 today"}
+    assert "ValueError" in capsys.readouterr().err
+    assert bench.optional("min2", lambda a, b=0: a + b, 2, b=3) == 5
