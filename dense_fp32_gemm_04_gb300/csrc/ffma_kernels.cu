@@ -62,17 +62,21 @@ using sgemm_cfg::kFfmaBK;
 
 constexpr int kTimeoutCode = 5 << 16;  // SGEMM_ERR_TIMEOUT << 16
 
-template <int BM_, int BN_, int STAGES_, int MINB_>
+template <int BM_, int BN_, int STAGES_, int MINB_, int EPI_ = 0>
 struct Tile {
     static constexpr int BM = BM_, BN = BN_, STAGES = STAGES_, MINB = MINB_, BK = kFfmaBK;
+    static constexpr int EPI = EPI_;  // > 0: a staging tile and EPI epilogue warps
     static constexpr int WM = 32, WN = 64;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMERS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMERS + 1) * 32;
+    static constexpr int THREADS = (CONSUMERS + 1 + EPI) * 32;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BK * BN * 4;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int SMEM_BYTES = sgemm_cfg::ffma_smem_bytes(BM, BN, STAGES);
+    static constexpr int STAGING_BYTES = (EPI > 0 ? 1 : 0) * BM * BN * 4;
+    static constexpr int SMEM_BYTES = sgemm_cfg::ffma_smem_bytes(BM, BN, STAGES, EPI);
+    static_assert(EPI == 0 || (BN == 128 && BM % EPI == 0),
+                  "an epilogue warp moves one 16-byte word of a staged row per lane, whole rows per warp");
     static_assert(BM % WM == 0 && BN % WN == 0, "CTA tile must be a multiple of the warp tile");
     static_assert(BM <= 256 && BN <= 256, "a TMA box side is at most 256 elements");
     static_assert(A_BYTES % 1024 == 0, "A stages must keep the 1024-byte swizzle alignment");
@@ -381,6 +385,104 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc
     }
 }
 
+// Staged epilogue (tiles with an epilogue warp). A consumer warp writes its
+// 32 x 64 part of the finished accumulator tile into the BM x BN staging tile
+// (the layout of a tile-packed partial; each quarter-warp stores 128 contiguous
+// bytes, so the 128-bit stores are conflict-free) and goes on with its next
+// tile; the epilogue warp moves the staging tile to its destination meanwhile.
+template <class T, bool AT>
+__device__ __forceinline__ void stage_tile(float *stg, const Acc<AT> &acc, int wm, int wn, int r, int c)
+{
+    const int lr0 = wm * T::WM;
+    const int lc0 = wn * T::WN + c * 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<float4 *>(stg + (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h) = out4(acc, i, h);
+    }
+}
+
+// 16 bytes of the staging tile (shared-memory address): an explicit shared-space
+// load, which the compiler knows cannot alias the global stores around it.
+__device__ __forceinline__ float4 lds128(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// The epilogue warps: for every work item of the CTA, warp e writes rows
+// [e BM / EPI, (e + 1) BM / EPI) of the staged tile (lane l: columns 4l..4l+3)
+// to its destination: C with alpha / beta (the C loads of 8 rows issued before
+// their stores), or raw to a split-K slice or a stream-K partial tile; then hands
+// the staging tile back (one arrival per epilogue warp). (Prefetching the tile's
+// C rows into L2 during its mainloop, and bulk asynchronous copies out of the
+// staging tile, were measured and gained nothing.)
+template <class T>
+__device__ __forceinline__ void epilogue_warp_loop(const FfmaParams &p, uint32_t stg, uint32_t staged, uint32_t freed,
+                                                   volatile int *abort_flag, int e, int lane)
+{
+    constexpr int ROWS = T::BM / T::EPI;
+    const int lc = 4 * lane;
+    const int lr_begin = e * ROWS;
+    const uint32_t src0 = stg + static_cast<uint32_t>((lr_begin * T::BN + lc) * 4);
+    Work w;
+    for (int item = 0; work_at(p, item, w); ++item) {
+        bool ok = mbar_wait_bounded(staged, static_cast<uint32_t>(item & 1), abort_flag, p.timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0 && !*abort_flag) {
+                *abort_flag = 1;
+                report_status(p.status, kTimeoutCode | kWhereStaging);
+            }
+            return;
+        }
+        if (w.dest == kToPartial) {
+            float *W = p.W + static_cast<long long>(w.idx) * (T::BM * T::BN) + lr_begin * T::BN + lc;
+#pragma unroll 8
+            for (int lr = 0; lr < ROWS; ++lr)
+                *reinterpret_cast<float4 *>(W + lr * T::BN) = lds128(src0 + lr * T::BN * 4);
+        } else if (w.dest == kToSplit) {
+            float *W = p.W + static_cast<long long>(w.idx) * p.wstride;
+            const int col = w.tn * T::BN + lc;
+            if (col < p.N) {
+#pragma unroll 8
+                for (int lr = 0; lr < ROWS; ++lr) {
+                    const int row = w.tm * T::BM + lr_begin + lr;
+                    if (row >= p.M) break;
+                    *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) =
+                        lds128(src0 + lr * T::BN * 4);
+                }
+            }
+        } else {
+            const int col = w.tn * T::BN + lc;
+            if (col < p.N) {
+                for (int lr0 = 0; lr0 < ROWS; lr0 += 8) {
+                    float4 cin[8];
+                    if (p.beta != 0.0f) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int row = w.tm * T::BM + lr_begin + lr0 + j;
+                            cin[j] = row < p.M ? load_c4(p, row, col) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int row = w.tm * T::BM + lr_begin + lr0 + j;
+                        if (row < p.M) store_c4_loaded(p, row, col, lds128(src0 + (lr0 + j) * T::BN * 4), cin[j]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(freed);  // this warp's rows of the staging tile have been read
+    }
+}
+
 template <class T, bool AT>
 __global__ void __launch_bounds__(T::THREADS, T::MINB)
 ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -391,9 +493,12 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const float *sA = reinterpret_cast<const float *>(smem);
     const float *sB = reinterpret_cast<const float *>(smem + T::STAGES * T::A_BYTES);
-    unsigned char *bar_ptr = smem + T::STAGES * T::STAGE_BYTES;
+    float *stg = reinterpret_cast<float *>(smem + T::STAGES * T::STAGE_BYTES);  // staging tile (EPI)
+    unsigned char *bar_ptr = smem + T::STAGES * T::STAGE_BYTES + T::STAGING_BYTES;
     const uint32_t bar_base = smem_addr(bar_ptr);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_ptr + 2 * T::STAGES * 8);
+    const uint32_t staged_bar = bar_base + 8 * (2 * T::STAGES);     // EPI: the consumers' arrivals
+    const uint32_t freed_bar = bar_base + 8 * (2 * T::STAGES + 1);  // EPI: the epilogue warps' arrivals
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_ptr + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0)) * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -402,6 +507,10 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(bar_base + 8 * s, 1);                          // full: producer's arrive + bytes
             mbar_init(bar_base + 8 * (T::STAGES + s), T::CONSUMERS); // empty: one arrive per consumer warp
+        }
+        if (T::EPI) {
+            mbar_init(staged_bar, T::CONSUMERS);
+            mbar_init(freed_bar, T::EPI);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -416,6 +525,12 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (lane == 0)
             producer_loop<T, AT>(&tmA, &tmB, p, smem_addr(sA), smem_addr(sB), bar_base, abort_flag);
         return;
+    }
+    if constexpr (T::EPI > 0) {
+        if (warp > T::CONSUMERS) {
+            epilogue_warp_loop<T>(p, smem_addr(stg), staged_bar, freed_bar, abort_flag, warp - T::CONSUMERS - 1, lane);
+            return;
+        }
     }
 
     const int wm = warp % T::WARPS_M;
@@ -466,13 +581,29 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 phase ^= 1u;
             }
         }
-        Work w;  // recomputed here so that only `item` stays live across the mainloop
-        work_at(p, item, w);
-        epilogue<T, AT>(p, acc, w, wm, wn, r, c);
+        if constexpr (T::EPI != 0) {
+            // wait until the epilogue warp has read the previous tile out of the staging tile
+            bool ok = mbar_wait_bounded(freed_bar, static_cast<uint32_t>(item & 1) ^ 1u, abort_flag, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) {
+                    *abort_flag = 1;
+                    report_status(p.status, kTimeoutCode | kWhereStaging);
+                }
+                return;
+            }
+            stage_tile<T, AT>(stg, acc, wm, wn, r, c);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(staged_bar);
+        } else {
+            Work w;  // recomputed here so that only `item` stays live across the mainloop
+            work_at(p, item, w);
+            epilogue<T, AT>(p, acc, w, wm, wn, r, c);
+        }
     }
 }
 
-using Cfg0 = Tile<128, 128, 5, 1>;
+using Cfg0 = Tile<128, 128, 5, 1, 2>;
 using Cfg1 = Tile<128, 64, 4, 2>;
 using Cfg2 = Tile<64, 128, 4, 2>;
 using Cfg3 = Tile<64, 64, 4, 3>;

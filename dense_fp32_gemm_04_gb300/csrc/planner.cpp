@@ -14,6 +14,24 @@ namespace {
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+// One work unit of kb_unit k-blocks on a CTA: the k-blocks plus the pipeline
+// fill and the epilogue, ~1.5 k-blocks. With epilogue warps the write-out of a
+// tile overlaps the next unit (~0.5 k-blocks left), but a unit then takes at
+// least as long as the epilogue warps need to write a tile out (measured at
+// 4096^2 x 32: the fitted 4 us raw or with beta = 0, 8 us reading C, pick
+// the faster row at 256^3 .. 1024^3 and the ragged shapes), and the kernel
+// ends with one such write-out (epilogue_tail).
+double epilogue_drain(const sgemm_cfg::TileConfig &c, bool reads_c)
+{
+    return c.epilogue_warps > 0 ? (reads_c ? 8.0e-6 : 4.0e-6) : 0.0;
+}
+
+double unit_time(const sgemm_cfg::TileConfig &c, double kb_unit, double t_kb, bool reads_c)
+{
+    if (c.epilogue_warps == 0) return (kb_unit + 1.5) * t_kb;
+    return std::max((kb_unit + 0.5) * t_kb, epilogue_drain(c, reads_c));
+}
+
 // Modelled time (seconds) of one FFMA configuration with S splits. Per CTA a
 // 32-deep k-block of a BM x BN tile costs BM*BN*32 FMAs at the SM's FP32 rate
 // shared by the CTAs resident on it; a persistent CTA runs ceil(units/slots)
@@ -29,7 +47,9 @@ double model_time(const sgemm_cfg::TileConfig &c, int M, int N, int K, int S, in
     const long long per_cta = ceil_div(units, slots);
     const double kb_per_unit = static_cast<double>(ceil_div(kb, S));
     const double t_kb = static_cast<double>(c.bm) * c.bn * sgemm_cfg::kFfmaBK * c.ctas_per_sm / fma_per_sm * c.rel_cost;
-    double t = static_cast<double>(per_cta) * (kb_per_unit + 1.5) * t_kb + 2.0e-6;
+    const bool reads_c = beta_read && S == 1;  // split slices are written raw
+    double t = static_cast<double>(per_cta) * unit_time(c, kb_per_unit, t_kb, reads_c) +
+               epilogue_drain(c, reads_c) + 2.0e-6;
     if (S > 1) {
         const double bytes = (2.0 * S + (beta_read ? 2.0 : 1.0)) * 4.0 * M * static_cast<double>(N);
         t += bytes / hbm + 2.5e-6;
@@ -55,8 +75,11 @@ double model_time_sk(const sgemm_cfg::TileConfig &c, int M, int N, int K, int nu
     const long long span = rem * kb;
     const long long G = std::min(slots, span);
     const double t_kb = static_cast<double>(c.bm) * c.bn * sgemm_cfg::kFfmaBK * c.ctas_per_sm / fma_per_sm * c.rel_cost;
-    double t = static_cast<double>(rounds - 1) * (static_cast<double>(kb) + 1.5) * t_kb +
-               (static_cast<double>(ceil_div(span, G)) + 3.0) * t_kb + 2.0e-6;
+    // whole tiles, then the span pieces (up to two partial tiles, written raw)
+    double t = static_cast<double>(rounds - 1) * unit_time(c, static_cast<double>(kb), t_kb, beta_read) +
+               std::max((static_cast<double>(ceil_div(span, G)) + (c.epilogue_warps > 0 ? 2.0 : 3.0)) * t_kb,
+                        2.0 * epilogue_drain(c, false)) +
+               epilogue_drain(c, false) + 2.0e-6;
     // Partial tiles (written, then read by the reduction) mostly stay in L2: counted
     // at twice the HBM rate; C at the HBM rate.
     const double tile_bytes = 4.0 * c.bm * c.bn;

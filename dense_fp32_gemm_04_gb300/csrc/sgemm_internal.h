@@ -19,7 +19,8 @@ enum : int {
     kWhereMmaEmpty = 4,      // TF32: the MMA issuer's wait for a filled stage ran out
     kWhereAccum = 5,         // TF32: the epilogue's wait for the accumulator ran out
     kWhereTmemAlloc = 6,     // TF32: TMEM allocation failed
-    kWherePairLayout = 7     // TF32 pair: the two CTAs' shared-memory layouts differ (no work done)
+    kWherePairLayout = 7,    // TF32 pair: the two CTAs' shared-memory layouts differ (no work done)
+    kWhereStaging = 8        // FFMA: a wait on the epilogue's staging tile ran out
 };
 
 // Everything the FFMA mainloop needs besides the two tensor maps.
