@@ -42,6 +42,12 @@
 //    of IEEE FP32 FMAs in ascending k, so both layouts give identical bits.
 //  * Persistent grid: CTAs loop over (tile, split) work units in a grouped
 //    order; the producer keeps prefetching across unit boundaries.
+//  * Epilogue: the pages write C from the compute threads once their K loop
+//    ends. On the 128 x 128 row the compute warps instead store the finished
+//    tile into a shared-memory staging tile and go on with the next one, and
+//    two epilogue warps write the staged tile out (alpha / beta into C, or raw
+//    split-K / stream-K partials) meanwhile; the other rows, whose 2-3 CTAs per
+//    SM leave no room for a staging tile, write from the compute warps.
 //  * Watchdog: every mbarrier wait is bounded; on expiry the CTA records
 //    SGEMM_ERR_TIMEOUT in the status word, waits (bounded) for its own copies
 //    in flight and returns — it never traps or spins forever.

@@ -8,7 +8,9 @@
 // Each consumer warp owns a 32 x 64 warp tile, each lane an 8 x 8 microtile
 // (the block / warp / thread tiling of "Optimizing Matrix Multiplication in
 // CUDA", warp tiling section; the 8 x 8 microtile of "Shared memory and
-// register blocking"). One extra warp issues the TMA copies.
+// register blocking"). One extra warp issues the TMA copies; on a row with
+// epilogue warps, those write each finished tile out of a shared-memory
+// staging tile while the compute warps go on.
 #pragma once
 
 namespace sgemm_cfg {
