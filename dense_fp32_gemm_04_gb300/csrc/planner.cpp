@@ -90,12 +90,14 @@ double model_time_sk(const sgemm_cfg::TileConfig &c, int M, int N, int K, int nu
 
 // Transposing A first pays when its copy (read + write of A, one more launch)
 // costs less than the ~10 % the A^T mainloop saves (measured 9-10 % at
-// 2048^3 .. 8192^3; kAtGain keeps a margin).
+// 2048^3 .. 8192^3; kAtGain keeps a margin). The launch costs ~1.5 us: the
+// mainloop is a programmatic dependent of the transposition, so its own launch
+// overlaps it (1024^3: A^T 45.2 against 47.1 us as given).
 bool transpose_pays(const Problem &q, double t_main)
 {
     constexpr double kAtGain = 0.07;
     const double hbm = 5.5e12;
-    const double t_copy = 8.0 * static_cast<double>(q.M) * q.K / hbm + 2.5e-6;
+    const double t_copy = 8.0 * static_cast<double>(q.M) * q.K / hbm + 1.5e-6;
     return t_copy < kAtGain * t_main;
 }
 

@@ -5,7 +5,9 @@ both TF32 kernel forms, every result checked against the FP64 oracle.
 The fixed cases of the other GPU tests sit on chosen edges (tile multiples +-1,
 the benchmark problems); this sweep draws the combinations in between, where a
 scheduling or indexing mistake (a stream-K range boundary, a split slice, a
-partial pair tile, a repacked operand with an offset) would show up. Integer
+partial pair tile, a repacked operand with an offset, a ragged row or column of
+the staged 128 x 128 epilogue) would show up. The FP32 cases also force a random
+tile-config row. Integer
 operands must be bit-exact; real ones must lie inside the mode's bound (for
 TF32 also the tight bound of test_gpu_tf32). Every case also checks the canary
 guards around C and the device status word.
@@ -47,6 +49,7 @@ def _draw_case(rng):
     beta = float(rng.choice(BETAS))
     dist = ("int", "int", "int") if rng.random() < 0.5 else ("normal", "uniform", "uniform")
     opts = {
+        "config": int(rng.choice([-1, -1, 0, 0, 1, 2, 3])),
         "streamk": int(rng.choice([-1, -1, 0, 1])),
         "splits": int(rng.choice([0, 0, 0, 2, 3, 5, 8])),
         "transpose_a": int(rng.choice([-1, -1, 0, 1])),
@@ -79,6 +82,7 @@ def test_random_problems(lib_built, mode):
             M, N, K, pads, offsets, alpha, beta, dist, opts = _draw_case(rng)
             h.set_option(sg.OPT_FORCE_STREAMK, opts["streamk"])
             if mode == "fp32":
+                h.set_option(sg.OPT_FORCE_CONFIG, opts["config"])
                 h.set_option(sg.OPT_FORCE_SPLITS, opts["splits"])
                 h.set_option(sg.OPT_FORCE_TRANSPOSE_A, opts["transpose_a"])
             A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=1000 + case, dist=dist)
