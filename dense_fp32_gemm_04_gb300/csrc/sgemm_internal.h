@@ -18,7 +18,7 @@ enum : int {
     kWhereDrain = 3,         // waiting for this CTA's own copies in flight ran out
     kWhereMmaEmpty = 4,      // TF32: the MMA issuer's wait for a filled stage ran out
     kWhereAccum = 5,         // TF32: the epilogue's wait for the accumulator ran out
-    kWhereTmemAlloc = 6,     // TF32: TMEM allocation failed
+    // 6: not used (TMEM allocation blocks until it succeeds; it reports nothing)
     kWherePairLayout = 7,    // TF32 pair: the two CTAs' shared-memory layouts differ (no work done)
     kWhereStaging = 8        // FFMA: a wait on the epilogue's staging tile ran out
 };

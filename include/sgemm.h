@@ -250,9 +250,15 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value);
 /*
  * Synchronize `stream`, then read and clear the handle's device status word.
  * device_status (may be NULL) receives 0 when no kernel reported a problem,
- * else a code whose upper 16 bits are an sgemm_status value (SGEMM_ERR_TIMEOUT)
- * and lower bits say which wait ran out. Returns that sgemm_status value, or
- * SGEMM_ERR_CUDA if synchronizing failed (e.g. a sticky device error).
+ * else a code whose upper 16 bits are an sgemm_status value (SGEMM_ERR_TIMEOUT,
+ * or SGEMM_ERR_NOT_SUPPORTED for a TF32 CTA pair whose shared-memory layouts
+ * disagree) and whose lower bits say where: 1 a compute warp's wait for a filled
+ * stage, 2 the copy warp's wait for a free stage, 3 the wait for a CTA's own
+ * copies and MMAs in flight at its end, 4 the TF32 MMA issuer's wait for a
+ * filled stage, 5 a wait on a TF32 accumulator, 7 the TF32 pair layout check,
+ * 8 a wait on the FP32 epilogue's staging tile (6 is not used). Returns that
+ * sgemm_status value, or SGEMM_ERR_CUDA if synchronizing failed (e.g. a sticky
+ * device error).
  */
 int sgemm_check_device_status(sgemm_handle_t h, struct CUstream_st *stream, int *device_status);
 
