@@ -275,8 +275,11 @@ __device__ __forceinline__ void store_c4(const FfmaParams &p, int row, int col, 
     }
 }
 
-// The batched form of store_c4 for the A-as-given kernel's epilogue: C read
-// first (load_c4), then written (store_c4_loaded).
+// The batched form of store_c4, C read first (load_c4) and written later
+// (store_c4_loaded): used by the epilogue warps and by the A-as-given compute
+// warps. The A^T compute warps keep store_c4 (load and store together): every
+// batched variant changed the register allocation of that whole kernel and
+// slowed its mainloop by more than it saved.
 __device__ __forceinline__ float4 load_c4(const FfmaParams &p, int row, int col)
 {
     const float *src = p.C + static_cast<long long>(row) * p.ldc + col;
