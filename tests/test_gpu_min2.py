@@ -147,3 +147,31 @@ def test_tf32_and_scale_only_plans(h):
     assert oracle.exact(got, ref)  # integer operands are exact in TF32
     rv, rr, rc = oracle.min2(ref)
     assert list(vals.astype(np.float64)) == rv and list(ij) == [rr[0], rc[0], rr[1], rc[1]]
+
+
+def _min2_reference(C):
+    """The definition on a given C: NaN ranks as +inf, equal values by row-major position."""
+    flat = np.where(np.isnan(C), np.inf, C).astype(np.float64).ravel()
+    order = np.lexsort((np.arange(flat.size), flat))[:2]
+    return flat[order], [(int(i) // C.shape[1], int(i) % C.shape[1]) for i in order]
+
+
+@pytest.mark.parametrize("N", [520, 517])  # 16-byte loads of C, and element loads
+def test_nan_ranks_as_infinity(h, N):
+    """NaN in C (through beta * C) ranks as +inf: it is never chosen while two other
+    values exist, and an all-NaN C gives +inf at the first two positions."""
+    M, K = 300, 40
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=N, dist=("int", "int", "int"))
+    rng = np.random.default_rng(N)
+    for kind in ("some", "all_but_one", "all"):
+        Cn = C.copy()
+        if kind == "some":
+            Cn[rng.random(Cn.shape) < 0.3] = np.nan
+        else:
+            Cn[:] = np.nan
+            if kind == "all_but_one":
+                Cn[M // 2, N // 3] = 0.0
+        got, vals, ij = _run(h, A, B, Cn, 1.0, 1.0)
+        want_vals, want_pos = _min2_reference(got)
+        assert [float(v) for v in vals] == [float(v) for v in want_vals], kind
+        assert [tuple(ij[:2]), tuple(ij[2:])] == want_pos, kind
