@@ -332,7 +332,7 @@ def run_reference(args, world):
 
 
 def measured_bf16_peak():
-    """Dense bf16 TFLOP/s measured on this machine (burst), or the stated fallback."""
+    """Dense bf16 TFLOP/s measured on this GPU model (burst), or the stated fallback."""
     try:
         d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
         return float(d["bf16_tflops"]), "measured"
