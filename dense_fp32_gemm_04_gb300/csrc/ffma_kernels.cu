@@ -394,11 +394,11 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc
     }
 }
 
-// Staged epilogue (tiles with an epilogue warp). A consumer warp writes its
-// 32 x 64 part of the finished accumulator tile into the BM x BN staging tile
-// (the layout of a tile-packed partial; each quarter-warp stores 128 contiguous
+// Staged epilogue (rows with epilogue warps). A consumer warp writes its 32 x 64
+// part of the finished accumulator tile into the BM x BN staging tile (the
+// layout of a tile-packed partial; each quarter-warp stores 128 contiguous
 // bytes, so the 128-bit stores are conflict-free) and goes on with its next
-// tile; the epilogue warp moves the staging tile to its destination meanwhile.
+// tile; the epilogue warps move the staging tile to its destination meanwhile.
 template <class T, bool AT>
 __device__ __forceinline__ void stage_tile(float *stg, const Acc<AT> &acc, int wm, int wn, int r, int c)
 {
@@ -412,8 +412,9 @@ __device__ __forceinline__ void stage_tile(float *stg, const Acc<AT> &acc, int w
     }
 }
 
-// 16 bytes of the staging tile (shared-memory address): an explicit shared-space
-// load, which the compiler knows cannot alias the global stores around it.
+// 16 bytes of the staging tile, by shared-memory address (an explicit
+// shared-space load rather than a generic one; ordered with the memory accesses
+// around it).
 __device__ __forceinline__ float4 lds128(uint32_t addr)
 {
     float4 v;
