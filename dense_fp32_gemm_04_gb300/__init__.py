@@ -51,7 +51,7 @@ class Plan(ctypes.Structure):
         "kernel", "config", "bm", "bn", "bk", "stages", "threads", "ctas_per_sm", "splits",
         "tiles_m", "tiles_n", "units", "grid", "repack_a", "repack_b", "vec_c", "math_mode",
         "launches")] + [("workspace_bytes", ctypes.c_longlong), ("transpose_a", ctypes.c_int),
-                        ("sk_tiles", ctypes.c_int), ("sk_grid", ctypes.c_int)]
+                        ("sk_tiles", ctypes.c_int), ("sk_grid", ctypes.c_int), ("repack_c", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -758,16 +758,35 @@ __global__ void scale_kernel(int M, int N, float beta, float *__restrict__ C, lo
 
 // dst (rows x cols, row stride ldd) = src (row stride lds): gives an operand a
 // 16-byte-aligned base and row stride so the TMA path can read it.
+constexpr int kRepackThreads = 256, kRepackPerThread = 8;
+constexpr int kRepackChunk = kRepackThreads * kRepackPerThread;  // columns per work item
 __global__ void repack_kernel(const float *__restrict__ src, long long lds, float *__restrict__ dst, long long ldd,
                               int rows, int cols)
 {
     pdl_trigger();  // the call's mainloop may become resident; it waits for this grid to finish
-    const long long total = static_cast<long long>(rows) * cols;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long row = idx / cols;
-        const long long col = idx - row * cols;
-        dst[row * ldd + col] = __ldg(src + row * lds + col);
+    // work items: (row, chunk of kRepackChunk columns); one division per item, the
+    // block's threads stride along the chunk (coalesced on both sides; launched with
+    // kRepackThreads threads)
+    const long long nchunks = (cols + kRepackChunk - 1) / kRepackChunk;
+    const long long items = static_cast<long long>(rows) * nchunks;
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const long long row = it / nchunks;
+        const int c0 = static_cast<int>(it - row * nchunks) * kRepackChunk;
+        const int c1 = min(cols, c0 + kRepackChunk);
+        const float *s = src + row * lds;
+        float *d = dst + row * ldd;
+        // kRepackPerThread loads in flight per thread before any store
+        float v[kRepackPerThread];
+#pragma unroll
+        for (int j = 0; j < kRepackPerThread; ++j) {
+            const int col = c0 + static_cast<int>(threadIdx.x) + j * kRepackThreads;
+            if (col < c1) v[j] = __ldg(s + col);
+        }
+#pragma unroll
+        for (int j = 0; j < kRepackPerThread; ++j) {
+            const int col = c0 + static_cast<int>(threadIdx.x) + j * kRepackThreads;
+            if (col < c1) d[col] = v[j];
+        }
     }
 }
 
@@ -877,8 +896,10 @@ cudaError_t launch_scale(int M, int N, float beta, float *C, long long ldc, int 
 cudaError_t launch_repack(const float *src, long long lds, float *dst, long long ldd, int rows, int cols,
                           int num_sms, cudaStream_t stream)
 {
-    repack_kernel<<<elementwise_grid(static_cast<long long>(rows) * cols, 256, num_sms), 256, 0, stream>>>(
-        src, lds, dst, ldd, rows, cols);
+    const long long items = static_cast<long long>(rows) * ((cols + kRepackChunk - 1) / kRepackChunk);
+    const long long cap = 8LL * num_sms;
+    const int grid = static_cast<int>(items < 1 ? 1 : (items < cap ? items : cap));
+    repack_kernel<<<grid, kRepackThreads, 0, stream>>>(src, lds, dst, ldd, rows, cols);
     return cudaGetLastError();
 }
 

@@ -280,8 +280,12 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
                 out->grid = static_cast<int>(cluster * (n_full > 0 ? slots : std::min(slots, rem * st)));
             }
         }
+        // C not 16-byte accessible: the epilogue would write it element by element, one
+        // row per thread (uncoalesced); for all but small C, compute into an aligned copy.
+        if (!out->vec_c && static_cast<long long>(q.M) * q.N >= (1LL << 18)) out->repack_c = 1;
         out->workspace_bytes = workspace_layout(q, *out).total;
-        out->launches = out->repack_a + out->repack_b + 1 + (out->sk_tiles > 0 ? 1 : 0);
+        out->launches = out->repack_a + out->repack_b + 1 + (out->sk_tiles > 0 ? 1 : 0) +
+                        (out->repack_c ? (q.beta != 0.0f ? 2 : 1) : 0);
         return SGEMM_OK;
     }
 
@@ -355,6 +359,11 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
         w.ldb = round_up(q.N, 4);
         w.b_off = off;
         off += round_up(static_cast<long long>(q.K) * w.ldb * 4, 256);
+    }
+    if (p.repack_c) {
+        w.ldc = round_up(q.N, 4);
+        w.c_off = off;
+        off += round_up(static_cast<long long>(q.M) * w.ldc * 4, 256);
     }
     if (p.sk_tiles > 0) {
         // two partial tiles per worker (CTA, or CTA pair) of the stream-K span

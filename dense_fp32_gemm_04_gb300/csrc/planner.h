@@ -33,6 +33,7 @@ struct Workspace {
     long long a_off = 0, lda = 0;       // repacked A (M x lda, plan.repack_a) or A^T (K x lda, plan.transpose_a)
     long long b_off = 0, ldb = 0;       // repacked B (K x ldb), when plan.repack_b
     long long w_off = 0, ldw = 0, wstride = 0;  // split-K or stream-K partials
+    long long c_off = 0, ldc = 0;       // aligned copy of C (M x ldc), when plan.repack_c
     long long total = 0;
 };
 

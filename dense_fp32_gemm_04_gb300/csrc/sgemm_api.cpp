@@ -144,8 +144,9 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
                  p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.sk_tiles);
 }
 
-// TF32 tensor-core path: [repack A] [repack B] -> tcgen05 mainloop (one CTA per
-// 128 x 256 tile, or a CTA pair per 256 x 256 tile) [-> stream-K reduction].
+// TF32 tensor-core path: [repack A] [repack B] [copy C in] -> tcgen05 mainloop (one
+// CTA per 128 x 256 tile, or a CTA pair per 256 x 256 tile) [-> stream-K reduction]
+// [-> copy C back].
 int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int M, int N, int K, float alpha,
              const float *A, int lda, const float *B, int ldb, float beta, float *C, int ldc, cudaStream_t stream)
 {
@@ -177,19 +178,28 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     if ((rc = make_tmap(h, &tmB, b_src, N, K, b_ld, 32, sgemm_cfg::kTf32BK, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) !=
         SGEMM_OK)
         return rc;
+    // C not 16-byte accessible: computed in an aligned copy, copied back at the end
+    float *c_dst = C;
+    long long c_ld = ldc;
+    if (plan.repack_c) {
+        c_dst = reinterpret_cast<float *>(ws + w.c_off);
+        c_ld = w.ldc;
+        if (beta != 0.0f && launch_repack(C, ldc, c_dst, c_ld, M, N, h->num_sms, stream) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+    }
     Tf32Params p{};
     p.M = M;
     p.N = N;
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
-    p.C = C;
-    p.ldc = ldc;
+    p.C = c_dst;
+    p.ldc = c_ld;
     p.tiles_m = plan.tiles_m;
     p.tiles_n = plan.tiles_n;
     p.units = plan.units;
     p.kblocks = (K + sgemm_cfg::kTf32BK - 1) / sgemm_cfg::kTf32BK;
-    p.vec_c = plan.vec_c;
+    p.vec_c = plan.repack_c ? 1 : plan.vec_c;
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
     p.splits = 1;
@@ -198,7 +208,7 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         p.sk_tiles = plan.sk_tiles;
         p.sk_grid = plan.sk_grid;
     }
-    const bool dependent = plan.repack_a || plan.repack_b;
+    const bool dependent = plan.repack_a || plan.repack_b || (plan.repack_c && beta != 0.0f);
     const cudaError_t le = pair ? launch_tf32_pair(tmA, tmB, p, plan.grid, stream, dependent)
                                 : launch_tf32(tmA, tmB, p, plan.grid, stream, dependent);
     if (le != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -209,19 +219,22 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         r.N = N;
         r.alpha = alpha;
         r.beta = beta;
-        r.C = C;
-        r.ldc = ldc;
+        r.C = c_dst;
+        r.ldc = c_ld;
         r.W = p.W;
         r.tiles_m = plan.tiles_m;
         r.tiles_n = plan.tiles_n;
         r.units = p.units;
         r.splits = 1;
         r.kblocks = p.kblocks;
-        r.vec_c = plan.vec_c;
+        r.vec_c = p.vec_c;
         r.sk_tiles = p.sk_tiles;
         r.sk_grid = p.sk_grid;
         if (launch_sk_reduce(r, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
     }
+    // (an ordinary launch: it waits for the kernels above to complete)
+    if (plan.repack_c && launch_repack(c_dst, c_ld, C, ldc, M, N, h->num_sms, stream) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     return SGEMM_OK;
 }
 

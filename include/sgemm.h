@@ -100,6 +100,9 @@ typedef struct sgemm_plan_s {
                                 (0 = none) */
     int sk_grid;             /* workers sharing the stream-K span (the first sk_grid CTAs, or CTA
                                 pairs for the TF32 pair kernel) */
+    int repack_c;            /* TF32 mode, C not 16-byte accessible (and at least 256K elements):
+                                C is computed in an aligned workspace copy (filled from C when
+                                beta != 0) and copied back */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */

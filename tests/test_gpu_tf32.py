@@ -85,11 +85,17 @@ def test_ragged_problem(h):
     A, B, C = inputs.problem_operands("ragged")
     got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
     assert st == sg.SGEMM_OK and guards
-    assert h.last_plan().repack_a == 1
+    plan = h.last_plan()
+    # lda, ldb and ldc are not multiples of 4: both operands repacked, and C (6.1 M
+    # elements) computed in an aligned copy, filled from C (beta = 1) and copied back
+    assert plan.repack_a == 1 and plan.repack_b == 1 and plan.repack_c == 1
+    # repack A, repack B, copy C in, mainloop, [stream-K reduction,] copy C back
+    assert plan.launches == 5 + (1 if plan.sk_tiles else 0)
     _check(got, A, B, C, p["alpha"], p["beta"])
 
 
 def test_unaligned_and_padded(h):
+    """Padded and unaligned operands; C small enough to be written in place."""
     M, N, K = 190, 300, 130
     A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=6, dist=("int", "int", "int"))
     for lds, offs in [((K + 4, N + 8, N + 4), (0, 0, 0)), ((K + 1, N + 3, N + 1), (1, 2, 3))]:
@@ -147,7 +153,7 @@ def _stream_k_case(h, shape):
     assert st == sg.SGEMM_OK and guards
     plan = h.last_plan()
     _assert_kernel(h)
-    assert plan.sk_tiles > 0 and plan.launches == 2 + plan.repack_a + plan.repack_b, plan.as_dict()
+    assert plan.sk_tiles > 0 and plan.launches == 2 + plan.repack_a + plan.repack_b + 2 * plan.repack_c, plan.as_dict()
     rows = sample_rows(M) if M > 1024 else None
     _check(got, A, B, C, 1.5, 0.5, rows=rows, exact=True)
     Ar, Br, Cr = inputs.problem_operands(M=M, N=N, K=K, seed=M + K + 1, dist=("normal", "uniform", "uniform"))
@@ -156,3 +162,17 @@ def _stream_k_case(h, shape):
     _check(r1, Ar, Br, Cr, -1.0, 0.25, rows=rows)
     r2, _, _ = run_gemm(torch, h, Ar, Br, Cr, -1.0, 0.25)
     assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
+
+
+def test_unaligned_c_through_an_aligned_copy(h):
+    """A C that is not 16-byte accessible and large enough is computed in an aligned
+    workspace copy: with beta != 0 filled from C first, with beta == 0 not read; the pad
+    columns and guard bands around C are untouched either way."""
+    M, N, K = 600, 700, 96
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=17, dist=("int", "int", "int"))
+    for beta in (0.5, 0.0):
+        got, guards, st = run_gemm(torch, h, A, B, C, 1.5, beta, lds=(K, N, N + 1), offsets=(0, 0, 1))
+        assert st == sg.SGEMM_OK and guards
+        plan = h.last_plan()
+        assert plan.repack_c == 1 and plan.vec_c == 0, plan.as_dict()
+        _check(got, A, B, C, 1.5, beta, exact=True)
