@@ -34,6 +34,7 @@ L2_BYTES = 126 * 2**20  # GB300 L2 (nvidia-smi reports ~126 MiB)
 KERNEL_SOURCES = ["dense_fp32_gemm_04_gb300/csrc/ffma_kernels.cu", "dense_fp32_gemm_04_gb300/csrc/device_ptx.cuh",
                   "dense_fp32_gemm_04_gb300/csrc/schedule.cuh", "dense_fp32_gemm_04_gb300/csrc/tile_table.h"]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "ffma_sgemm_4096_traffic.md")
+TRAFFIC_WORKLOAD = "square4096"  # the workload that capture was taken on
 
 
 def parse_args(argv=None):
@@ -548,6 +549,9 @@ def run_ours(args, world):
     sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(world.local_rank)))
     sampler.start()
 
+    # Operands that fit in L2 would be timed warm: flush it (a 256 MiB write) before every
+    # call and take the time from the per-call events alone.
+    flush = torch.empty(64 * 2**20, dtype=torch.float32, device=dev) if operand_bytes <= L2_BYTES else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     world.barrier()
@@ -557,6 +561,8 @@ def run_ours(args, world):
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(1.0)
         starts[i].record(stream)
         h.run(dA, dB, dC, alpha, beta, stream=stream)
         ends[i].record(stream)
@@ -567,6 +573,9 @@ def run_ours(args, world):
     sampler.stop()
     elapsed = ev0.elapsed_time(ev1) / 1e3
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if flush is not None:
+        elapsed = sum(kernel_ms) / 1e3  # the flushes between calls are not GEMM time
+        del flush
     st, code = h.check_device_status()
     if st != sg.SGEMM_OK:
         raise RuntimeError(f"device status {code:#x} in the timed region")
@@ -606,7 +615,8 @@ def run_ours(args, world):
     sm_mhz = clocks["sm_mhz"] if clocks else None
     peak = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": (achieved / peak) if peak else None, "traffic": recorded_traffic(),
+                "frac": (achieved / peak) if peak else None,
+                "traffic": recorded_traffic() if args.workload == TRAFFIC_WORKLOAD else None,
                 "kernel": ("ffma_sgemm_kernel (plan config %d, %dx%d tile, A %s)" %
                            (plan.config, plan.bm, plan.bn, "transposed first" if plan.transpose_a else "as given")) +
                           (" + transpose_kernel (A^T)" if plan.transpose_a else "") +
@@ -623,7 +633,10 @@ def run_ours(args, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_text(p),
                    "M": M, "N": N, "K": K, "layout": "row-major",
-                   "l2": f"no flush: operands {operand_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB",
+                   "l2": (f"no flush: operands {operand_bytes / 2**20:.0f} MiB > L2 {L2_BYTES / 2**20:.0f} MiB"
+                          if operand_bytes > L2_BYTES else
+                          f"operands {operand_bytes / 2**20:.0f} MiB fit in L2: 256 MiB flush before every call, "
+                          "time from the per-call events"),
                    "parallelism": f"replicas x{world.size}", "plan": plan.as_dict(),
                    "operand_load_bytes_model": operand_load_bytes(M, N, K, plan.bm, plan.bn)},
         "pct_fp32_ffma_peak": (100.0 * achieved / peak) if peak else None,
