@@ -42,6 +42,7 @@ OPT_SKEW_NS = 6
 OPT_FORCE_TRANSPOSE_A = 7
 OPT_FORCE_STREAMK = 8
 OPT_FORCE_TF32_KERNEL = 9
+OPT_FORCE_REPACK_C = 10
 
 
 class Plan(ctypes.Structure):

@@ -721,6 +721,48 @@ __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int 
     if (e >= bm * q4) return;
     int tm, tn;
     decode_tile(p.tiles_m, p.tiles_n, p.units + rel, tm, tn);
+    if (!p.vec_c) {
+        // C not 16-byte accessible: the warp's 128 consecutive elements of the tile
+        // (tile-packed order) go one per lane and 32 apart, so that every access to C
+        // and to the partials is a coalesced 4-byte one; all partial loads come before
+        // the C accesses (same sums, same order as below)
+        const int lane = static_cast<int>(threadIdx.x & 31u);
+        const int t0 = 4 * (e - lane) + lane;  // t0 + 96 < bm * bn: whole blocks per tile (launch_sk_reduce)
+        bool in[4];
+        long long cidx[4];
+        float s[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int t = t0 + 32 * k;
+            const int lr = t / bn, lc = t - lr * bn;
+            const int row = tm * bm + lr, col = tn * bn + lc;
+            in[k] = row < p.M && col < p.N;
+            cidx[k] = static_cast<long long>(row) * p.ldc + col;
+            s[k] = in[k] ? __ldg(p.W + off[0] + t) : 0.0f;
+        }
+        for (int j = 1; j < nseg; ++j) {
+            long long o;
+            if (j < kSkMaxShared) {
+                o = off[j];
+            } else {
+                const long long g = g0 + j;
+                o = (2 * g + (rel == (g * S / G) / p.kblocks ? 0 : 1)) * bm * bn;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (in[k]) s[k] += __ldg(p.W + o + t0 + 32 * k);
+        }
+        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (p.beta != 0.0f) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (in[k]) c[k] = p.C[cidx[k]];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (in[k]) p.C[cidx[k]] = (p.beta != 0.0f) ? fmaf(p.alpha, s[k], p.beta * c[k]) : p.alpha * s[k];
+        return;
+    }
     const int lr = e / q4, lc = (e - lr * q4) * 4;
     const int row = tm * bm + lr, col = tn * bn + lc;
     if (row >= p.M || col >= p.N) return;
@@ -882,7 +924,8 @@ cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstrid
 cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)
 {
     (void)num_sms;
-    const dim3 grid((bm * (bn / 4) + 255) / 256, p.sk_tiles);  // sk_tiles < SMs * CTAs per SM
+    if ((bm * bn) % 1024 != 0) return cudaErrorInvalidValue;  // whole blocks of 256 column quads per tile
+    const dim3 grid(bm * (bn / 4) / 256, p.sk_tiles);  // sk_tiles < SMs * CTAs per SM
     return launch_kernel(true, sk_reduce_kernel, grid, dim3(256), 0, stream, p, bm, bn);
 }
 

@@ -26,6 +26,7 @@ struct Overrides {
     int force_transpose_a = -1;  // -1 automatic, 0 never, 1 always (FFMA kernel)
     int force_streamk = -1;      // -1 automatic, 0 never, 1 whenever the last round is partial
     int force_tf32_kernel = -1;  // -1 automatic, 0 one CTA per tile, 1 CTA pairs
+    int force_repack_c = -1;     // TF32, C not 16-byte accessible: -1 automatic, 0 in place, 1 aligned copy
 };
 
 // Offsets (bytes) into the handle's workspace and the strides used there.

@@ -722,6 +722,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
         if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
         h->ov.force_tf32_kernel = static_cast<int>(value);
         return SGEMM_OK;
+    case SGEMM_OPT_FORCE_REPACK_C:
+        if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.force_repack_c = static_cast<int>(value);
+        return SGEMM_OK;
     default:
         return SGEMM_ERR_INVALID_VALUE;
     }

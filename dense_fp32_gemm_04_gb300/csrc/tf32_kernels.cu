@@ -152,11 +152,101 @@ __device__ __forceinline__ void store_partial_row(uint32_t t_row, float *wrow)
     }
 }
 
+// Shifted frame for a row of C that is not 16-byte aligned. With s the number of
+// elements before the row's first 16-byte boundary (C itself is 4-byte aligned),
+// the row is written in 4-element chunks at columns s - 4 + 4j: every chunk that
+// lies wholly inside [0, lim) is one 16-byte access, the rest (the first chunk,
+// the last one when s != 0, chunks past N) go element by element. The step's
+// accumulator values come after the previous step's last four (x[0..3]), so
+// chunk j of a step holds x[4j + s .. 4j + s + 3]; `pick` makes that runtime
+// offset a choice among four registers (i is a constant once the loops unroll).
+__device__ __forceinline__ float pick(const float *x, int i, int s)
+{
+    return s == 0 ? x[i] : s == 1 ? x[i + 1] : s == 2 ? x[i + 2] : x[i + 3];
+}
+
+__device__ __forceinline__ bool chunk_whole(int r0, int lim) { return r0 >= 0 && r0 + 3 < lim; }
+
+__device__ __forceinline__ float4 load_chunk(const float *cbase, int r0, int lim)
+{
+    if (chunk_whole(r0, lim)) return *reinterpret_cast<const float4 *>(cbase + r0);
+    float e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) e[q] = (r0 + q >= 0 && r0 + q < lim) ? cbase[r0 + q] : 0.0f;
+    return make_float4(e[0], e[1], e[2], e[3]);
+}
+
+__device__ __forceinline__ void store_chunk(const Tf32Params &p, float *cbase, int r0, int lim, const float (&a)[4],
+                                            float4 c)
+{
+    float4 out;
+    if (p.beta != 0.0f)
+        out = make_float4(fmaf(p.alpha, a[0], p.beta * c.x), fmaf(p.alpha, a[1], p.beta * c.y),
+                          fmaf(p.alpha, a[2], p.beta * c.z), fmaf(p.alpha, a[3], p.beta * c.w));
+    else
+        out = make_float4(p.alpha * a[0], p.alpha * a[1], p.alpha * a[2], p.alpha * a[3]);
+    if (chunk_whole(r0, lim)) {
+        *reinterpret_cast<float4 *>(cbase + r0) = out;
+    } else {
+        const float e[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (r0 + q >= 0 && r0 + q < lim) cbase[r0 + q] = e[q];
+    }
+}
+
+// The tile's part of row `row` of C (cbase = its first column, lim = the columns
+// of the tile inside N) in the shifted frame; same steps and load batching as
+// store_c_row.
+template <int NB>
+__device__ __forceinline__ void store_c_row_shifted(const Tf32Params &p, uint32_t t_row, int row, float *cbase,
+                                                    int lim)
+{
+    const int s = static_cast<int>((4u - ((static_cast<uint32_t>(reinterpret_cast<uintptr_t>(cbase)) >> 2) & 3u)) & 3u);
+    float x[16 * NB + 4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = 0.0f;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 16; ch += NB) {
+        uint32_t v[NB][16];
+        load_row_chunks<NB>(t_row + ch * 16, v);  // every lane: .sync.aligned
+        if (row >= p.M) continue;
+#pragma unroll
+        for (int i = 0; i < 16 * NB; ++i) x[4 + i] = __uint_as_float(v[i >> 4][i & 15]);
+        const int cb = ch * 16 + s - 4;  // column of chunk 0
+        float4 c[4 * NB];
+        if (p.beta != 0.0f) {
+#pragma unroll
+            for (int j = 0; j < 4 * NB; ++j) c[j] = load_chunk(cbase, cb + 4 * j, lim);
+        }
+#pragma unroll
+        for (int j = 0; j < 4 * NB; ++j) {
+            const float a[4] = {pick(x, 4 * j, s), pick(x, 4 * j + 1, s), pick(x, 4 * j + 2, s),
+                                pick(x, 4 * j + 3, s)};
+            store_chunk(p, cbase, cb + 4 * j, lim, a, c[j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = x[16 * NB + i];
+    }
+    if (row >= p.M) return;
+    // last chunk: columns BN - 4 + s .. BN - 1 (x[s..3]); the rest of it is the next tile's
+    float y[8] = {x[0], x[1], x[2], x[3], 0.0f, 0.0f, 0.0f, 0.0f};
+    const int r0 = BN - 4 + s;
+    const int lim_last = min(lim, BN);
+    const float4 c = p.beta != 0.0f ? load_chunk(cbase, r0, lim_last) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float a[4] = {pick(y, 0, s), pick(y, 1, s), pick(y, 2, s), pick(y, 3, s)};
+    store_chunk(p, cbase, r0, lim_last, a, c);
+}
+
 // C[row, tn*BN ...] = alpha * acc + beta * C (beta == 0: C not read).
 template <int NB>
 __device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row, int row, int tn)
 {
     float *crow = p.C + static_cast<long long>(row) * p.ldc;
+    if (!p.vec_c) {
+        store_c_row_shifted<(NB > 2 ? 2 : NB)>(p, t_row, row, crow + tn * BN, min(BN, p.N - tn * BN));
+        return;
+    }
 #pragma unroll 1
     for (int ch = 0; ch < BN / 16; ch += NB) {
         uint32_t v[NB][16];
@@ -183,9 +273,8 @@ __device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row,
                 *reinterpret_cast<float4 *>(crow + colb + 4 * q) = out;
             }
         } else {
-            // N edge or C not 16-byte accessible: element by element, every C load of
-            // the step issued before any use (one memory latency per step, not one per
-            // element)
+            // N edge: element by element, every C load of the step issued before any
+            // use (one memory latency per step, not one per element)
             float c[16 * NB];
             if (p.beta != 0.0f) {
 #pragma unroll

@@ -100,9 +100,9 @@ typedef struct sgemm_plan_s {
                                 (0 = none) */
     int sk_grid;             /* workers sharing the stream-K span (the first sk_grid CTAs, or CTA
                                 pairs for the TF32 pair kernel) */
-    int repack_c;            /* TF32 mode, C not 16-byte accessible (and at least 256K elements):
-                                C is computed in an aligned workspace copy (filled from C when
-                                beta != 0) and copied back */
+    int repack_c;            /* TF32 mode, C not 16-byte accessible and SGEMM_OPT_FORCE_REPACK_C
+                                = 1: C is computed in an aligned workspace copy (filled from C
+                                when beta != 0) and copied back (0: C written in place) */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */
@@ -121,10 +121,14 @@ typedef enum sgemm_option {
                                      1 = always transpose A first (same results either way) */
     SGEMM_OPT_FORCE_STREAMK = 8,  /* -1 = automatic (the default), 0 = never, 1 = whenever the last
                                      round of tiles is partial (ignored with forced splits) */
-    SGEMM_OPT_FORCE_TF32_KERNEL = 9 /* TF32 mode: -1 = automatic (the default), 0 = one CTA per
+    SGEMM_OPT_FORCE_TF32_KERNEL = 9, /* TF32 mode: -1 = automatic (the default), 0 = one CTA per
                                      128 x 256 tile, 1 = a CTA pair (cluster of two, tcgen05
                                      .cta_group::2) per 256 x 256 tile; 1 fails with
                                      SGEMM_ERR_NOT_SUPPORTED where no pair fits */
+    SGEMM_OPT_FORCE_REPACK_C = 10 /* TF32 mode, C not 16-byte accessible: -1 = automatic (the
+                                     default) and 0 = write C in place (16-byte accesses inside
+                                     each row, element by element at its ends); 1 = compute into
+                                     an aligned workspace copy of C and copy it back */
 } sgemm_option_t;
 
 /*

@@ -198,6 +198,10 @@ def test_tf32_plan(lib):
     # an odd SM count: pairs = floor(SMs / 2), the grid is whole pairs
     p = sg.plan(4096, 4096, 4096, num_sms=151, math_mode=sg.MATH_TF32)
     assert p.config == 1 and p.grid == 150
+    # C not 16-byte accessible (ldc not a multiple of 4): written in place, no copy of C
+    p = sg.plan(2047, 3001, 1531, math_mode=sg.MATH_TF32)
+    assert p.vec_c == 0 and p.repack_c == 0 and p.repack_a == 1 and p.repack_b == 1
+    assert p.launches == 3 + (1 if p.sk_tiles else 0)
 
 
 def test_tf32_single_cta_plan(lib):

@@ -6,7 +6,8 @@ The fixed cases of the other GPU tests sit on chosen edges (tile multiples +-1,
 the benchmark problems); this sweep draws the combinations in between, where a
 scheduling or indexing mistake (a stream-K range boundary, a split slice, a
 partial pair tile, a repacked operand with an offset, a ragged row or column of
-the staged 128 x 128 epilogue) would show up. The FP32 cases also force a random
+the staged 128 x 128 epilogue, an unaligned row of C written in place or through
+its aligned copy) would show up. The FP32 cases also force a random
 tile-config row. Integer
 operands must be bit-exact; real ones must lie inside the mode's bound (for
 TF32 also the tight bound of test_gpu_tf32). Every case also checks the canary
@@ -85,6 +86,10 @@ def test_random_problems(lib_built, mode):
                 h.set_option(sg.OPT_FORCE_CONFIG, opts["config"])
                 h.set_option(sg.OPT_FORCE_SPLITS, opts["splits"])
                 h.set_option(sg.OPT_FORCE_TRANSPOSE_A, opts["transpose_a"])
+            else:
+                # C written in place or through an aligned copy (own generator: the
+                # cases drawn above stay the same)
+                h.set_option(sg.OPT_FORCE_REPACK_C, int(np.random.default_rng(case).choice([-1, 0, 1])))
             A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=1000 + case, dist=dist)
             lds = (K + pads[0], N + pads[1], N + pads[2])
             got, guards, st = run_gemm(torch, h, A, B, C, alpha, beta, lds=lds, offsets=offsets)

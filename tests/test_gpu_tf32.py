@@ -86,11 +86,11 @@ def test_ragged_problem(h):
     got, guards, st = run_gemm(torch, h, A, B, C, p["alpha"], p["beta"])
     assert st == sg.SGEMM_OK and guards
     plan = h.last_plan()
-    # lda, ldb and ldc are not multiples of 4: both operands repacked, and C (6.1 M
-    # elements) computed in an aligned copy, filled from C (beta = 1) and copied back
-    assert plan.repack_a == 1 and plan.repack_b == 1 and plan.repack_c == 1
-    # repack A, repack B, copy C in, mainloop, [stream-K reduction,] copy C back
-    assert plan.launches == 5 + (1 if plan.sk_tiles else 0)
+    # lda, ldb and ldc are not multiples of 4: both operands repacked, C written in
+    # place (16-byte accesses inside each row)
+    assert plan.repack_a == 1 and plan.repack_b == 1 and plan.repack_c == 0 and plan.vec_c == 0
+    # repack A, repack B, mainloop, [stream-K reduction]
+    assert plan.launches == 3 + (1 if plan.sk_tiles else 0)
     _check(got, A, B, C, p["alpha"], p["beta"])
 
 
@@ -164,15 +164,24 @@ def _stream_k_case(h, shape):
     assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
 
 
-def test_unaligned_c_through_an_aligned_copy(h):
-    """A C that is not 16-byte accessible and large enough is computed in an aligned
-    workspace copy: with beta != 0 filled from C first, with beta == 0 not read; the pad
-    columns and guard bands around C are untouched either way."""
-    M, N, K = 600, 700, 96
+@pytest.mark.parametrize("repack_c", [0, 1])
+@pytest.mark.parametrize("K", [96, 600])
+def test_unaligned_c_in_place_or_through_a_copy(h, repack_c, K):
+    """A C that is not 16-byte accessible, written in place (16-byte accesses inside
+    each row, whose first aligned column differs from row to row, element by element
+    at the row ends and past N) or computed in an aligned workspace copy (filled from
+    C first when beta != 0). Short K (3 k-blocks) and long K (19) take the epilogue's
+    two step widths; N = 700 leaves a partial last tile. Pad columns and guard bands
+    around C stay untouched."""
+    M, N = 600, 700
     A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=17, dist=("int", "int", "int"))
-    for beta in (0.5, 0.0):
-        got, guards, st = run_gemm(torch, h, A, B, C, 1.5, beta, lds=(K, N, N + 1), offsets=(0, 0, 1))
-        assert st == sg.SGEMM_OK and guards
-        plan = h.last_plan()
-        assert plan.repack_c == 1 and plan.vec_c == 0, plan.as_dict()
-        _check(got, A, B, C, 1.5, beta, exact=True)
+    h.set_option(sg.OPT_FORCE_REPACK_C, repack_c)
+    try:
+        for beta, pad, off in ((0.5, 1, 1), (0.0, 1, 1), (1.0, 2, 3), (-1.0, 3, 2), (0.5, 4, 1)):
+            got, guards, st = run_gemm(torch, h, A, B, C, 1.5, beta, lds=(K, N, N + pad), offsets=(0, 0, off))
+            assert st == sg.SGEMM_OK and guards
+            plan = h.last_plan()
+            assert plan.repack_c == repack_c and plan.vec_c == 0, plan.as_dict()
+            _check(got, A, B, C, 1.5, beta, exact=True)
+    finally:
+        h.set_option(sg.OPT_FORCE_REPACK_C, -1)
