@@ -125,6 +125,7 @@ int check_args(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
                float *C, int ldc)
 {
     if (h == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    if (!elem_aligned(A) || !elem_aligned(B) || !elem_aligned(C)) return SGEMM_ERR_INVALID_VALUE;
     Problem q{M, N, K, lda, ldb, ldc, 0, 1, SGEMM_MATH_FP32, alpha, 0.0f};
     const int v = validate(q);
     if (v != SGEMM_OK) return v;
@@ -642,7 +643,8 @@ int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
 {
     const int v = check_args(h, M, N, K, alpha, A, lda, B, ldb, C, ldc);
     if (v != SGEMM_OK) return v;
-    if (min_vals == nullptr || min_ij == nullptr) return SGEMM_ERR_INVALID_VALUE;
+    if (min_vals == nullptr || min_ij == nullptr || !elem_aligned(min_vals) || !elem_aligned(min_ij))
+        return SGEMM_ERR_INVALID_VALUE;
     DeviceGuard g(h->device);
     if (!g.ok) return SGEMM_ERR_CUDA;
     int rc = run_device(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
@@ -657,6 +659,7 @@ int sgemm_ladder_run(int rung, int M, int N, int K, float alpha, const float *A,
                      struct CUstream_st *stream)
 {
     if (rung < 1 || rung > 7 || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (!elem_aligned(A) || !elem_aligned(B) || !elem_aligned(C)) return SGEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return SGEMM_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return SGEMM_ERR_INVALID_VALUE;
     if (M > (1 << 21)) return SGEMM_ERR_NOT_SUPPORTED;

@@ -11,6 +11,10 @@
 
 namespace sgemm_impl {
 
+// A pointer the kernels may dereference as float (or int): NULL or 4-byte aligned.
+// Checked on the host before any launch; a misaligned one is SGEMM_ERR_INVALID_VALUE.
+inline bool elem_aligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
 // Device status codes: (sgemm_status << 16) | where.
 enum : int {
     kWhereConsumerFull = 1,  // a consumer's wait for a filled stage ran out

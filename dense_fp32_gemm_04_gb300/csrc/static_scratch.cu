@@ -129,6 +129,9 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
                                        struct CUstream_st *stream)
 {
     if (splits < 1 || splits > sgemm_impl::kMaxSplits) return SGEMM_ERR_INVALID_VALUE;
+    if (!sgemm_impl::elem_aligned(A) || !sgemm_impl::elem_aligned(B) || !sgemm_impl::elem_aligned(C) ||
+        !sgemm_impl::elem_aligned(device_status))
+        return SGEMM_ERR_INVALID_VALUE;
     const int align = (aligned16(A) ? 1 : 0) | (aligned16(B) ? 2 : 0) | (aligned16(C) ? 4 : 0);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

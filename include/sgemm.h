@@ -161,8 +161,9 @@ int sgemm_destroy(sgemm_handle_t h);
  * A, B, C: caller-owned DEVICE pointers (the library never frees them).
  * Requirements: M, N, K >= 0; lda >= max(1, K); ldb >= max(1, N);
  * ldc >= max(1, N); A and B non-NULL when M, N > 0 and K > 0 and alpha != 0;
- * C non-NULL when M, N > 0. Any violation returns SGEMM_ERR_INVALID_VALUE
- * and touches nothing. SGEMM_ERR_ALLOC if the workspace cannot grow.
+ * C non-NULL when M, N > 0; A, B and C 4-byte aligned (a float's alignment;
+ * 16-byte alignment only selects the faster path). Any violation returns
+ * SGEMM_ERR_INVALID_VALUE and touches nothing. SGEMM_ERR_ALLOC if the workspace cannot grow.
  */
 int sgemm_run(sgemm_handle_t h, int M, int N, int K,
               float alpha, const float *A, int lda,
@@ -212,8 +213,8 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K,
  * contents: calls that overlap on the GPU (e.g. on two unordered streams)
  * race on it.
  *
- * device_status: optional caller-owned device int that receives the
- * kernels' watchdog code (see sgemm_check_device_status); it is set to 0 on
+ * device_status: optional caller-owned device int (4-byte aligned, checked
+ * with the operands before anything else) that receives the kernels' watchdog code (see sgemm_check_device_status); it is set to 0 on
  * `stream` at the start of the call. NULL uses an internal static word.
  *
  * The first call on a device performs a one-time set-up with that device

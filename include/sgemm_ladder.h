@@ -30,7 +30,7 @@ struct CUstream_st;
  * matrices (A: M x K, B: K x N, C: M x N, leading dimensions K, N, N), on the
  * current device, asynchronously on `stream`. beta == 0: C is not read.
  * Returns SGEMM_OK, SGEMM_ERR_INVALID_VALUE (unknown rung, negative dimension,
- * NULL operand with work to do), SGEMM_ERR_NOT_SUPPORTED (rungs 6 and 7 need
+ * NULL operand with work to do, an operand not 4-byte aligned), SGEMM_ERR_NOT_SUPPORTED (rungs 6 and 7 need
  * K % 4 == 0, N % 4 == 0 and 16-byte-aligned A and B, as the page's vectorised
  * kernel does; M > 2^21) or SGEMM_ERR_LAUNCH.
  */

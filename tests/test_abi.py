@@ -52,6 +52,25 @@ def test_create_without_gpu_fails_cleanly(lib):
     assert st in (sg.SGEMM_ERR_ARCH, sg.SGEMM_ERR_INVALID_VALUE) and not h.value
 
 
+def test_misaligned_pointers_are_refused_on_the_host(lib):
+    """An operand pointer that is not 4-byte aligned (a float's alignment) is refused
+    with SGEMM_ERR_INVALID_VALUE before any CUDA call. On this GPU-less host the same
+    call with aligned pointers passes that check and fails later (no device), which
+    shows the check is what refused the misaligned ones. The pointers are never
+    dereferenced on the host."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the aligned fake pointers would reach a launch")
+    good, bad = 0x100000, 0x100002
+    args = lambda a, b, c, st: (4, 4, 4, 1.0, a, 4, b, 4, 0.0, c, 4, 1, st, None)
+    for ptrs in ((bad, good, good, None), (good, bad, good, None), (good, good, bad, None), (good, good, good, bad)):
+        assert lib.sgemm_run_splitk_static(*args(*ptrs)) == sg.SGEMM_ERR_INVALID_VALUE, ptrs
+    assert lib.sgemm_run_splitk_static(*args(good, good, good, None)) == sg.SGEMM_ERR_CUDA
+    for ptrs in ((bad, good, good), (good, bad, good), (good, good, bad)):
+        assert lib.sgemm_ladder_run(1, 4, 4, 4, 1.0, ptrs[0], ptrs[1], 0.0, ptrs[2], None) == sg.SGEMM_ERR_INVALID_VALUE
+    assert lib.sgemm_ladder_run(1, 4, 4, 4, 1.0, good, good, 0.0, good, None) != sg.SGEMM_ERR_INVALID_VALUE
+
+
 @pytest.mark.parametrize("args", [
     (-1, 4, 4, 4, 4, 4), (4, -1, 4, 4, 4, 4), (4, 4, -1, 4, 4, 4),
     (4, 4, 8, 7, 4, 4),   # lda < K
