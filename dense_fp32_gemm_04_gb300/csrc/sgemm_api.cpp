@@ -179,7 +179,8 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     if ((rc = make_tmap(h, &tmB, b_src, N, K, b_ld, 32, sgemm_cfg::kTf32BK, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B)) !=
         SGEMM_OK)
         return rc;
-    // C not 16-byte accessible: computed in an aligned copy, copied back at the end
+    // plan.repack_c (C not 16-byte accessible, SGEMM_OPT_FORCE_REPACK_C = 1): computed in an
+    // aligned copy, copied back at the end; otherwise the kernel writes C in place
     float *c_dst = C;
     long long c_ld = ldc;
     if (plan.repack_c) {
