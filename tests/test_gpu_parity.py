@@ -166,6 +166,16 @@ def test_invalid_arguments_touch_nothing(h):
     assert np.array_equal(bufs[2].cpu().numpy(), C)
 
 
+def test_option_values_are_checked(h):
+    """Out-of-range option values and unknown options are refused and change nothing."""
+    lib = sg.library()
+    for opt, bad in ((sg.OPT_FORCE_TF32_KERNEL, 2), (sg.OPT_FORCE_REPACK_C, 2), (sg.OPT_FORCE_REPACK_C, -2),
+                     (sg.OPT_FORCE_STREAMK, 2), (sg.OPT_FORCE_TRANSPOSE_A, -2), (99, 0)):
+        assert lib.sgemm_set_option(h._h, opt, bad) == sg.SGEMM_ERR_INVALID_VALUE, (opt, bad)
+    for opt in (sg.OPT_FORCE_TF32_KERNEL, sg.OPT_FORCE_REPACK_C, sg.OPT_FORCE_STREAMK, sg.OPT_FORCE_TRANSPOSE_A):
+        assert lib.sgemm_set_option(h._h, opt, -1) == sg.SGEMM_OK
+
+
 def test_non_default_stream(h):
     A, B, C = ops(333, 222, 111, seed=8)
     dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
