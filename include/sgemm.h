@@ -88,7 +88,9 @@ typedef struct sgemm_plan_s {
                                 tiles before the stream-K span */
     int grid;                /* CTAs launched (persistent: min(units, SMs * ctas_per_sm)) */
     int repack_a, repack_b;  /* operand first copied to a 16-byte-aligned workspace copy */
-    int vec_c;               /* 1: C read/written with 16-byte accesses */
+    int vec_c;               /* 1: C (base and ldc) 16-byte accessible, read/written with 16-byte
+                                accesses; 0: 4-byte accesses (FP32 path), or in TF32 mode 16-byte
+                                accesses from each row's first 16-byte boundary on */
     int math_mode;           /* sgemm_math_mode_t */
     int launches;            /* kernels one sgemm_run launches for this plan */
     long long workspace_bytes; /* device workspace the handle holds for it */
