@@ -43,7 +43,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=WORKLOAD)
+    from dense_fp32_gemm_04_gb300 import inputs
+
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.PROBLEMS),
+                    help="configured problem timed as the headline (default: %(default)s)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--tf32-steps", type=int, default=50, help="calls timed in the flagged TF32 mode (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
