@@ -221,6 +221,12 @@ def test_tf32_plan(lib):
     p = sg.plan(2047, 3001, 1531, math_mode=sg.MATH_TF32)
     assert p.vec_c == 0 and p.repack_c == 0 and p.repack_a == 1 and p.repack_b == 1
     assert p.launches == 3 + (1 if p.sk_tiles else 0)
+    # at any size, and for an unaligned C base (align bit 2 clear) as well
+    for (M, N, K, ldc, align) in [(8191, 8191, 512, 8191, 7), (4096, 4096, 4096, 4096, 3), (300, 301, 64, 301, 7),
+                                  (4095, 4093, 4096, 4093, 7)]:
+        p = sg.plan(M, N, K, ldc=ldc, align_flags=align, math_mode=sg.MATH_TF32)
+        assert p.vec_c == 0 and p.repack_c == 0, (M, N, K, ldc, align)
+        assert p.launches == p.repack_a + p.repack_b + 1 + (1 if p.sk_tiles else 0)
 
 
 def test_tf32_single_cta_plan(lib):
