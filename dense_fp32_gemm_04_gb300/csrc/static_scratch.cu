@@ -16,7 +16,8 @@
 //  * Every GPU that loads this library holds the array until process exit.
 //  * All calls on a device share the array, which keeps the last call's
 //    contents; calls that overlap on the GPU (different streams, no ordering
-//    between them) race on it and must be avoided by the caller.
+//    between them) race on it and must be avoided by the caller. The same holds
+//    for the internal watchdog word used when the caller passes no status word.
 //  * The first call on a device does a one-time set-up with that device
 //    current (symbol address lookup, kernel attributes); make that first call
 //    before any stream capture.
@@ -42,7 +43,9 @@ constexpr long long kTimeoutNs = 4000000000LL;
 
 // Partials (and aligned operand copies) of sgemm_run_splitk_static.
 static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
-// Watchdog word used when the caller passes no status pointer.
+// Watchdog word used when the caller passes no status pointer. Nothing reads it
+// back: with a NULL status pointer a timeout code is dropped (calls that overlap
+// on the GPU race on it like they race on g_scratch).
 static __device__ __align__(256) int g_status[64];
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -155,18 +158,22 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
     ov.force_streamk = 0;
     sgemm_plan_t plan;
     if ((rc = sgemm_impl::make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
-    if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;
     cudaStream_t st = stream;
+    const Workspace w = sgemm_impl::workspace_layout(q, plan);
+    const bool gemm = plan.kernel != SGEMM_KERNEL_NONE && plan.kernel != SGEMM_KERNEL_SCALE;
+    if (gemm && static_cast<unsigned long long>(w.total) > kStaticScratchBytes) return SGEMM_ERR_NOT_SUPPORTED;
+
+    // The watchdog word starts at zero for every call that succeeds, also for the
+    // quick returns, so a caller that reuses its word never reads an old code.
+    int *status = device_status ? device_status : s->status;
+    if ((gemm || device_status) && cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    if (plan.kernel == SGEMM_KERNEL_NONE) return SGEMM_OK;
     if (plan.kernel == SGEMM_KERNEL_SCALE)
         return sgemm_impl::launch_scale(M, N, beta, C, ldc, s->num_sms, st) == cudaSuccess ? SGEMM_OK
                                                                                             : SGEMM_ERR_LAUNCH;
-
-    const Workspace w = sgemm_impl::workspace_layout(q, plan);
-    if (static_cast<unsigned long long>(w.total) > kStaticScratchBytes) return SGEMM_ERR_NOT_SUPPORTED;
-
-    // The watchdog word must start at zero for this call.
-    int *status = device_status ? device_status : s->status;
-    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return SGEMM_ERR_CUDA;
 
     unsigned char *ws = s->scratch;
     const float *a_src = A;

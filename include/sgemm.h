@@ -213,11 +213,17 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K,
  * otherwise the call returns SGEMM_ERR_NOT_SUPPORTED and launches nothing.
  * All calls on a device share the array and it keeps the last call's
  * contents: calls that overlap on the GPU (e.g. on two unordered streams)
- * race on it.
+ * race on it, and, when they pass no status word, on the internal one too.
  *
- * device_status: optional caller-owned device int (4-byte aligned, checked
- * with the operands before anything else) that receives the kernels' watchdog code (see sgemm_check_device_status); it is set to 0 on
- * `stream` at the start of the call. NULL uses an internal static word.
+ * device_status: optional caller-owned DEVICE int (4-byte aligned, checked
+ * with the operands before anything else). Every call that returns SGEMM_OK
+ * sets it to 0 on `stream` before its kernels (quick returns included); a
+ * bounded wait that runs out in a kernel then writes
+ * (SGEMM_ERR_TIMEOUT << 16) | location into it, and C may be partly written.
+ * Read it after synchronizing `stream`. A call that returns an error enqueues
+ * nothing and leaves the word as it was. With NULL the kernels write into an
+ * internal static word that no call reads back, so a timeout code is lost:
+ * callers that need to know pass their own word.
  *
  * The first call on a device performs a one-time set-up with that device
  * current (looks up the array's device address, sets kernel attributes);
