@@ -19,19 +19,22 @@
 //    is the pages' zero-fill predication ("SGEMM CUDA kernel (First Half)",
 //    Part 5 load_ast) done in hardware.
 //  * A layout and bank conflicts: the pages transpose A in shared memory so a
-//    thread's TM values of A are contiguous (same page, Part 5). Here the
-//    transposition happens once per call, in global memory: transpose_kernel
-//    writes A^T (K x M, M contiguous) into the handle's workspace and the copy
-//    engine stages As[k][m] slabs of it exactly like B. A thread owns rows
-//    4r..4r+3 and 16+4r..16+4r+3 of its warp tile and columns 4c..4c+3 and
-//    32+4c..32+4c+3; per k it reads two 128-bit words of A and two of B.
-//    The 8 lanes sharing r read the same A word (a broadcast) and the 8 lanes
-//    sharing c read 8 consecutive B words, so every 128-bit shared load is
-//    conflict-free. When transposing A costs more than it saves (N small
-//    against M * K), A stays K-major as the caller gave it: a thread then
-//    takes rows r, r+4, ..., r+28 and reads 4 consecutive k of one row per
-//    128-bit load, and the 128-byte swizzle of the A slab puts the four row
-//    groups of a warp in four distinct bank quads.
+//    thread's TM values of A are contiguous (same page, Part 5). Here A
+//    reaches the compute warps M-major in one of two ways. Either
+//    transpose_kernel writes A^T (K x M, M contiguous) into the handle's
+//    workspace once per call and the copy engine stages As[k][m] slabs of it
+//    exactly like B, or (when that copy costs more than it saves: N small
+//    against M * K) the copy engine stages A as given and a transposer warp
+//    rewrites each slab M-major in shared memory (TMA cannot transpose 4-byte
+//    elements). A thread owns rows 4r..4r+3 and 16+4r..16+4r+3 of its warp
+//    tile and columns 4c..4c+3 and 32+4c..32+4c+3; per k it reads two 128-bit
+//    words of A and two of B. The 8 lanes sharing r read the same A word (a
+//    broadcast) and the 8 lanes sharing c read 8 consecutive B words, so every
+//    128-bit shared load is conflict-free. A third form, kept for comparison
+//    and reachable by option, reads A K-major as given: a thread then takes
+//    rows r, r+4, ..., r+28 and reads 4 consecutive k of one row per 128-bit
+//    load, and the 128-byte swizzle of the A slab puts the four row groups of
+//    a warp in four distinct bank quads.
 //  * Arithmetic: packed FFMA2 (two FP32 fused multiply-adds per instruction,
 //    round-to-nearest-even, sm_100+) halves the issue slots the 64 FMAs of a
 //    k-step need. With A^T the packed operand is a pair of A values along M
@@ -39,7 +42,7 @@
 //    sustains about 10 % more of this form than of (a_m, a_m) * (b_n, b_n+1),
 //    which the K-major layout has to use because its two A values of a pair
 //    would sit in different 128-bit loads. Either way each output is one chain
-//    of IEEE FP32 FMAs in ascending k, so both layouts give identical bits.
+//    of IEEE FP32 FMAs in ascending k, so all three layouts give identical bits.
 //  * Persistent grid: CTAs loop over (tile, split) work units in a grouped
 //    order; the producer keeps prefetching across unit boundaries.
 //  * Epilogue: the pages write C from the compute threads once their K loop
@@ -68,27 +71,37 @@ using sgemm_cfg::kFfmaBK;
 
 constexpr int kTimeoutCode = 5 << 16;  // SGEMM_ERR_TIMEOUT << 16
 
-template <int BM_, int BN_, int STAGES_, int MINB_, int EPI_ = 0>
+// Where the mainloop's A operand comes from (plan.transpose_a):
+//  kAKMajor  A as given, staged K-major (128-byte swizzle), FFMA2 form (a_m, a_m) * (b_n, b_n+1);
+//  kAMMajor  A^T written to the workspace by transpose_kernel first, staged M-major like B;
+//  kASmemT   A as given, staged K-major, then turned M-major in shared memory by a
+//            transposer warp; the compute warps read it like A^T.
+enum : int { kAKMajor = 0, kAMMajor = 1, kASmemT = 2 };
+
+template <int BM_, int BN_, int STAGES_, int MINB_, int EPI_ = 0, int XB_ = 0>
 struct Tile {
     static constexpr int BM = BM_, BN = BN_, STAGES = STAGES_, MINB = MINB_, BK = kFfmaBK;
     static constexpr int EPI = EPI_;  // > 0: a staging tile and EPI epilogue warps
+    static constexpr int XB = XB_;    // > 0: XB M-major A buffers and a transposer warp (kASmemT)
     static constexpr int WM = 32, WN = 64;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
     static constexpr int CONSUMERS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMERS + 1 + EPI) * 32;
+    static constexpr int THREADS = (CONSUMERS + 1 + (XB > 0 ? 1 : 0) + EPI) * 32;
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = BK * BN * 4;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int XBUF_BYTES = XB * A_BYTES;
     static constexpr int STAGING_BYTES = (EPI > 0 ? 1 : 0) * BM * BN * 4;
-    static constexpr int SMEM_BYTES = sgemm_cfg::ffma_smem_bytes(BM, BN, STAGES, EPI);
+    static constexpr int SMEM_BYTES = sgemm_cfg::ffma_smem_bytes(BM, BN, STAGES, EPI, XB);
     static_assert(EPI == 0 || (BN == 128 && BM % EPI == 0),
                   "an epilogue warp moves one 16-byte word of a staged row per lane, whole rows per warp");
     static_assert(BM % WM == 0 && BN % WN == 0, "CTA tile must be a multiple of the warp tile");
     static_assert(BM <= 256 && BN <= 256, "a TMA box side is at most 256 elements");
     static_assert(A_BYTES % 1024 == 0, "A stages must keep the 1024-byte swizzle alignment");
+    static_assert(XB == 0 || (BM == 64 || BM == 128), "the transposer warp covers 64 or 128 rows per slab");
 };
 
-template <class T, bool AT>
+template <class T, int AL>
 __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUtensorMap *tmB,
                                               const FfmaParams &p, uint32_t a_base, uint32_t b_base,
                                               uint32_t bar_base, volatile int *abort_flag)
@@ -117,7 +130,7 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
             const bool skip = (p.inject_skip >= 0 && blockIdx.x == 0 && seq == p.inject_skip);
             if (!skip) {
                 mbar_arrive_expect_tx(full, T::STAGE_BYTES);
-                if (AT)  // A^T slab: BK rows of k, BM consecutive m
+                if (AL == kAMMajor)  // A^T slab: BK rows of k, BM consecutive m
                     tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, tm * T::BM, kb * T::BK);
                 else  // A slab: BM rows of m, BK consecutive k (128-byte swizzle)
                     tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, kb * T::BK, tm * T::BM);
@@ -425,6 +438,92 @@ __device__ __forceinline__ float4 lds128(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void sts32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// One staged K-major A slab (BM rows of 32 k, 128-byte swizzle: 16-byte chunk
+// q of row m sits at chunk q ^ (m & 7)) rewritten M-major (32 rows of BM m),
+// the layout the compute warps read A^T in. This is the pages' transposition of
+// A on its way into shared memory ("SGEMM CUDA kernel (First Half)", Part 5),
+// done by one warp after the copy engine has landed the slab, since TMA cannot
+// transpose 4-byte elements.
+//
+// Lane l takes row m = 32 blk + l of each 32-row block: it loads the row's 8
+// chunks of 4 k (16 bytes each) and stores each value on its own into M-major
+// row k. A quarter-warp's 8 loads of chunk t read rows with 8 different
+// (m & 7), so the swizzle puts them in 8 different 16-byte bank groups; a
+// warp's 4-byte stores of one k cover 32 consecutive m, one bank each. Both
+// sides are conflict-free and no value moves between registers.
+template <class T>
+__device__ __forceinline__ void transpose_slab(uint32_t src, uint32_t dst, int lane)
+{
+    const uint32_t s0 = src + static_cast<uint32_t>(lane * 128);
+    const uint32_t d0 = dst + static_cast<uint32_t>(lane * 4);
+    const int sw = lane & 7;  // m & 7 of every row this lane takes
+#pragma unroll
+    for (int blk = 0; blk < T::BM / 32; ++blk) {
+        float4 v[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) v[t] = lds128(s0 + blk * 32 * 128 + ((t ^ sw) << 4));
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const uint32_t d = d0 + static_cast<uint32_t>((4 * t * T::BM + 32 * blk) * 4);
+            sts32(d, v[t].x);
+            sts32(d + T::BM * 4, v[t].y);
+            sts32(d + 2 * T::BM * 4, v[t].z);
+            sts32(d + 3 * T::BM * 4, v[t].w);
+        }
+    }
+}
+
+// The transposer warp (kASmemT): walks the CTA's k-slabs in the producer's
+// order; for each, waits for the stage to land and for a free M-major buffer,
+// transposes the A slab into it, then releases the stage's A (one arrival on
+// its empty barrier, beside the compute warps' ones for B) and marks the buffer
+// full. Bounded waits: on expiry it records the location and returns.
+template <class T>
+__device__ __forceinline__ void transposer_loop(const FfmaParams &p, uint32_t a_base, uint32_t x_base,
+                                                uint32_t bar_base, uint32_t xbar_base, volatile int *abort_flag,
+                                                int lane)
+{
+    int stage = 0, xs = 0;
+    uint32_t phase = 0, xphase = 0;
+    Work w;
+    for (int item = 0; work_at(p, item, w); ++item) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            const uint32_t full = bar_base + 8 * stage;
+            const uint32_t xempty = xbar_base + 8 * (T::XB + xs);
+            bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns) &&
+                      mbar_wait_bounded(xempty, xphase ^ 1u, abort_flag, p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag) {
+                    *abort_flag = 1;
+                    report_status(p.status, kTimeoutCode | kWhereTransposer);
+                }
+                return;
+            }
+            if (p.skew_ns > 0) __nanosleep(static_cast<unsigned>(p.skew_ns));
+            transpose_slab<T>(a_base + stage * T::A_BYTES, x_base + xs * T::A_BYTES, lane);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_base + 8 * (T::STAGES + stage));  // the stage's A has been read
+                mbar_arrive(xbar_base + 8 * xs);                  // the M-major slab is written
+            }
+            if (++stage == T::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++xs == T::XB) {
+                xs = 0;
+                xphase ^= 1u;
+            }
+        }
+    }
+}
+
 // The epilogue warps: for every work item of the CTA, warp e writes rows
 // [e BM / EPI, (e + 1) BM / EPI) of the staged tile (lane l: columns 4l..4l+3)
 // to its destination: C with alpha / beta (the C loads of 8 rows issued before
@@ -493,34 +592,45 @@ __device__ __forceinline__ void epilogue_warp_loop(const FfmaParams &p, uint32_t
     }
 }
 
-template <class T, bool AT>
+template <class T, int AL>
 __global__ void __launch_bounds__(T::THREADS, T::MINB)
 ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const FfmaParams p)
 {
+    constexpr bool AT = AL != kAKMajor;  // the compute warps read A M-major
+    static_assert((AL == kASmemT) == (T::XB > 0), "M-major A buffers exactly when A is transposed in shared memory");
+    constexpr int XW = T::XB > 0 ? 1 : 0;  // transposer warps
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const float *sA = reinterpret_cast<const float *>(smem);
     const float *sB = reinterpret_cast<const float *>(smem + T::STAGES * T::A_BYTES);
-    float *stg = reinterpret_cast<float *>(smem + T::STAGES * T::STAGE_BYTES);  // staging tile (EPI)
-    unsigned char *bar_ptr = smem + T::STAGES * T::STAGE_BYTES + T::STAGING_BYTES;
+    const float *sX = reinterpret_cast<const float *>(smem + T::STAGES * T::STAGE_BYTES);  // M-major A (XB)
+    float *stg = reinterpret_cast<float *>(smem + T::STAGES * T::STAGE_BYTES + T::XBUF_BYTES);  // staging tile (EPI)
+    unsigned char *bar_ptr = smem + T::STAGES * T::STAGE_BYTES + T::XBUF_BYTES + T::STAGING_BYTES;
     const uint32_t bar_base = smem_addr(bar_ptr);
     const uint32_t staged_bar = bar_base + 8 * (2 * T::STAGES);     // EPI: the consumers' arrivals
     const uint32_t freed_bar = bar_base + 8 * (2 * T::STAGES + 1);  // EPI: the epilogue warps' arrivals
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_ptr + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0)) * 8);
+    // XB: xfull[x] (the transposer's arrival), then xempty[x] (one arrival per consumer warp)
+    const uint32_t xbar_base = bar_base + 8 * (2 * T::STAGES + (T::EPI > 0 ? 2 : 0));
+    volatile int *abort_flag =
+        reinterpret_cast<volatile int *>(bar_ptr + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0) + 2 * T::XB) * 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::STAGES; ++s) {
-            mbar_init(bar_base + 8 * s, 1);                          // full: producer's arrive + bytes
-            mbar_init(bar_base + 8 * (T::STAGES + s), T::CONSUMERS); // empty: one arrive per consumer warp
+            mbar_init(bar_base + 8 * s, 1);                                 // full: producer's arrive + bytes
+            mbar_init(bar_base + 8 * (T::STAGES + s), T::CONSUMERS + XW);  // empty: consumers (+ transposer)
         }
         if (T::EPI) {
             mbar_init(staged_bar, T::CONSUMERS);
             mbar_init(freed_bar, T::EPI);
+        }
+        for (int x = 0; x < T::XB; ++x) {
+            mbar_init(xbar_base + 8 * x, 1);
+            mbar_init(xbar_base + 8 * (T::XB + x), T::CONSUMERS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -533,12 +643,19 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == T::CONSUMERS) {
         if (lane == 0)
-            producer_loop<T, AT>(&tmA, &tmB, p, smem_addr(sA), smem_addr(sB), bar_base, abort_flag);
+            producer_loop<T, AL>(&tmA, &tmB, p, smem_addr(sA), smem_addr(sB), bar_base, abort_flag);
         return;
     }
+    if constexpr (T::XB > 0) {
+        if (warp == T::CONSUMERS + 1) {
+            transposer_loop<T>(p, smem_addr(sA), smem_addr(sX), bar_base, xbar_base, abort_flag, lane);
+            return;
+        }
+    }
     if constexpr (T::EPI > 0) {
-        if (warp > T::CONSUMERS) {
-            epilogue_warp_loop<T>(p, smem_addr(stg), staged_bar, freed_bar, abort_flag, warp - T::CONSUMERS - 1, lane);
+        if (warp > T::CONSUMERS + XW) {
+            epilogue_warp_loop<T>(p, smem_addr(stg), staged_bar, freed_bar, abort_flag, warp - T::CONSUMERS - 1 - XW,
+                                  lane);
             return;
         }
     }
@@ -547,11 +664,14 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int wn = warp / T::WARPS_M;
     const int r = lane >> 3;  // row group: rows wm*32 + out_row(r, i)
     const int c = lane & 7;   // column group: columns wn*64 + 4c + {0..3} and + 32
-    const float *a_base = AT ? sA + wm * T::WM + 4 * r : sA + (wm * T::WM + r) * T::BK;
+    // A slab of the current k-block: ring stage (kAKMajor, kAMMajor) or M-major buffer (kASmemT)
+    const float *a_base = AL == kASmemT ? sX + wm * T::WM + 4 * r
+                          : AT          ? sA + wm * T::WM + 4 * r
+                                        : sA + (wm * T::WM + r) * T::BK;
     const float *b_cols_base = sB + wn * T::WN + c * 4;
 
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, xs = 0;
+    uint32_t phase = 0, xphase = 0;
     for (int item = 0;; ++item) {
         int kb0, kb1;
         {
@@ -570,6 +690,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         for (int kb = kb0; kb < kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns);
+            if constexpr (AL == kASmemT) ok = ok && mbar_wait_bounded(xbar_base + 8 * xs, xphase, abort_flag, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0 && !*abort_flag) {
@@ -578,17 +699,28 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 return;
             }
-            if constexpr (AT)
+            if constexpr (AL == kASmemT)
+                compute_slab_mmajor<T>(a_base + xs * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), acc);
+            else if constexpr (AT)
                 compute_slab_mmajor<T>(a_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), acc);
             else
                 compute_slab_kmajor<T>(a_base + stage * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), r,
                                        acc);
             if (p.skew_ns < 0) __nanosleep(static_cast<unsigned>(-p.skew_ns));
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_base + 8 * (T::STAGES + stage));
+            if (lane == 0) {
+                mbar_arrive(bar_base + 8 * (T::STAGES + stage));
+                if constexpr (AL == kASmemT) mbar_arrive(xbar_base + 8 * (T::XB + xs));
+            }
             if (++stage == T::STAGES) {
                 stage = 0;
                 phase ^= 1u;
+            }
+            if constexpr (AL == kASmemT) {
+                if (++xs == T::XB) {
+                    xs = 0;
+                    xphase ^= 1u;
+                }
             }
         }
         if constexpr (T::EPI != 0) {
@@ -613,42 +745,53 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
-using Cfg0 = Tile<128, 128, 5, 1, 2>;
-using Cfg1 = Tile<128, 64, 4, 2>;
-using Cfg2 = Tile<64, 128, 4, 2>;
-using Cfg3 = Tile<64, 64, 4, 3>;
-
-template <class T>
-constexpr bool matches(int i)
-{
-    return sgemm_cfg::kFfmaConfigs[i].bm == T::BM && sgemm_cfg::kFfmaConfigs[i].bn == T::BN &&
-           sgemm_cfg::kFfmaConfigs[i].stages == T::STAGES && sgemm_cfg::kFfmaConfigs[i].ctas_per_sm == T::MINB &&
-           sgemm_cfg::kFfmaConfigs[i].threads == T::THREADS &&
-           sgemm_cfg::kFfmaConfigs[i].smem_bytes == T::SMEM_BYTES;
-}
+// Table row i in both ring forms: R (A staged for the compute warps) and X (A
+// transposed in shared memory by a transposer warp, fewer ring stages).
+template <int I>
+struct Row {
+    static constexpr sgemm_cfg::TileConfig c = sgemm_cfg::kFfmaConfigs[I];
+    using R = Tile<c.bm, c.bn, c.stages, c.ctas_per_sm, c.epilogue_warps>;
+    using X = Tile<c.bm, c.bn, c.xstages, c.ctas_per_sm, c.epilogue_warps, c.xbufs>;
+    static_assert(R::THREADS == c.threads && R::SMEM_BYTES == c.smem_bytes && X::THREADS == c.xthreads &&
+                      X::SMEM_BYTES == c.xsmem_bytes,
+                  "kernel instantiations must match the tile-config table");
+};
 static_assert(sgemm_cfg::kNumFfmaConfigs == 4, "one instantiation per table row");
-static_assert(matches<Cfg0>(0) && matches<Cfg1>(1) && matches<Cfg2>(2) && matches<Cfg3>(3),
-              "kernel instantiations must match the tile-config table");
 
-template <class T>
+template <int I>
 cudaError_t set_attr()
 {
-    cudaError_t e = cudaFuncSetAttribute(ffma_sgemm_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(ffma_sgemm_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                T::SMEM_BYTES);
+    using R = typename Row<I>::R;
+    using X = typename Row<I>::X;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(ffma_sgemm_kernel<R, kAMMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  R::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(ffma_sgemm_kernel<R, kAKMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  R::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(ffma_sgemm_kernel<X, kASmemT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                X::SMEM_BYTES);
 }
 
-template <class T>
-cudaError_t launch(bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
+template <int I>
+cudaError_t launch(int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
                    cudaStream_t stream, bool dependent)
 {
-    if (a_mmajor)
-        return launch_kernel(dependent, ffma_sgemm_kernel<T, true>, dim3(grid), dim3(T::THREADS), T::SMEM_BYTES,
+    using R = typename Row<I>::R;
+    using X = typename Row<I>::X;
+    switch (a_layout) {
+    case kAMMajor:
+        return launch_kernel(dependent, ffma_sgemm_kernel<R, kAMMajor>, dim3(grid), dim3(R::THREADS), R::SMEM_BYTES,
                              stream, tmA, tmB, p);
-    return launch_kernel(dependent, ffma_sgemm_kernel<T, false>, dim3(grid), dim3(T::THREADS), T::SMEM_BYTES, stream,
-                         tmA, tmB, p);
+    case kAKMajor:
+        return launch_kernel(dependent, ffma_sgemm_kernel<R, kAKMajor>, dim3(grid), dim3(R::THREADS), R::SMEM_BYTES,
+                             stream, tmA, tmB, p);
+    case kASmemT:
+        return launch_kernel(dependent, ffma_sgemm_kernel<X, kASmemT>, dim3(grid), dim3(X::THREADS), X::SMEM_BYTES,
+                             stream, tmA, tmB, p);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -894,20 +1037,20 @@ int elementwise_grid(long long work, int threads, int num_sms)
 cudaError_t ffma_set_attributes()
 {
     cudaError_t e;
-    if ((e = set_attr<Cfg0>()) != cudaSuccess) return e;
-    if ((e = set_attr<Cfg1>()) != cudaSuccess) return e;
-    if ((e = set_attr<Cfg2>()) != cudaSuccess) return e;
-    return set_attr<Cfg3>();
+    if ((e = set_attr<0>()) != cudaSuccess) return e;
+    if ((e = set_attr<1>()) != cudaSuccess) return e;
+    if ((e = set_attr<2>()) != cudaSuccess) return e;
+    return set_attr<3>();
 }
 
-cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB,
+cudaError_t launch_ffma(int config, int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const FfmaParams &p, int grid, cudaStream_t stream, bool dependent)
 {
     switch (config) {
-    case 0: return launch<Cfg0>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
-    case 1: return launch<Cfg1>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
-    case 2: return launch<Cfg2>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
-    case 3: return launch<Cfg3>(a_mmajor, tmA, tmB, p, grid, stream, dependent);
+    case 0: return launch<0>(a_layout, tmA, tmB, p, grid, stream, dependent);
+    case 1: return launch<1>(a_layout, tmA, tmB, p, grid, stream, dependent);
+    case 2: return launch<2>(a_layout, tmA, tmB, p, grid, stream, dependent);
+    case 3: return launch<3>(a_layout, tmA, tmB, p, grid, stream, dependent);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -325,21 +325,28 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         }
     }
 
-    // A^T: the mainloop's FFMA2 form with A pairs along M runs ~10 % faster;
-    // transposing A costs one read and one write of A.
+    // A layout. The mainloop's FFMA2 form with A pairs along M runs ~10 % faster
+    // than the one A as given allows; it needs A M-major, either transposed in
+    // global memory first (one read and one write of A) or turned M-major slab by
+    // slab in shared memory by a transposer warp (no copy; a shorter ring).
     if (ov.force_transpose_a >= 0) {
         out->transpose_a = ov.force_transpose_a;
     } else {
         const bool beta_read = q.beta != 0.0f;
         const double t_main = out->sk_tiles > 0 ? model_time_sk(c, q.M, q.N, q.K, q.num_sms, beta_read)
                                                 : model_time(c, q.M, q.N, q.K, S, q.num_sms, beta_read);
-        out->transpose_a = transpose_pays(q, t_main) ? 1 : 0;
+        out->transpose_a = transpose_pays(q, t_main) ? 1 : 2;
     }
-    if (out->transpose_a) out->repack_a = 0;  // the transposed copy is aligned whatever A was
+    if (out->transpose_a == 1) out->repack_a = 0;  // the transposed copy is aligned whatever A was
+    if (out->transpose_a == 2) {
+        out->stages = c.xstages;
+        out->threads = c.xthreads;
+    }
 
     const Workspace w = workspace_layout(q, *out);
     out->workspace_bytes = w.total;
-    out->launches = 1 + out->transpose_a + out->repack_a + out->repack_b + (S > 1 || out->sk_tiles > 0 ? 1 : 0);
+    out->launches = 1 + (out->transpose_a == 1 ? 1 : 0) + out->repack_a + out->repack_b +
+                    (S > 1 || out->sk_tiles > 0 ? 1 : 0);
     return SGEMM_OK;
 }
 
@@ -347,7 +354,7 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p)
 {
     Workspace w{};
     long long off = 0;
-    if (p.transpose_a) {
+    if (p.transpose_a == 1) {
         w.lda = round_up(q.M, 4);
         w.a_off = off;
         off += round_up(static_cast<long long>(q.K) * w.lda * 4, 256);

@@ -23,7 +23,8 @@ struct Problem {
 struct Overrides {
     int force_config = -1;  // table row, -1 automatic
     int force_splits = 0;   // 0 automatic
-    int force_transpose_a = -1;  // -1 automatic, 0 never, 1 always (FFMA kernel)
+    int force_transpose_a = -1;  // FFMA kernel, A layout: -1 automatic, 0 as given, 1 transposed in
+                                 // global memory first, 2 transposed in shared memory
     int force_streamk = -1;      // -1 automatic, 0 never, 1 whenever the last round is partial
     int force_tf32_kernel = -1;  // -1 automatic, 0 one CTA per tile, 1 CTA pairs
     int force_repack_c = -1;     // TF32, C not 16-byte accessible: -1 automatic, 0 in place, 1 aligned copy

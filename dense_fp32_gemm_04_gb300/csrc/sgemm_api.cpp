@@ -331,10 +331,10 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
 
     Workspace w = workspace_layout(q, plan);
     rc = ensure_workspace(h, static_cast<size_t>(w.total), stream);
-    if (rc == SGEMM_ERR_ALLOC && plan.transpose_a && h->ov.force_transpose_a < 0) {
-        // No room for A^T (a very large A): read A as given instead, same results.
+    if (rc == SGEMM_ERR_ALLOC && plan.transpose_a == 1 && h->ov.force_transpose_a < 0) {
+        // No room for A^T (a very large A): transpose A in shared memory instead, same results.
         Overrides ov = h->ov;
-        ov.force_transpose_a = 0;
+        ov.force_transpose_a = 2;
         if ((rc = make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
         w = workspace_layout(q, plan);
         rc = ensure_workspace(h, static_cast<size_t>(w.total), stream);
@@ -349,7 +349,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     const float *b_src = B;
     long long b_ld = ldb;
     if (plan.kernel == SGEMM_KERNEL_TF32) return run_tf32(h, plan, w, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
-    if (plan.transpose_a) {
+    if (plan.transpose_a == 1) {
         float *dst = reinterpret_cast<float *>(ws + w.a_off);
         if (launch_transpose(A, lda, dst, w.lda, M, K, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_src = dst;
@@ -368,9 +368,9 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     }
 
     CUtensorMap tmA, tmB;
-    if (plan.transpose_a)  // A^T: K rows of M, boxes of 32 k x BM m
+    if (plan.transpose_a == 1)  // A^T: K rows of M, boxes of 32 k x BM m
         rc = make_tmap(h, &tmA, a_src, M, K, a_ld, plan.bm, sgemm_cfg::kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE);
-    else  // A: M rows of K, boxes of BM m x 32 k, 128-byte swizzle
+    else  // A (as given, or turned M-major in shared memory): M rows of K, boxes of BM m x 32 k, 128-byte swizzle
         rc = make_tmap(h, &tmA, a_src, K, M, a_ld, sgemm_cfg::kFfmaBK, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != SGEMM_OK) return rc;
     if ((rc = make_tmap(h, &tmB, b_src, N, K, b_ld, plan.bn, sgemm_cfg::kFfmaBK, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
@@ -404,8 +404,8 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         p.sk_grid = plan.sk_grid;
     }
     // Right after this call's transpose / repack: launched as its programmatic dependent.
-    const bool after_copy = plan.transpose_a || plan.repack_a || plan.repack_b;
-    if (launch_ffma(plan.config, plan.transpose_a != 0, tmA, tmB, p, plan.grid, stream, after_copy) != cudaSuccess)
+    const bool after_copy = plan.transpose_a == 1 || plan.repack_a || plan.repack_b;
+    if (launch_ffma(plan.config, plan.transpose_a, tmA, tmB, p, plan.grid, stream, after_copy) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.sk_tiles > 0 && launch_sk_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
@@ -496,7 +496,7 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
     }
     if (const char *ft = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
         const long v = std::strtol(ft, nullptr, 10);
-        if (v >= -1 && v <= 1) h->ov.force_transpose_a = static_cast<int>(v);
+        if (v >= -1 && v <= 2) h->ov.force_transpose_a = static_cast<int>(v);
     }
     if (const char *fk = std::getenv("SGEMM_FORCE_STREAMK")) {
         const long v = std::strtol(fk, nullptr, 10);
@@ -715,7 +715,7 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
         h->skew_ns = static_cast<int>(value);
         return SGEMM_OK;
     case SGEMM_OPT_FORCE_TRANSPOSE_A:
-        if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
+        if (value < -1 || value > 2) return SGEMM_ERR_INVALID_VALUE;
         h->ov.force_transpose_a = static_cast<int>(value);
         return SGEMM_OK;
     case SGEMM_OPT_FORCE_STREAMK:

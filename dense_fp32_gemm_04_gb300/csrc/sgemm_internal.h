@@ -24,7 +24,9 @@ enum : int {
     kWhereAccum = 5,         // TF32: the epilogue's wait for the accumulator ran out
     // 6: not used (TMEM allocation blocks until it succeeds; it reports nothing)
     kWherePairLayout = 7,    // TF32 pair: the two CTAs' shared-memory layouts differ (no work done)
-    kWhereStaging = 8        // FFMA: a wait on the epilogue's staging tile ran out
+    kWhereStaging = 8,       // FFMA: a wait on the epilogue's staging tile ran out
+    kWhereTransposer = 9     // FFMA, A transposed in shared memory: the transposer warp's wait for a
+                             // filled stage or a free M-major buffer ran out
 };
 
 // Everything the FFMA mainloop needs besides the two tensor maps.
@@ -79,10 +81,12 @@ struct Tf32Params {
 // Plain-launch helpers implemented in the .cu files. All return the CUDA
 // error of the launch (cudaSuccess when it was enqueued).
 cudaError_t ffma_set_attributes();  // opt in to large dynamic shared memory (current device)
-// a_mmajor: tmA maps A^T (K rows of M, M contiguous) instead of A (M rows of K).
+// a_layout (plan.transpose_a): 0 = tmA maps A (M rows of K) and the mainloop reads
+// it K-major; 1 = tmA maps A^T (K rows of M, M contiguous); 2 = tmA maps A as for
+// 0 and a transposer warp turns each staged slab M-major in shared memory.
 // dependent: launched as a programmatic dependent of the call's previous kernel
 // (transpose / repack), whose completion its copy issue waits for.
-cudaError_t launch_ffma(int config, bool a_mmajor, const CUtensorMap &tmA, const CUtensorMap &tmB,
+cudaError_t launch_ffma(int config, int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const FfmaParams &p, int grid, cudaStream_t stream, bool dependent);
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
                                  int M, int N, float alpha, float beta, float *C, long long ldc,

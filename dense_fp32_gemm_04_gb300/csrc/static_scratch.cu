@@ -220,7 +220,7 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
     p.status = status;
     p.timeout_ns = kTimeoutNs;
     p.inject_skip = -1;
-    if (sgemm_impl::launch_ffma(plan.config, false, tmA, tmB, p, plan.grid, st, false) != cudaSuccess)
+    if (sgemm_impl::launch_ffma(plan.config, plan.transpose_a, tmA, tmB, p, plan.grid, st, false) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1 &&
         sgemm_impl::launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,

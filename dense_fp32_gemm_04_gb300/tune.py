@@ -6,8 +6,8 @@ For each shape it times the library's automatic plan and every forced
 (config, splits) combination with CUDA events (operands uniform[-1,1), alpha=1,
 beta=0, packed unless the shape says otherwise) and prints one line per shape:
 the automatic plan's time, the best forced combination and the ratio. It also
-times the automatic plan with A read as given and with A transposed first
-(``--layout-only``: only that). The planner's cost model, table and
+times the automatic plan with A read as given, transposed first and transposed
+in shared memory (``--layout-only``: only that). The planner's cost model, table and
 transposition rule are checked against this sweep.
 """
 
@@ -44,10 +44,14 @@ def time_call(torch, fn, budget_flops, flops):
     return e0.elapsed_time(e1) / n
 
 
+LAYOUTS = {0: "as given", 1: "transposed first", 2: "transposed in shared memory"}
+
+
 def layouts(torch, sg, h, run, budget_flops, flops):
-    """Time of the automatic plan with A as given (0) and transposed first (1)."""
+    """Time of the automatic plan with each A layout: as given (0), transposed
+    first in global memory (1), transposed in shared memory (2)."""
     out = {}
-    for ta in (0, 1):
+    for ta in LAYOUTS:
         h.set_option(sg.OPT_FORCE_TRANSPOSE_A, ta)
         out[ta] = time_call(torch, run, budget_flops, flops)
     h.set_option(sg.OPT_FORCE_TRANSPOSE_A, -1)
@@ -71,13 +75,13 @@ def sweep(shapes, budget_flops=4e11, layout_only=False):
         auto_ms = time_call(torch, run, budget_flops, flops)
         auto = h.last_plan().as_dict()
         lay = layouts(torch, sg, h, run, budget_flops, flops)
-        lay_line = (f"A as given {lay[0]:8.3f} ms, transposed {lay[1]:8.3f} ms "
-                    f"(auto picks {'transposed' if auto['transpose_a'] else 'as given'})")
+        lay_line = (f"A as given {lay[0]:8.3f} ms, transposed first {lay[1]:8.3f} ms, in shared memory "
+                    f"{lay[2]:8.3f} ms (auto picks {LAYOUTS[auto['transpose_a']]})")
         if layout_only:
             print(f"{M:6d} {N:6d} {K:6d}  auto cfg {auto['config']} S {auto['splits']}: {auto_ms:8.3f} ms | {lay_line}",
                   flush=True)
             results.append({"shape": [M, N, K], "auto_ms": auto_ms, "auto_plan": auto, "a_as_given_ms": lay[0],
-                            "a_transposed_ms": lay[1]})
+                            "a_transposed_ms": lay[1], "a_smem_transposed_ms": lay[2]})
             continue
         rows = []
         for cfg in range(len(sg.configs())):
@@ -94,7 +98,7 @@ def sweep(shapes, budget_flops=4e11, layout_only=False):
         best = min(rows, key=lambda r: r["ms"])
         rec = {"shape": [M, N, K], "auto_ms": auto_ms, "auto_tflops": flops / auto_ms / 1e9, "auto_plan": auto,
                "best": best, "auto_over_best": auto_ms / best["ms"], "status": st, "forced": rows,
-               "a_as_given_ms": lay[0], "a_transposed_ms": lay[1]}
+               "a_as_given_ms": lay[0], "a_transposed_ms": lay[1], "a_smem_transposed_ms": lay[2]}
         results.append(rec)
         print(f"{M:6d} {N:6d} {K:6d}  auto cfg {auto['config']} S {auto['splits']} sk {auto['sk_tiles']}"
               f": {auto_ms:8.3f} ms {rec['auto_tflops']:6.2f} TFLOP/s | best cfg {best['config']} "
@@ -108,7 +112,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--out", default=None)
     ap.add_argument("--shapes", default="bench", choices=sorted(SHAPES))
-    ap.add_argument("--layout-only", action="store_true", help="time only the two A layouts of the automatic plan")
+    ap.add_argument("--layout-only", action="store_true", help="time only the three A layouts of the automatic plan")
     args = ap.parse_args(argv)
     res = sweep(SHAPES[args.shapes], layout_only=args.layout_only)
     if args.out:

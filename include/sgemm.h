@@ -94,8 +94,11 @@ typedef struct sgemm_plan_s {
     int math_mode;           /* sgemm_math_mode_t */
     int launches;            /* kernels one sgemm_run launches for this plan */
     long long workspace_bytes; /* device workspace the handle holds for it */
-    int transpose_a;         /* 1: A is first transposed into the workspace (K x M, M contiguous)
-                                and the FP32 mainloop reads A^T; 0: it reads A as given */
+    int transpose_a;         /* FP32 mainloop's A layout: 1 = A is first transposed into the
+                                workspace (K x M, M contiguous) and the mainloop reads A^T;
+                                2 = A is staged as given and a transposer warp turns each slab
+                                M-major in shared memory (no copy; stages/threads then describe
+                                that form: a shorter ring, one more warp); 0 = A is read as given */
     int sk_tiles;            /* stream-K (both modes): the last sk_tiles tiles (after `units`
                                 whole tiles) form one span of k-blocks cut evenly over the grid's
                                 CTAs; tiles shared by two or more CTAs are reduced in k order
@@ -120,7 +123,8 @@ typedef enum sgemm_option {
                                      issue by this many ns per k-slab, < 0 delays every compute warp
                                      before it releases a slab; |value| <= 100000, 0 = off */
     SGEMM_OPT_FORCE_TRANSPOSE_A = 7,/* FP32 path: -1 = automatic (the default), 0 = read A as given,
-                                     1 = always transpose A first (same results either way) */
+                                     1 = always transpose A first in global memory, 2 = always
+                                     transpose A in shared memory (same results every way) */
     SGEMM_OPT_FORCE_STREAMK = 8,  /* -1 = automatic (the default), 0 = never, 1 = whenever the last
                                      round of tiles is partial (ignored with forced splits) */
     SGEMM_OPT_FORCE_TF32_KERNEL = 9, /* TF32 mode: -1 = automatic (the default), 0 = one CTA per
@@ -143,7 +147,7 @@ typedef enum sgemm_option {
  * sgemm_run_host, device staging buffers.
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
- * SGEMM_FORCE_SPLITS=<S>, SGEMM_FORCE_TRANSPOSE_A=<-1|0|1>,
+ * SGEMM_FORCE_SPLITS=<S>, SGEMM_FORCE_TRANSPOSE_A=<-1|0|1|2>,
  * SGEMM_FORCE_STREAMK=<-1|0|1> and SGEMM_FORCE_TF32_KERNEL=<-1|0|1> preset the
  * planner overrides of sgemm_set_option.
  */
@@ -272,7 +276,8 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value);
  * stage, 2 the copy warp's wait for a free stage, 3 the wait for a CTA's own
  * copies and MMAs in flight at its end, 4 the TF32 MMA issuer's wait for a
  * filled stage, 5 a wait on a TF32 accumulator, 7 the TF32 pair layout check,
- * 8 a wait on the FP32 epilogue's staging tile (6 is not used). Returns that
+ * 8 a wait on the FP32 epilogue's staging tile, 9 the FP32 transposer
+ * warp's wait for a filled stage or a free M-major A buffer (6 is not used). Returns that
  * sgemm_status value, or SGEMM_ERR_CUDA if synchronizing failed (e.g. a sticky
  * device error).
  */

@@ -123,14 +123,16 @@ def test_plan_ragged_unaligned_repacks(lib):
     assert p.transpose_a == 1 and p.repack_a == 0 and p.repack_b == 1 and p.vec_c == 0
     assert p.launches == 3 + (1 if (p.splits > 1 or p.sk_tiles > 0) else 0)
     assert p.workspace_bytes >= 4 * (1531 * 2048 + 1531 * 3004)
-    # Without the transposition (small N) an unaligned A is repacked instead.
+    # Without the global transposition (small N) an unaligned A is repacked and then
+    # transposed slab by slab in shared memory.
     q = sg.plan(20000, 16, 1531, lda=1531, ldb=16, ldc=16)
-    assert q.transpose_a == 0 and q.repack_a == 1 and q.repack_b == 0
+    assert q.transpose_a == 2 and q.repack_a == 1 and q.repack_b == 0
+    assert q.launches == 2 + (1 if (q.splits > 1 or q.sk_tiles > 0) else 0)
 
 
 def test_plan_misaligned_pointer_repacks(lib):
     p = sg.plan(512, 512, 512, align_flags=0b110)
-    assert p.transpose_a == 0 and p.repack_a == 1 and p.repack_b == 0
+    assert p.transpose_a == 2 and p.repack_a == 1 and p.repack_b == 0
 
 
 def test_plan_skinny_shares_k(lib):
@@ -145,8 +147,13 @@ def test_plan_skinny_shares_k(lib):
         else:
             assert p.splits > 1 and p.units >= 152, p.as_dict()
             assert p.workspace_bytes >= p.splits * M * N * 4
-        # transposing a 16384 x 8192 A costs more than it saves; a 64 x 8192 A is cheap
-        assert p.transpose_a == (1 if M == 64 else 0)
+        # transposing a 16384 x 8192 A in global memory costs more than it saves (it is
+        # transposed slab by slab in shared memory instead); a 64 x 8192 A is cheap
+        assert p.transpose_a == (1 if M == 64 else 2)
+        if p.transpose_a == 2:
+            # one more warp (the transposer) and a shorter ring beside the M-major A buffers
+            row = sg.configs()[p.config]
+            assert p.threads == row.threads + 32 and 2 <= p.stages < row.stages
 
 
 def test_config_table(lib):
@@ -156,6 +163,7 @@ def test_config_table(lib):
         assert r.bm % 32 == 0 and r.bn % 64 == 0 and r.bk == 32
         # warp tiles + the TMA producer warp (+ the 2 epilogue warps of the 128 x 128 row)
         assert r.threads == ((r.bm // 32) * (r.bn // 64) + 1 + (2 if (r.bm, r.bn) == (128, 128) else 0)) * 32
+
 
 
 def test_plan_invariants_random_shapes(lib):
@@ -190,14 +198,14 @@ def test_plan_invariants_random_shapes(lib):
             if p.splits > 1:
                 assert p.workspace_bytes >= p.splits * M * (-(-N // 4) * 4) * 4
         assert 1 <= p.grid <= (slots if p.sk_tiles else min(p.units, slots))
-        assert p.transpose_a in (0, 1)
-        assert p.repack_a == (0 if (p.transpose_a or (align & 1 and lda % 4 == 0)) else 1)
+        assert p.transpose_a in (1, 2)  # A as given (0) only when forced
+        assert p.repack_a == (0 if (p.transpose_a == 1 or (align & 1 and lda % 4 == 0)) else 1)
         assert p.repack_b == (0 if (align & 2 and ldb % 4 == 0) else 1)
         assert p.vec_c == (1 if (align & 4 and ldc % 4 == 0) else 0)
-        if p.transpose_a:
+        if p.transpose_a == 1:
             assert p.workspace_bytes >= K * (-(-M // 4) * 4) * 4
         extra = 1 if (p.splits > 1 or p.sk_tiles > 0) else 0
-        assert p.launches == 1 + p.transpose_a + p.repack_a + p.repack_b + extra
+        assert p.launches == 1 + (p.transpose_a == 1) + p.repack_a + p.repack_b + extra
 
 
 def test_tf32_plan(lib):

@@ -95,7 +95,8 @@ def test_deterministic_under_ties(h):
 
 
 @pytest.mark.parametrize("force", [dict(), dict(config=1, splits=3), dict(config=3, splits=1),
-                                   dict(config=0, splits=1, transpose_a=0), dict(config=2, splits=5, transpose_a=1)])
+                                   dict(config=0, splits=1, transpose_a=0), dict(config=2, splits=5, transpose_a=1),
+                                   dict(config=0, splits=1, transpose_a=2)])
 @pytest.mark.parametrize("shape", [(300, 200, 100), (1000, 2500, 513), (2047, 3001, 1531)])
 def test_every_plan(h, force, shape):
     """Whichever kernel writes the final C values (whole-tile epilogue with either A

@@ -51,10 +51,10 @@ def force(h, config=-1, splits=0, transpose_a=-1):
 
 @pytest.mark.parametrize("cfg", range(4))
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
-@pytest.mark.parametrize("ta", [0, 1])
+@pytest.mark.parametrize("ta", [0, 1, 2])
 def test_every_config_and_split(h, cfg, splits, ta):
-    """Each tile-config row, split factor and A layout (as given / transposed first),
-    around tile multiples, integer and real operands."""
+    """Each tile-config row, split factor and A layout (as given / transposed first /
+    transposed in shared memory), around tile multiples, integer and real operands."""
     force(h, cfg, splits, ta)
     try:
         for (M, N, K) in [(63, 65, 33), (129, 127, 95), (200, 300, 257), (256, 128, 224)]:
@@ -74,12 +74,12 @@ def test_every_config_and_split(h, cfg, splits, ta):
 
 @pytest.mark.parametrize("cfg", range(4))
 def test_a_layouts_give_identical_bits(h, cfg):
-    """Both A layouts evaluate every output as the same FMA chain in ascending k:
+    """The three A layouts evaluate every output as the same FMA chain in ascending k:
     the results must agree bit for bit (real operands, every split path)."""
     for (M, N, K), splits in [((300, 260, 777), 1), ((129, 200, 500), 3), ((1000, 2500, 513), 0)]:
         A, B, C = ops(M, N, K, seed=cfg + M, dist=("normal", "normal", "uniform"))
         outs = []
-        for ta in (0, 1):
+        for ta in (0, 1, 2):
             force(h, cfg, splits, ta)
             try:
                 got, guards, st = run_gemm(torch, h, A, B, C, 1.25, -0.5)
@@ -87,7 +87,8 @@ def test_a_layouts_give_identical_bits(h, cfg):
             finally:
                 force(h)
             outs.append(got)
-        assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32)), (cfg, M, N, K)
+        for o in outs[1:]:
+            assert np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)), (cfg, M, N, K)
         check_against_oracle(outs[1], A, B, C, 1.25, -0.5)
 
 
@@ -98,10 +99,11 @@ def test_deterministic(h):
     assert np.array_equal(r1.view(np.uint32), r2.view(np.uint32))
 
 
-@pytest.mark.parametrize("ta", [0, 1])
+@pytest.mark.parametrize("ta", [0, 1, 2])
 def test_leading_dimensions_and_misalignment(h, ta):
     """Padded leading dimensions keep pad columns untouched; misaligned pointers take
-    the repack path (A as given) or the transposition (A transposed first)."""
+    the repack path (A as given or transposed in shared memory) or the transposition
+    (A transposed first)."""
     M, N, K = 190, 170, 150
     A, B, C = ops(M, N, K, seed=77)
     force(h, transpose_a=ta)
@@ -116,7 +118,7 @@ def test_leading_dimensions_and_misalignment(h, ta):
         p = h.last_plan()
     finally:
         force(h)
-    assert p.transpose_a == ta and p.repack_a == 1 - ta and p.vec_c == 0
+    assert p.transpose_a == ta and p.repack_a == (0 if ta == 1 else 1) and p.vec_c == 0
 
 
 def test_quick_returns(h):
@@ -170,7 +172,8 @@ def test_option_values_are_checked(h):
     """Out-of-range option values and unknown options are refused and change nothing."""
     lib = sg.library()
     for opt, bad in ((sg.OPT_FORCE_TF32_KERNEL, 2), (sg.OPT_FORCE_REPACK_C, 2), (sg.OPT_FORCE_REPACK_C, -2),
-                     (sg.OPT_FORCE_STREAMK, 2), (sg.OPT_FORCE_TRANSPOSE_A, -2), (99, 0)):
+                     (sg.OPT_FORCE_STREAMK, 2), (sg.OPT_FORCE_TRANSPOSE_A, -2), (sg.OPT_FORCE_TRANSPOSE_A, 3),
+                     (99, 0)):
         assert lib.sgemm_set_option(h._h, opt, bad) == sg.SGEMM_ERR_INVALID_VALUE, (opt, bad)
     for opt in (sg.OPT_FORCE_TF32_KERNEL, sg.OPT_FORCE_REPACK_C, sg.OPT_FORCE_STREAMK, sg.OPT_FORCE_TRANSPOSE_A):
         assert lib.sgemm_set_option(h._h, opt, -1) == sg.SGEMM_OK
@@ -263,7 +266,7 @@ def test_skinny(h, name):
 
 @pytest.mark.parametrize("shape", [(1000, 2500, 513), (1999, 3001, 1031), (1500, 4095, 2050), (1024, 1024, 1024),
                                    (300, 260, 777), (129, 127, 95)])
-@pytest.mark.parametrize("ta", [0, 1])
+@pytest.mark.parametrize("ta", [0, 1, 2])
 def test_stream_k(h, shape, ta):
     """Stream-K: the tiles of the last, partial round share one span of k-blocks cut
     evenly over the CTAs (whole tiles before it; for small problems the span is all
@@ -359,7 +362,11 @@ def test_timing_skew_is_race_free(h, skew):
     cases = [((1999, 3001, 1031), dict()), ((700, 900, 1500), dict(config=1, splits=3, transpose_a=0)),
              ((700, 900, 1500), dict(config=1, splits=3, transpose_a=1)),
              ((300, 260, 777), dict(config=3, splits=1, transpose_a=0)),
-             ((300, 260, 777), dict(config=3, splits=1, transpose_a=1))]
+             ((300, 260, 777), dict(config=3, splits=1, transpose_a=1)),
+             ((1999, 3001, 1031), dict(config=0, splits=1, transpose_a=2)),
+             ((700, 900, 1500), dict(config=1, splits=3, transpose_a=2)),
+             ((300, 260, 777), dict(config=3, splits=1, transpose_a=2)),
+             ((333, 700, 900), dict(config=2, splits=2, transpose_a=2))]
     for (M, N, K), forced in cases:
         A, B, C = ops(M, N, K, seed=M + skew, dist=("normal", "uniform", "uniform"))
         force(h, **forced)

@@ -53,7 +53,7 @@ def _draw_case(rng):
         "config": int(rng.choice([-1, -1, 0, 0, 1, 2, 3])),
         "streamk": int(rng.choice([-1, -1, 0, 1])),
         "splits": int(rng.choice([0, 0, 0, 2, 3, 5, 8])),
-        "transpose_a": int(rng.choice([-1, -1, 0, 1])),
+        "transpose_a": int(rng.choice([-1, -1, 0, 1, 2])),
     }
     return M, N, K, pads, offsets, alpha, beta, dist, opts
 

@@ -17,7 +17,10 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def test_timeout_is_reported_and_gpu_recovers():
+@pytest.mark.parametrize("ta", [0, 1, 2])
+def test_timeout_is_reported_and_gpu_recovers(ta):
+    """Each A layout: with A transposed in shared memory the transposer warp waits
+    for the missing stage too, and whichever wait runs out first reports."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from dense_fp32_gemm_04_gb300 import _build
@@ -29,12 +32,14 @@ def test_timeout_is_reported_and_gpu_recovers():
         A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=2, dist=("int", "int", "int"))
         h.set_option(sg.OPT_FORCE_CONFIG, 0)
         h.set_option(sg.OPT_FORCE_SPLITS, 1)  # CTA 0 then walks all 16 k-blocks of its tile
+        h.set_option(sg.OPT_FORCE_TRANSPOSE_A, ta)
         h.set_option(sg.OPT_WAIT_TIMEOUT_NS, 50_000_000)  # 50 ms
         h.set_option(sg.OPT_INJECT_SKIP, 3)
         _, _, st = run_gemm(torch, h, A, B, C, 1.0, 1.0)
         assert st == sg.SGEMM_OK  # the launch itself is accepted
         status, code = h.check_device_status()
         assert status == sg.SGEMM_ERR_TIMEOUT and (code >> 16) == sg.SGEMM_ERR_TIMEOUT, hex(code)
+        assert h.last_plan().transpose_a == ta
         # the status word is cleared and the context is healthy
         h.set_option(sg.OPT_INJECT_SKIP, -1)
         h.set_option(sg.OPT_WAIT_TIMEOUT_NS, 4_000_000_000)
