@@ -43,6 +43,7 @@ OPT_FORCE_TRANSPOSE_A = 7
 OPT_FORCE_STREAMK = 8
 OPT_FORCE_TF32_KERNEL = 9
 OPT_FORCE_REPACK_C = 10
+OPT_CLUSTER_SPLIT = 11
 
 
 class Plan(ctypes.Structure):
@@ -52,7 +53,8 @@ class Plan(ctypes.Structure):
         "kernel", "config", "bm", "bn", "bk", "stages", "threads", "ctas_per_sm", "splits",
         "tiles_m", "tiles_n", "units", "grid", "repack_a", "repack_b", "vec_c", "math_mode",
         "launches")] + [("workspace_bytes", ctypes.c_longlong), ("transpose_a", ctypes.c_int),
-                        ("sk_tiles", ctypes.c_int), ("sk_grid", ctypes.c_int), ("repack_c", ctypes.c_int)]
+                        ("sk_tiles", ctypes.c_int), ("sk_grid", ctypes.c_int), ("repack_c", ctypes.c_int),
+                        ("cluster_split", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -2,8 +2,10 @@
 // loads, the global timer used by the kernels' bounded waits, programmatic
 // dependent launch, and the launch helper. Each wraps one PTX instruction (PTX
 // ISA, "Parallel Synchronization and Communication Instructions: mbarrier",
-// "Data Movement: cp.async.bulk.tensor", "griddepcontrol"). The tensor-core and
-// CTA-pair helpers are in tcgen05_ptx.cuh.
+// "Data Movement: cp.async.bulk.tensor", "griddepcontrol"), and the thread-block
+// cluster primitives (rank, mapa, distributed shared memory loads,
+// barrier.cluster). The tensor-core and CTA-pair (.cta_group::2) helpers are in
+// tcgen05_ptx.cuh.
 #pragma once
 
 #include <cstdint>
@@ -106,6 +108,89 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// Thread-block clusters (PTX ISA "Cluster of Cooperative Thread Arrays",
+// mapa, ld.shared::cluster, barrier.cluster): used by the TF32 CTA-pair kernel
+// and by the FFMA kernel's split-K reduced within a cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// CTAs in this CTA's cluster (1 when the kernel was not launched with clusters).
+__device__ __forceinline__ uint32_t cluster_size()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the variable at shared::cta address `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// 32-bit load from the shared memory of a CTA of the cluster.
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Every thread of every CTA of the cluster (warp-aligned): release this thread's
+// earlier memory operations, acquire the others'.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 128-bit load from the shared memory of a CTA of the cluster.
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a
+// multiple of 32, whole warps): returns whether any participating thread
+// passed pred = true.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // Record the first error of a launch in the handle's device status word.

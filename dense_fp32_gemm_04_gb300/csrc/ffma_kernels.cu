@@ -69,7 +69,8 @@ namespace {
 using namespace sgemm_dev;
 using sgemm_cfg::kFfmaBK;
 
-constexpr int kTimeoutCode = 5 << 16;  // SGEMM_ERR_TIMEOUT << 16
+constexpr int kTimeoutCode = 5 << 16;       // SGEMM_ERR_TIMEOUT << 16
+constexpr int kNotSupportedCode = 7 << 16;  // SGEMM_ERR_NOT_SUPPORTED << 16
 
 // Where the mainloop's A operand comes from (plan.transpose_a):
 //  kAKMajor  A as given, staged K-major (128-byte swizzle), FFMA2 form (a_m, a_m) * (b_n, b_n+1);
@@ -592,6 +593,72 @@ __device__ __forceinline__ void epilogue_warp_loop(const FfmaParams &p, uint32_t
     }
 }
 
+// Split-K reduced within a thread-block cluster (p.cluster_split = S > 0): the
+// cluster's S CTAs hold the S K slices of one tile (rank = slice). Each stages
+// its raw partial tile in its own shared memory (the staging tile, or the
+// drained stage ring on rows without one), then, after a cluster barrier, adds
+// 1/S of the tile's elements over all S partials in slice order 0..S-1 through
+// distributed shared memory and writes them to C with alpha / beta: the same
+// additions, in the same order, as splitk_reduce_kernel does from a workspace,
+// so the bits match the split-K path, without the workspace round trip or a
+// second launch. A second cluster barrier keeps every CTA (and its shared
+// memory) alive until its peers have read it. Run by the compute warps only
+// (threads 0 .. CONSUMERS * 32 - 1); the other warps have exited, and exited
+// threads do not take part in cluster barriers. `staged_ok` is false after a
+// bounded wait ran out: the CTA then still meets both barriers (its peers would
+// otherwise read the shared memory of an exited CTA) but writes nothing.
+template <class T, bool AT>
+__device__ __forceinline__ void cluster_split_epilogue(const FfmaParams &p, const Acc<AT> &acc, float *stg,
+                                                       uint32_t layout_word, uint32_t layout, int wm, int wn, int r,
+                                                       int c, bool staged_ok)
+{
+    constexpr int kThreads = T::CONSUMERS * 32;
+    // every compute warp is done with the ring (its memory may hold the staged tile)
+    named_barrier_or(1, kThreads, false);
+    if (staged_ok) stage_tile<T, AT>(stg, acc, wm, wn, r, c);
+    cluster_sync();
+    const int S = p.cluster_split;
+    // The partials are read at this CTA's own staging offset in every peer: all
+    // CTAs of the launch must have laid out their shared memory alike.
+    const int t = static_cast<int>(threadIdx.x);
+    bool mismatch = false;
+    // compared on the offset inside the CTA's shared memory (higher bits of a
+    // shared::cta address differ between the CTAs of a cluster)
+    constexpr uint32_t kOffsetMask = 0x3FFFFu;
+    if (t < S)
+        mismatch = ((ld_shared_cluster_u32(mapa_shared(layout_word, static_cast<uint32_t>(t))) ^ layout) & kOffsetMask) != 0;
+    mismatch = named_barrier_or(1, kThreads, mismatch);
+    if (mismatch && t == 0) report_status(p.status, kNotSupportedCode | kWhereClusterShape);
+    if (staged_ok && !mismatch) {
+        Work w;
+        work_at(p, 0, w);
+        const int rank = static_cast<int>(cluster_ctarank());
+        constexpr int Q = T::BM * T::BN / 4;  // 16-byte groups of the tile-packed partial
+        const int q1 = (rank + 1) * Q / S;
+        const uint32_t base = smem_addr(stg);
+        for (int q = rank * Q / S + t; q < q1; q += kThreads) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < S) v[j] = ld_shared_cluster_v4(mapa_shared(base + static_cast<uint32_t>(q) * 16u, j));
+            float4 sum = v[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) {
+                if (j < S) {
+                    sum.x += v[j].x;
+                    sum.y += v[j].y;
+                    sum.z += v[j].z;
+                    sum.w += v[j].w;
+                }
+            }
+            const int lr = (4 * q) / T::BN, lc = (4 * q) % T::BN;
+            const int row = w.tm * T::BM + lr, col = w.tn * T::BN + lc;
+            if (row < p.M && col < p.N) store_c4(p, row, col, sum);
+        }
+    }
+    cluster_sync();
+}
+
 template <class T, int AL>
 __global__ void __launch_bounds__(T::THREADS, T::MINB)
 ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -616,10 +683,27 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     volatile int *abort_flag =
         reinterpret_cast<volatile int *>(bar_ptr + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0) + 2 * T::XB) * 8);
 
+    // split-K within clusters: the partial tile is staged in the staging tile, or
+    // in the drained ring on rows without one; its offset goes into the layout
+    // word beside the abort flag, which the cluster's CTAs compare
+    float *cs_stage = T::EPI > 0 ? stg : reinterpret_cast<float *>(smem);
+    static_assert(T::EPI > 0 || T::BM * T::BN * 4 <= T::STAGES * T::STAGE_BYTES, "a partial tile fits in the ring");
+    const uint32_t layout_word = smem_addr(bar_ptr) + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0) + 2 * T::XB) * 8 + 4;
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    if (p.cluster_split > 0 && (cluster_size() != static_cast<uint32_t>(p.cluster_split) || p.splits != p.cluster_split ||
+                                p.units != static_cast<int>(gridDim.x) || p.sk_tiles != 0)) {
+        // not launched as the plan's clusters of one unit per CTA: do nothing (before any barrier or copy)
+        if (threadIdx.x == 0) report_status(p.status, kNotSupportedCode | kWhereClusterShape);
+        return;
+    }
+
     if (threadIdx.x == 0) {
+        if (p.cluster_split > 0)
+            *reinterpret_cast<volatile uint32_t *>(bar_ptr + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0) + 2 * T::XB) * 8 +
+                                                   4) = smem_addr(cs_stage);
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(bar_base + 8 * s, 1);                                 // full: producer's arrive + bytes
             mbar_init(bar_base + 8 * (T::STAGES + s), T::CONSUMERS + XW);  // empty: consumers (+ transposer)
@@ -654,8 +738,10 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
     if constexpr (T::EPI > 0) {
         if (warp > T::CONSUMERS + XW) {
-            epilogue_warp_loop<T>(p, smem_addr(stg), staged_bar, freed_bar, abort_flag, warp - T::CONSUMERS - 1 - XW,
-                                  lane);
+            // (split-K within clusters: the compute warps write C themselves)
+            if (p.cluster_split == 0)
+                epilogue_warp_loop<T>(p, smem_addr(stg), staged_bar, freed_bar, abort_flag,
+                                      warp - T::CONSUMERS - 1 - XW, lane);
             return;
         }
     }
@@ -687,6 +773,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 32 / kRows; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
+        bool failed = false;
         for (int kb = kb0; kb < kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns);
@@ -696,6 +783,10 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (lane == 0 && !*abort_flag) {
                     *abort_flag = 1;
                     report_status(p.status, kTimeoutCode | kWhereConsumerFull);
+                }
+                if (p.cluster_split > 0) {  // still meet the cluster's barriers
+                    failed = true;
+                    break;
                 }
                 return;
             }
@@ -722,6 +813,10 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     xphase ^= 1u;
                 }
             }
+        }
+        if (p.cluster_split > 0) {  // one unit per CTA
+            cluster_split_epilogue<T, AT>(p, acc, cs_stage, layout_word, smem_addr(cs_stage), wm, wn, r, c, !failed);
+            return;
         }
         if constexpr (T::EPI != 0) {
             // wait until the epilogue warp has read the previous tile out of the staging tile
@@ -774,22 +869,25 @@ cudaError_t set_attr()
                                 X::SMEM_BYTES);
 }
 
+// Split-K within clusters launches clusters of p.cluster_split CTAs along x.
 template <int I>
 cudaError_t launch(int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
                    cudaStream_t stream, bool dependent)
 {
     using R = typename Row<I>::R;
     using X = typename Row<I>::X;
+    const int cl = p.cluster_split > 0 ? p.cluster_split : 1;
+    if (cl > 8 || grid % cl != 0) return cudaErrorInvalidValue;
     switch (a_layout) {
     case kAMMajor:
-        return launch_kernel(dependent, ffma_sgemm_kernel<R, kAMMajor>, dim3(grid), dim3(R::THREADS), R::SMEM_BYTES,
-                             stream, tmA, tmB, p);
+        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<R, kAMMajor>, dim3(grid), dim3(R::THREADS),
+                                     R::SMEM_BYTES, stream, tmA, tmB, p);
     case kAKMajor:
-        return launch_kernel(dependent, ffma_sgemm_kernel<R, kAKMajor>, dim3(grid), dim3(R::THREADS), R::SMEM_BYTES,
-                             stream, tmA, tmB, p);
+        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<R, kAKMajor>, dim3(grid), dim3(R::THREADS),
+                                     R::SMEM_BYTES, stream, tmA, tmB, p);
     case kASmemT:
-        return launch_kernel(dependent, ffma_sgemm_kernel<X, kASmemT>, dim3(grid), dim3(X::THREADS), X::SMEM_BYTES,
-                             stream, tmA, tmB, p);
+        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<X, kASmemT>, dim3(grid), dim3(X::THREADS),
+                                     X::SMEM_BYTES, stream, tmA, tmB, p);
     default: return cudaErrorInvalidValue;
     }
 }

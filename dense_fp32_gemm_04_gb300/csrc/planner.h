@@ -9,6 +9,7 @@
 namespace sgemm_impl {
 
 constexpr int kMaxSplits = 16;
+constexpr int kMaxClusterSplits = 8;  // portable cluster size
 
 struct Problem {
     int M, N, K;
@@ -28,6 +29,8 @@ struct Overrides {
     int force_streamk = -1;      // -1 automatic, 0 never, 1 whenever the last round is partial
     int force_tf32_kernel = -1;  // -1 automatic, 0 one CTA per tile, 1 CTA pairs
     int force_repack_c = -1;     // TF32, C not 16-byte accessible: -1 automatic, 0 in place, 1 aligned copy
+    int cluster_split = -1;      // FFMA split-K reduced within clusters: -1 automatic, 0 never,
+                                 // 1 whenever the plan has 2..kMaxClusterSplits splits (and no stream-K)
 };
 
 // Offsets (bytes) into the handle's workspace and the strides used there.
@@ -45,5 +48,6 @@ Workspace workspace_layout(const Problem &q, const sgemm_plan_t &p);
 void config_as_plan(int index, sgemm_plan_t *out);
 int choose_ffma(int M, int N, int K, int num_sms, bool beta_read, int force_config, int force_splits,
                 int *config, int *splits);
+
 
 }  // namespace sgemm_impl

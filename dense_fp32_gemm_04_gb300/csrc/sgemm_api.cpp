@@ -140,9 +140,10 @@ void log_plan(const sgemm_plan_t &p, int M, int N, int K)
 {
     std::fprintf(stderr,
                  "[sgemm] M=%d N=%d K=%d kernel=%d config=%d tile=%dx%dx%d stages=%d splits=%d units=%d grid=%d "
-                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld sk_tiles=%d\n",
+                 "repack=(%d,%d) transpose_a=%d vec_c=%d mode=%d launches=%d ws=%lld sk_tiles=%d cluster_split=%d\n",
                  M, N, K, p.kernel, p.config, p.bm, p.bn, p.bk, p.stages, p.splits, p.units, p.grid, p.repack_a,
-                 p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.sk_tiles);
+                 p.repack_b, p.transpose_a, p.vec_c, p.math_mode, p.launches, p.workspace_bytes, p.sk_tiles,
+                 p.cluster_split);
 }
 
 // TF32 tensor-core path: [repack A] [repack B] [copy C in] -> tcgen05 mainloop (one
@@ -385,7 +386,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     p.beta = beta;
     p.C = C;
     p.ldc = ldc;
-    p.W = plan.splits > 1 ? reinterpret_cast<float *>(ws + w.w_off) : nullptr;
+    p.W = plan.splits > 1 && !plan.cluster_split ? reinterpret_cast<float *>(ws + w.w_off) : nullptr;
     p.ldw = w.ldw;
     p.wstride = w.wstride;
     p.splits = plan.splits;
@@ -403,13 +404,14 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         p.sk_tiles = plan.sk_tiles;
         p.sk_grid = plan.sk_grid;
     }
+    p.cluster_split = plan.cluster_split ? plan.splits : 0;
     // Right after this call's transpose / repack: launched as its programmatic dependent.
     const bool after_copy = plan.transpose_a == 1 || plan.repack_a || plan.repack_b;
     if (launch_ffma(plan.config, plan.transpose_a, tmA, tmB, p, plan.grid, stream, after_copy) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.sk_tiles > 0 && launch_sk_reduce(p, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
-    if (plan.splits > 1) {
+    if (plan.splits > 1 && !plan.cluster_split) {
         if (launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
                                  h->num_sms, stream) != cudaSuccess)
             return SGEMM_ERR_LAUNCH;
@@ -497,6 +499,10 @@ int sgemm_create_for_device(int dev, sgemm_handle_t *out)
     if (const char *ft = std::getenv("SGEMM_FORCE_TRANSPOSE_A")) {
         const long v = std::strtol(ft, nullptr, 10);
         if (v >= -1 && v <= 2) h->ov.force_transpose_a = static_cast<int>(v);
+    }
+    if (const char *fc2 = std::getenv("SGEMM_CLUSTER_SPLIT")) {
+        const long v = std::strtol(fc2, nullptr, 10);
+        if (v >= -1 && v <= 1) h->ov.cluster_split = static_cast<int>(v);
     }
     if (const char *fk = std::getenv("SGEMM_FORCE_STREAMK")) {
         const long v = std::strtol(fk, nullptr, 10);
@@ -725,6 +731,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value)
     case SGEMM_OPT_FORCE_TF32_KERNEL:
         if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
         h->ov.force_tf32_kernel = static_cast<int>(value);
+        return SGEMM_OK;
+    case SGEMM_OPT_CLUSTER_SPLIT:
+        if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;
+        h->ov.cluster_split = static_cast<int>(value);
         return SGEMM_OK;
     case SGEMM_OPT_FORCE_REPACK_C:
         if (value < -1 || value > 1) return SGEMM_ERR_INVALID_VALUE;

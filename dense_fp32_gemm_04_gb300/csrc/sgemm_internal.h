@@ -25,8 +25,10 @@ enum : int {
     // 6: not used (TMEM allocation blocks until it succeeds; it reports nothing)
     kWherePairLayout = 7,    // TF32 pair: the two CTAs' shared-memory layouts differ (no work done)
     kWhereStaging = 8,       // FFMA: a wait on the epilogue's staging tile ran out
-    kWhereTransposer = 9     // FFMA, A transposed in shared memory: the transposer warp's wait for a
+    kWhereTransposer = 9,    // FFMA, A transposed in shared memory: the transposer warp's wait for a
                              // filled stage or a free M-major buffer ran out
+    kWhereClusterShape = 10  // FFMA split-K within clusters: the launch's cluster shape or the CTAs'
+                             // shared-memory layouts do not match the plan (nothing computed)
 };
 
 // Everything the FFMA mainloop needs besides the two tensor maps.
@@ -55,6 +57,10 @@ struct FfmaParams {
     // Test only (race detection): > 0 delays the producer by this many ns before
     // every fill, < 0 delays every consumer warp before it releases a slab.
     int skew_ns;
+    // > 0: split-K reduced within thread-block clusters of cluster_split CTAs
+    // (= splits; one (tile, slice) unit per CTA, cluster rank = slice): the
+    // partial tiles meet in distributed shared memory, W is not used.
+    int cluster_split;
 };
 
 // Everything the TF32 tcgen05 mainloops need besides the two tensor maps

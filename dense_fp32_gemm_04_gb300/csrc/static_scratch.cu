@@ -154,8 +154,9 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
 
     Overrides ov;
     ov.force_splits = splits;
-    ov.force_transpose_a = 0;  // the scratch array holds split-K partials only
+    ov.force_transpose_a = 2;  // A transposed in shared memory: the scratch array holds split-K partials only
     ov.force_streamk = 0;
+    ov.cluster_split = 0;  // partials in the static array, reduced by the reduction kernel
     sgemm_plan_t plan;
     if ((rc = sgemm_impl::make_plan(q, ov, &plan)) != SGEMM_OK) return rc;
     cudaStream_t st = stream;

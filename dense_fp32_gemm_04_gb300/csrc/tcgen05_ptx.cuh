@@ -132,57 +132,9 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn = fals
 // Cooperative Thread Arrays", and the .cta_group::2 forms of the tcgen05 and
 // TMA instructions). Rank 0 of the pair issues the MMAs for both CTAs.
 
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// CTAs in this CTA's cluster (1 when the kernel was not launched with clusters).
-__device__ __forceinline__ uint32_t cluster_size()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_count_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-
-// shared::cluster address of the variable at shared::cta address `addr` in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-// 32-bit load from the shared memory of a CTA of the cluster.
-__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
-
-// Every thread of every CTA of the cluster (warp-aligned): release this thread's
-// earlier memory operations, acquire the others'.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+// cluster_ctarank, cluster_size, mapa_shared, ld_shared_cluster_* and
+// cluster_sync are in device_ptx.cuh (the FFMA kernel's cluster split-K uses
+// them too).
 
 // Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)

@@ -108,6 +108,11 @@ typedef struct sgemm_plan_s {
     int repack_c;            /* TF32 mode, C not 16-byte accessible and SGEMM_OPT_FORCE_REPACK_C
                                 = 1: C is computed in an aligned workspace copy (filled from C
                                 when beta != 0) and copied back (0: C written in place) */
+    int cluster_split;       /* FP32 split-K (2 <= splits <= 8): 1 = the `splits` CTAs of a tile
+                                form one thread-block cluster and add their partial tiles in
+                                distributed shared memory (one CTA per (tile, slice), grid =
+                                units, no workspace and no reduction launch); 0 = partials go
+                                through the workspace to a reduction kernel */
 } sgemm_plan_t;
 
 /* Tuning and test options for sgemm_set_option. */
@@ -131,10 +136,14 @@ typedef enum sgemm_option {
                                      128 x 256 tile, 1 = a CTA pair (cluster of two, tcgen05
                                      .cta_group::2) per 256 x 256 tile; 1 fails with
                                      SGEMM_ERR_NOT_SUPPORTED where no pair fits */
-    SGEMM_OPT_FORCE_REPACK_C = 10 /* TF32 mode, C not 16-byte accessible: -1 = automatic (the
+    SGEMM_OPT_FORCE_REPACK_C = 10,/* TF32 mode, C not 16-byte accessible: -1 = automatic (the
                                      default) and 0 = write C in place (16-byte accesses inside
                                      each row, element by element at its ends); 1 = compute into
                                      an aligned workspace copy of C and copy it back */
+    SGEMM_OPT_CLUSTER_SPLIT = 11  /* FP32 split-K: -1 = automatic (the default), 0 = partials
+                                     always through the workspace and a reduction kernel, 1 =
+                                     always within thread-block clusters when 2..8 splits (same
+                                     results either way) */
 } sgemm_option_t;
 
 /*
@@ -148,7 +157,8 @@ typedef enum sgemm_option {
  * A handle must not be used by two host threads or two streams at once.
  * Environment: SGEMM_LOG=1 logs every plan; SGEMM_FORCE_CONFIG=<row> and
  * SGEMM_FORCE_SPLITS=<S>, SGEMM_FORCE_TRANSPOSE_A=<-1|0|1|2>,
- * SGEMM_FORCE_STREAMK=<-1|0|1> and SGEMM_FORCE_TF32_KERNEL=<-1|0|1> preset the
+ * SGEMM_FORCE_STREAMK=<-1|0|1>, SGEMM_FORCE_TF32_KERNEL=<-1|0|1> and
+ * SGEMM_CLUSTER_SPLIT=<-1|0|1> preset the
  * planner overrides of sgemm_set_option.
  */
 int sgemm_create(sgemm_handle_t *out);
@@ -277,7 +287,10 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value);
  * copies and MMAs in flight at its end, 4 the TF32 MMA issuer's wait for a
  * filled stage, 5 a wait on a TF32 accumulator, 7 the TF32 pair layout check,
  * 8 a wait on the FP32 epilogue's staging tile, 9 the FP32 transposer
- * warp's wait for a filled stage or a free M-major A buffer (6 is not used). Returns that
+ * warp's wait for a filled stage or a free M-major A buffer, 10 (with
+ * SGEMM_ERR_NOT_SUPPORTED) a split-K cluster launched in another shape than
+ * planned or with CTAs whose shared memory is laid out differently, in which
+ * case nothing is computed (6 is not used). Returns that
  * sgemm_status value, or SGEMM_ERR_CUDA if synchronizing failed (e.g. a sticky
  * device error).
  */

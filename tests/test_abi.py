@@ -195,16 +195,20 @@ def test_plan_invariants_random_shapes(lib):
             assert p.workspace_bytes >= 2 * p.grid * p.bm * p.bn * 4
         else:
             assert p.units == tiles * p.splits
-            if p.splits > 1:
+            if p.splits > 1 and not p.cluster_split:
                 assert p.workspace_bytes >= p.splits * M * (-(-N // 4) * 4) * 4
-        assert 1 <= p.grid <= (slots if p.sk_tiles else min(p.units, slots))
+        if p.cluster_split:
+            # split-K within clusters: one CTA per (tile, slice), no partials in the workspace
+            assert 2 <= p.splits <= 8 and p.sk_tiles == 0 and p.grid == p.units
+        else:
+            assert 1 <= p.grid <= (slots if p.sk_tiles else min(p.units, slots))
         assert p.transpose_a in (1, 2)  # A as given (0) only when forced
         assert p.repack_a == (0 if (p.transpose_a == 1 or (align & 1 and lda % 4 == 0)) else 1)
         assert p.repack_b == (0 if (align & 2 and ldb % 4 == 0) else 1)
         assert p.vec_c == (1 if (align & 4 and ldc % 4 == 0) else 0)
         if p.transpose_a == 1:
             assert p.workspace_bytes >= K * (-(-M // 4) * 4) * 4
-        extra = 1 if (p.splits > 1 or p.sk_tiles > 0) else 0
+        extra = 1 if ((p.splits > 1 and not p.cluster_split) or p.sk_tiles > 0) else 0
         assert p.launches == 1 + (p.transpose_a == 1) + p.repack_a + p.repack_b + extra
 
 
@@ -253,10 +257,23 @@ def test_plan_rows_follow_the_measured_epilogue_costs(lib):
     planner leaves the smallest problems to row 1 (measured on GB300: 256^3 12.3 us
     and 512^3 16.4 us on row 1 against 14.3 and 18.4 on row 0) and takes row 0 from
     1024^3 up (1024^3 50.2 us, ragged 2047 x 3001 x 1531 328 us against 349 on row 1)."""
-    assert sg.plan(256, 256, 256).config == 1
-    assert sg.plan(512, 512, 512).config == 1
+    for n in (256, 512):  # (or split-K within clusters, which has no epilogue warps' write-out)
+        p = sg.plan(n, n, n)
+        assert p.config == 1 or p.cluster_split == 1
     for shape in [(1024, 1024, 1024), (2048, 2048, 2048), (4096, 4096, 4096), (8192, 8192, 8192),
                   (2047, 3001, 1531)]:
         assert sg.plan(*shape).config == 0, shape
     p = sg.plan(4096, 4096, 4096)
     assert p.threads == (8 + 1 + 2) * 32  # 8 compute warps, the TMA warp, 2 epilogue warps
+
+
+def test_plan_small_problems_reduce_within_clusters(lib):
+    """Small problems: the split-K CTAs of a tile form one cluster and add their
+    partial tiles in distributed shared memory, so the call is one launch with no
+    workspace; large ones keep the persistent grid."""
+    for n in (256, 512):
+        p = sg.plan(n, n, n, num_sms=152)
+        assert p.cluster_split == 1 and 2 <= p.splits <= 8 and p.launches == 1 and p.workspace_bytes == 0
+        assert p.grid == p.units == p.tiles_m * p.tiles_n * p.splits
+    for shape in ((4096, 4096, 4096), (2047, 3001, 1531), (16384, 64, 8192)):
+        assert sg.plan(*shape, num_sms=152).cluster_split == 0

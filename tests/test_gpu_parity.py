@@ -92,6 +92,58 @@ def test_a_layouts_give_identical_bits(h, cfg):
         check_against_oracle(outs[1], A, B, C, 1.25, -0.5)
 
 
+@pytest.mark.parametrize("cfg", range(4))
+@pytest.mark.parametrize("splits", [2, 3, 5, 8])
+@pytest.mark.parametrize("ta", [1, 2])
+def test_cluster_split_matches_workspace_split(h, cfg, splits, ta):
+    """Split-K reduced within thread-block clusters (partials added in distributed
+    shared memory, one launch) against the same plan with the partials going
+    through the workspace to the reduction kernel: the same additions in the same
+    order, so bit for bit the same C; exact on integers, inside the bound on reals.
+    Shapes around tile multiples, ragged N and unaligned / padded C."""
+    shapes = [((63, 65, 333), (None, None, None), (0, 0, 0)), ((129, 127, 500), (None, None, 130), (0, 0, 1)),
+              ((256, 200, 1000), (1001, 203, 201), (0, 0, 0)), ((300, 260, 777), (None, None, None), (1, 0, 2))]
+    for (M, N, K), lds, offs in shapes:
+        for dist, alpha, beta in ((("int", "int", "int"), 1.5, 0.5), (("normal", "uniform", "uniform"), -0.75, 1.25),
+                                  (("normal", "normal", "uniform"), 1.0, 0.0)):
+            A, B, C = ops(M, N, K, seed=cfg * 100 + splits * 10 + M, dist=dist)
+            outs = []
+            for cl in (1, 0):
+                force(h, cfg, splits, ta)
+                h.set_option(sg.OPT_CLUSTER_SPLIT, cl)
+                try:
+                    got, guards, st = run_gemm(torch, h, A, B, C, alpha, beta, lds=lds, offsets=offs)
+                    assert st == sg.SGEMM_OK and guards
+                    assert h.check_device_status() == (sg.SGEMM_OK, 0)
+                    p = h.last_plan()
+                    assert p.cluster_split == cl and p.splits == min(splits, (K + 31) // 32), p.as_dict()
+                    if cl:  # no reduction launch; the workspace holds operand copies at most
+                        assert p.grid == p.units and p.launches == 1 + (p.transpose_a == 1) + p.repack_a + p.repack_b
+                finally:
+                    force(h)
+                    h.set_option(sg.OPT_CLUSTER_SPLIT, -1)
+                outs.append(got)
+            assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32)), (cfg, splits, ta, M, N, K)
+            check_against_oracle(outs[0], A, B, C, alpha, beta, exact=dist[0] == "int")
+
+
+def test_cluster_split_beta_zero_never_reads_c(h):
+    """Within clusters too, beta = 0 writes C without reading it (NaN in C stays out)."""
+    M, N, K = 200, 190, 600
+    A, B, _ = ops(M, N, K, seed=9, dist=("normal", "normal", "uniform"))
+    nanC = np.full((M, N), np.nan, np.float32)
+    h.set_option(sg.OPT_CLUSTER_SPLIT, 1)
+    force(h, 3, 4, 2)
+    try:
+        got, guards, st = run_gemm(torch, h, A, B, nanC, 1.0, 0.0)
+        assert st == sg.SGEMM_OK and guards and h.last_plan().cluster_split == 1
+    finally:
+        force(h)
+        h.set_option(sg.OPT_CLUSTER_SPLIT, -1)
+    assert np.all(np.isfinite(got))
+    check_against_oracle(got, A, B, None, 1.0, 0.0)
+
+
 def test_deterministic(h):
     A, B, C = ops(300, 260, 700, seed=5, dist=("normal", "normal", "uniform"))
     r1, _, _ = run_gemm(torch, h, A, B, C, 1.0, 1.0)
@@ -172,10 +224,12 @@ def test_option_values_are_checked(h):
     """Out-of-range option values and unknown options are refused and change nothing."""
     lib = sg.library()
     for opt, bad in ((sg.OPT_FORCE_TF32_KERNEL, 2), (sg.OPT_FORCE_REPACK_C, 2), (sg.OPT_FORCE_REPACK_C, -2),
+                     (sg.OPT_CLUSTER_SPLIT, 2), (sg.OPT_CLUSTER_SPLIT, -2),
                      (sg.OPT_FORCE_STREAMK, 2), (sg.OPT_FORCE_TRANSPOSE_A, -2), (sg.OPT_FORCE_TRANSPOSE_A, 3),
                      (99, 0)):
         assert lib.sgemm_set_option(h._h, opt, bad) == sg.SGEMM_ERR_INVALID_VALUE, (opt, bad)
-    for opt in (sg.OPT_FORCE_TF32_KERNEL, sg.OPT_FORCE_REPACK_C, sg.OPT_FORCE_STREAMK, sg.OPT_FORCE_TRANSPOSE_A):
+    for opt in (sg.OPT_FORCE_TF32_KERNEL, sg.OPT_FORCE_REPACK_C, sg.OPT_FORCE_STREAMK, sg.OPT_FORCE_TRANSPOSE_A,
+                sg.OPT_CLUSTER_SPLIT):
         assert lib.sgemm_set_option(h._h, opt, -1) == sg.SGEMM_OK
 
 

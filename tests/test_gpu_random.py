@@ -86,6 +86,9 @@ def test_random_problems(lib_built, mode):
                 h.set_option(sg.OPT_FORCE_CONFIG, opts["config"])
                 h.set_option(sg.OPT_FORCE_SPLITS, opts["splits"])
                 h.set_option(sg.OPT_FORCE_TRANSPOSE_A, opts["transpose_a"])
+                # split-K within clusters or through the workspace (own generator: the
+                # cases drawn above stay the same)
+                h.set_option(sg.OPT_CLUSTER_SPLIT, int(np.random.default_rng(7000 + case).choice([-1, -1, 0, 1])))
             else:
                 # C written in place or through an aligned copy (own generator: the
                 # cases drawn above stay the same)
