@@ -23,6 +23,12 @@
 //   7 warp tile    128 x 128 block, BK = 16, four warps of 64 x 64, each lane
 //                  8 x 4 outputs in four column sub-tiles ("Optimizing Matrix
 //                  Multiplication in CUDA", warp tiling); same shape rule
+//   8 cache blocks 128 x 128 block, 8 x 8 register microtile per thread, A and
+//                  B read straight from global memory through L1 / L2 and no
+//                  shared memory: the block's reuse is left to the caches'
+//                  eviction policy ("Shared memory and register blocking", the
+//                  cache-blocking kernel it measures the shared-memory tiles
+//                  against); same shape rule
 #include <cuda_runtime.h>
 
 #include "sgemm_internal.h"
@@ -272,18 +278,70 @@ __global__ void __launch_bounds__(128) rung_warp(int M, int N, int K, float alph
     }
 }
 
+// ---- rung 8: cache blocking --------------------------------------------------
+// 256 threads; thread t owns rows 8 (t / 16) .. + 7 of the block's 128 and columns
+// 4 (t % 16) .. + 3 and 64 + 4 (t % 16) .. + 3. Per 4-deep k step it loads 16 bytes
+// of each of its 8 A rows and, for each k, 16 bytes of each of its 2 B column groups,
+// all from global memory on the read-only path: the 16 lanes that share a row group
+// read the same A bytes and the 16 that share a column group the same B bytes, so a
+// block's operands are re-read from L1 / L2 rather than staged. Needs K % 4 == 0,
+// N % 4 == 0 and 16-byte-aligned A and B.
+__global__ void __launch_bounds__(256) rung_cache(int M, int N, int K, float alpha, const float *__restrict__ A,
+                                                  const float *__restrict__ B, float beta, float *__restrict__ C)
+{
+    const int t = threadIdx.x;
+    const int row0 = blockIdx.y * 128 + 8 * (t / 16);
+    const int col0 = blockIdx.x * 128 + 4 * (t % 16);
+    const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            a[i] = row0 + i < M ? __ldg(reinterpret_cast<const float4 *>(A + static_cast<long long>(row0 + i) * K + k0))
+                                : zero;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const float *brow = B + static_cast<long long>(k0 + kk) * N;
+            const float4 b0 = col0 < N ? __ldg(reinterpret_cast<const float4 *>(brow + col0)) : zero;
+            const float4 b1 = col0 + 64 < N ? __ldg(reinterpret_cast<const float4 *>(brow + col0 + 64)) : zero;
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av, bv[j], acc[i][j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = row0 + i;
+        if (row >= M) break;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int col = col0 + (j < 4 ? j : 60 + j);
+            if (col < N) write_c(C, static_cast<long long>(row) * N + col, acc[i][j], alpha, beta);
+        }
+    }
+}
+
 dim3 grid_for(int M, int N, int bm, int bn) { return dim3((N + bn - 1) / bn, (M + bm - 1) / bm); }
 
 }  // namespace
 
-// Launch rung 1..7 (see the file header). Returns cudaErrorInvalidValue for an
+// Launch rung 1..8 (see the file header). Returns cudaErrorInvalidValue for an
 // unknown rung or a shape/alignment the rung does not handle.
 cudaError_t launch_ladder(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta,
                           float *C, cudaStream_t stream)
 {
     const bool vec_ok = K % 4 == 0 && N % 4 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0 &&
                         (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
-    if ((rung == 6 || rung == 7) && !vec_ok) return cudaErrorInvalidValue;
+    if (rung >= 6 && !vec_ok) return cudaErrorInvalidValue;
     if ((M + 31) / 32 > 65535) return cudaErrorInvalidValue;
     switch (rung) {
     case 1: rung_simple<false><<<grid_for(M, N, 32, 32), dim3(32, 32), 0, stream>>>(M, N, K, alpha, A, B, beta, C); break;
@@ -293,6 +351,7 @@ cudaError_t launch_ladder(int rung, int M, int N, int K, float alpha, const floa
     case 5: rung_2d<<<grid_for(M, N, 128, 128), 256, 0, stream>>>(M, N, K, alpha, A, B, beta, C); break;
     case 6: rung_vec<<<grid_for(M, N, 128, 128), 256, 0, stream>>>(M, N, K, alpha, A, B, beta, C); break;
     case 7: rung_warp<<<grid_for(M, N, 128, 128), 128, 0, stream>>>(M, N, K, alpha, A, B, beta, C); break;
+    case 8: rung_cache<<<grid_for(M, N, 128, 128), 256, 0, stream>>>(M, N, K, alpha, A, B, beta, C); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

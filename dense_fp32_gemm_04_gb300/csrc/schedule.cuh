@@ -16,7 +16,7 @@
 
 namespace sgemm_impl {
 
-constexpr int kGroupM = 8;  // tile rows per raster group (L2 reuse of B)
+constexpr int kGroupM = 16;  // tile rows per raster group (L2 reuse of A and B)
 
 // Tile index t -> (tile row, tile column): tiles run in groups of kGroupM tile
 // rows, column by column, so concurrently running CTAs share B columns and A

@@ -665,7 +665,7 @@ int sgemm_run_min2(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
 int sgemm_ladder_run(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta, float *C,
                      struct CUstream_st *stream)
 {
-    if (rung < 1 || rung > 7 || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (rung < 1 || rung > 8 || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
     if (!elem_aligned(A) || !elem_aligned(B) || !elem_aligned(C)) return SGEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return SGEMM_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return SGEMM_ERR_INVALID_VALUE;

@@ -14,7 +14,10 @@
  *     kernel (First Half)", Part 4;
  *   6 transposed A in shared memory + 128-bit loads: same page, Parts 5 and 6;
  *   7 warp tiling (64 x 64 warp tiles): "Optimizing Matrix Multiplication in
- *     CUDA", warp tiling.
+ *     CUDA", warp tiling;
+ *   8 cache blocking: 8 x 8 register microtiles per thread with A and B read
+ *     through L1 / L2 and no shared memory, the kernel "Shared memory and
+ *     register blocking" measures its 32 x 32 shared-memory tiles against.
  */
 #ifndef SGEMM_GB300_LADDER_H
 #define SGEMM_GB300_LADDER_H
@@ -26,11 +29,11 @@ extern "C" {
 struct CUstream_st;
 
 /*
- * C = alpha * A * B + beta * C with rung `rung` (1..7), PACKED row-major DEVICE
+ * C = alpha * A * B + beta * C with rung `rung` (1..8), PACKED row-major DEVICE
  * matrices (A: M x K, B: K x N, C: M x N, leading dimensions K, N, N), on the
  * current device, asynchronously on `stream`. beta == 0: C is not read.
  * Returns SGEMM_OK, SGEMM_ERR_INVALID_VALUE (unknown rung, negative dimension,
- * NULL operand with work to do, an operand not 4-byte aligned), SGEMM_ERR_NOT_SUPPORTED (rungs 6 and 7 need
+ * NULL operand with work to do, an operand not 4-byte aligned), SGEMM_ERR_NOT_SUPPORTED (rungs 6, 7 and 8 need
  * K % 4 == 0, N % 4 == 0 and 16-byte-aligned A and B, as the page's vectorised
  * kernel does; M > 2^21) or SGEMM_ERR_LAUNCH.
  */

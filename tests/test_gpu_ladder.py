@@ -27,7 +27,7 @@ def _run(rung, A, B, C, alpha, beta):
     return st, dC.cpu().numpy()
 
 
-@pytest.mark.parametrize("rung", range(1, 8))
+@pytest.mark.parametrize("rung", range(1, 9))
 def test_rung_parity(rung):
     shapes = [(1, 4, 4), (33, 68, 40), (130, 260, 100), (256, 256, 256)] if rung >= 6 else \
              [(1, 1, 1), (33, 65, 17), (130, 257, 99), (256, 256, 256)]
@@ -45,9 +45,10 @@ def test_rung_parity(rung):
 
 def test_vector_rungs_reject_unaligned_shapes():
     A, B, C = inputs.problem_operands(M=16, N=16, K=15, seed=1, dist=("int", "int", "int"))
-    for rung in (6, 7):
+    for rung in (6, 7, 8):
         st, got = _run(rung, A, B, C, 1.0, 0.0)
         assert st == sg.SGEMM_ERR_NOT_SUPPORTED
         assert np.array_equal(got, C)
-    st, _ = _run(8, A, B, C, 1.0, 0.0)
-    assert st == sg.SGEMM_ERR_INVALID_VALUE
+    for rung in (0, 9):
+        st, _ = _run(rung, A, B, C, 1.0, 0.0)
+        assert st == sg.SGEMM_ERR_INVALID_VALUE
