@@ -17,7 +17,10 @@ import threading
 from . import inputs  # noqa: F401  (seeded synthetic operands; no GEMM arithmetic)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm_gb300.so")
+# SGEMM_GB300_DEBUG_CHECKS=1 loads the debug build, whose kernels check the indices
+# of their accesses (python -m dense_fp32_gemm_04_gb300._build --debug builds it).
+LIB_PATH = os.path.join(_PKG, "_lib", "libsgemm_gb300_debug.so" if os.environ.get("SGEMM_GB300_DEBUG_CHECKS") == "1"
+                        else "libsgemm_gb300.so")
 
 SGEMM_OK = 0
 SGEMM_ERR_INVALID_VALUE = 1
@@ -27,6 +30,7 @@ SGEMM_ERR_LAUNCH = 4
 SGEMM_ERR_TIMEOUT = 5
 SGEMM_ERR_CUDA = 6
 SGEMM_ERR_NOT_SUPPORTED = 7
+SGEMM_ERR_INDEX = 8
 
 MATH_FP32 = 0
 MATH_TF32 = 1

@@ -199,6 +199,27 @@ __device__ __forceinline__ void report_status(int *status, int code)
     if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Debug builds (compiled with SGEMM_DEBUG_CHECKS=1): index checks in front of
+// the kernels' memory accesses. A failed check records
+// (SGEMM_ERR_INDEX << 16) | where in the status word and returns false, and the
+// caller skips the access; it never traps. In the default build the check is
+// `true` and compiles away.
+#ifndef SGEMM_DEBUG_CHECKS
+#define SGEMM_DEBUG_CHECKS 0
+#endif
+__device__ __forceinline__ bool index_ok(bool ok, int *status, int where)
+{
+#if SGEMM_DEBUG_CHECKS
+    if (!ok) report_status(status, (8 << 16) | where);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    (void)where;
+    return true;
+#endif
+}
+
 // Launch `kernel`; with `dependent`, as a programmatic dependent of the kernel
 // launched before it on `stream` (used only between kernels of one call, so a
 // grid never waits on a previous call's kernels beyond their completion).

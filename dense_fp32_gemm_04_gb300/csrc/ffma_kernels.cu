@@ -130,6 +130,8 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *tmA, const CUte
             if (p.skew_ns > 0) __nanosleep(static_cast<unsigned>(p.skew_ns));
             const bool skip = (p.inject_skip >= 0 && blockIdx.x == 0 && seq == p.inject_skip);
             if (!skip) {
+                // a box outside the problem would only read fill values: recorded, not skipped
+                index_ok(tm < p.tiles_m && tn < p.tiles_n && kb < p.kblocks, p.status, kWhereIdxCopy);
                 mbar_arrive_expect_tx(full, T::STAGE_BYTES);
                 if (AL == kAMMajor)  // A^T slab: BK rows of k, BM consecutive m
                     tma_load_2d(a_base + stage * T::A_BYTES, tmA, full, tm * T::BM, kb * T::BK);
@@ -270,6 +272,7 @@ __device__ __forceinline__ float4 axpby4(float alpha, float4 v, float beta, floa
 // epilogue; bounds predicates of "SGEMM CUDA kernel (First Half)", Part 2).
 __device__ __forceinline__ void store_c4(const FfmaParams &p, int row, int col, float4 v)
 {
+    if (!index_ok(row >= 0 && row < p.M && col >= 0 && col < p.N, p.status, kWhereIdxStoreC)) return;
     float *dst = p.C + static_cast<long long>(row) * p.ldc + col;
     if (p.vec_c && col + 3 < p.N) {
         float4 out;
@@ -306,6 +309,7 @@ __device__ __forceinline__ float4 load_c4(const FfmaParams &p, int row, int col)
 
 __device__ __forceinline__ void store_c4_loaded(const FfmaParams &p, int row, int col, float4 v, float4 c)
 {
+    if (!index_ok(row >= 0 && row < p.M && col >= 0 && col < p.N, p.status, kWhereIdxStoreC)) return;
     float *dst = p.C + static_cast<long long>(row) * p.ldc + col;
     const float4 out = p.beta != 0.0f ? axpby4(p.alpha, v, p.beta, c)
                                       : make_float4(p.alpha * v.x, p.alpha * v.y, p.alpha * v.z, p.alpha * v.w);
@@ -335,8 +339,11 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc
         for (int i = 0; i < 8; ++i) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                *reinterpret_cast<float4 *>(W + (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h) =
-                    out4(acc, i, h);
+                const long long e = static_cast<long long>(w.idx) * (T::BM * T::BN) +
+                                    (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h;
+                if (index_ok(w.idx >= 0 && e + 4 <= p.w_elems, p.status, kWhereIdxPartial))
+                    *reinterpret_cast<float4 *>(W + (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h) =
+                        out4(acc, i, h);
             }
         }
         return;
@@ -351,7 +358,9 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int col = col0 + 32 * h;
-                if (col < p.N) {
+                const long long e = static_cast<long long>(w.idx) * p.wstride + static_cast<long long>(row) * p.ldw + col;
+                if (col < p.N && index_ok(w.idx >= 0 && w.idx < p.splits && col + 4 <= p.ldw && e + 4 <= p.w_elems,
+                                          p.status, kWhereIdxSplit)) {
                     *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) = out4(acc, i, h);
                 }
             }
@@ -414,15 +423,18 @@ __device__ __forceinline__ void epilogue(const FfmaParams &p, const Acc<AT> &acc
 // bytes, so the 128-bit stores are conflict-free) and goes on with its next
 // tile; the epilogue warps move the staging tile to its destination meanwhile.
 template <class T, bool AT>
-__device__ __forceinline__ void stage_tile(float *stg, const Acc<AT> &acc, int wm, int wn, int r, int c)
+__device__ __forceinline__ void stage_tile(float *stg, const Acc<AT> &acc, int wm, int wn, int r, int c, int *status)
 {
     const int lr0 = wm * T::WM;
     const int lc0 = wn * T::WN + c * 4;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-            *reinterpret_cast<float4 *>(stg + (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h) = out4(acc, i, h);
+        for (int h = 0; h < 2; ++h) {
+            const int e = (lr0 + out_row<AT>(r, i)) * T::BN + lc0 + 32 * h;
+            if (index_ok(e >= 0 && e + 4 <= T::BM * T::BN, status, kWhereIdxStaging))
+                *reinterpret_cast<float4 *>(stg + e) = out4(acc, i, h);
+        }
     }
 }
 
@@ -458,7 +470,7 @@ __device__ __forceinline__ void sts32(uint32_t addr, float v)
 // warp's 4-byte stores of one k cover 32 consecutive m, one bank each. Both
 // sides are conflict-free and no value moves between registers.
 template <class T>
-__device__ __forceinline__ void transpose_slab(uint32_t src, uint32_t dst, int lane)
+__device__ __forceinline__ void transpose_slab(uint32_t src, uint32_t dst, int lane, int *status)
 {
     const uint32_t s0 = src + static_cast<uint32_t>(lane * 128);
     const uint32_t d0 = dst + static_cast<uint32_t>(lane * 4);
@@ -467,10 +479,17 @@ __device__ __forceinline__ void transpose_slab(uint32_t src, uint32_t dst, int l
     for (int blk = 0; blk < T::BM / 32; ++blk) {
         float4 v[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) v[t] = lds128(s0 + blk * 32 * 128 + ((t ^ sw) << 4));
+        for (int t = 0; t < 8; ++t) {
+            const int off = (32 * blk + lane) * 128 + ((t ^ sw) << 4);
+            v[t] = index_ok(off >= 0 && off + 16 <= T::A_BYTES, status, kWhereIdxTranspose)
+                       ? lds128(s0 + blk * 32 * 128 + ((t ^ sw) << 4))
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             const uint32_t d = d0 + static_cast<uint32_t>((4 * t * T::BM + 32 * blk) * 4);
+            const int off = (4 * t * T::BM + 32 * blk + lane) * 4;
+            if (!index_ok(off >= 0 && off + 3 * T::BM * 4 + 4 <= T::A_BYTES, status, kWhereIdxTranspose)) continue;
             sts32(d, v[t].x);
             sts32(d + T::BM * 4, v[t].y);
             sts32(d + 2 * T::BM * 4, v[t].z);
@@ -507,7 +526,7 @@ __device__ __forceinline__ void transposer_loop(const FfmaParams &p, uint32_t a_
                 return;
             }
             if (p.skew_ns > 0) __nanosleep(static_cast<unsigned>(p.skew_ns));
-            transpose_slab<T>(a_base + stage * T::A_BYTES, x_base + xs * T::A_BYTES, lane);
+            transpose_slab<T>(a_base + stage * T::A_BYTES, x_base + xs * T::A_BYTES, lane, p.status);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar_base + 8 * (T::STAGES + stage));  // the stage's A has been read
@@ -551,11 +570,16 @@ __device__ __forceinline__ void epilogue_warp_loop(const FfmaParams &p, uint32_t
             }
             return;
         }
-        if (w.dest == kToPartial) {
+        if (!index_ok(lr_begin + ROWS <= T::BM && lc + 4 <= T::BN, p.status, kWhereIdxEpiRead)) {
+            // (nothing of this tile is moved)
+        } else if (w.dest == kToPartial) {
             float *W = p.W + static_cast<long long>(w.idx) * (T::BM * T::BN) + lr_begin * T::BN + lc;
+            const long long e_last = static_cast<long long>(w.idx) * (T::BM * T::BN) + (lr_begin + ROWS - 1) * T::BN + lc;
+            if (index_ok(w.idx >= 0 && e_last + 4 <= p.w_elems, p.status, kWhereIdxPartial)) {
 #pragma unroll 8
-            for (int lr = 0; lr < ROWS; ++lr)
-                *reinterpret_cast<float4 *>(W + lr * T::BN) = lds128(src0 + lr * T::BN * 4);
+                for (int lr = 0; lr < ROWS; ++lr)
+                    *reinterpret_cast<float4 *>(W + lr * T::BN) = lds128(src0 + lr * T::BN * 4);
+            }
         } else if (w.dest == kToSplit) {
             float *W = p.W + static_cast<long long>(w.idx) * p.wstride;
             const int col = w.tn * T::BN + lc;
@@ -564,8 +588,11 @@ __device__ __forceinline__ void epilogue_warp_loop(const FfmaParams &p, uint32_t
                 for (int lr = 0; lr < ROWS; ++lr) {
                     const int row = w.tm * T::BM + lr_begin + lr;
                     if (row >= p.M) break;
-                    *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) =
-                        lds128(src0 + lr * T::BN * 4);
+                    const long long e = static_cast<long long>(w.idx) * p.wstride + static_cast<long long>(row) * p.ldw + col;
+                    if (index_ok(w.idx >= 0 && w.idx < p.splits && col + 4 <= p.ldw && e + 4 <= p.w_elems, p.status,
+                                 kWhereIdxSplit))
+                        *reinterpret_cast<float4 *>(W + static_cast<long long>(row) * p.ldw + col) =
+                            lds128(src0 + lr * T::BN * 4);
                 }
             }
         } else {
@@ -615,7 +642,7 @@ __device__ __forceinline__ void cluster_split_epilogue(const FfmaParams &p, cons
     constexpr int kThreads = T::CONSUMERS * 32;
     // every compute warp is done with the ring (its memory may hold the staged tile)
     named_barrier_or(1, kThreads, false);
-    if (staged_ok) stage_tile<T, AT>(stg, acc, wm, wn, r, c);
+    if (staged_ok) stage_tile<T, AT>(stg, acc, wm, wn, r, c, p.status);
     cluster_sync();
     const int S = p.cluster_split;
     // The partials are read at this CTA's own staging offset in every peer: all
@@ -638,6 +665,8 @@ __device__ __forceinline__ void cluster_split_epilogue(const FfmaParams &p, cons
         const uint32_t base = smem_addr(stg);
         for (int q = rank * Q / S + t; q < q1; q += kThreads) {
             float4 v[8];
+            if (!index_ok(q >= 0 && q < Q && S <= static_cast<int>(cluster_size()) && S <= 8, p.status, kWhereIdxCluster))
+                continue;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 if (j < S) v[j] = ld_shared_cluster_v4(mapa_shared(base + static_cast<uint32_t>(q) * 16u, j));
@@ -659,7 +688,10 @@ __device__ __forceinline__ void cluster_split_epilogue(const FfmaParams &p, cons
     cluster_sync();
 }
 
-template <class T, int AL>
+// CL: the split-K-within-clusters form (p.cluster_split > 0), compiled as a
+// kernel of its own so that the other forms' code, and their register
+// allocation, do not carry its branches.
+template <class T, int AL, bool CL = false>
 __global__ void __launch_bounds__(T::THREADS, T::MINB)
 ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const FfmaParams p)
@@ -693,15 +725,17 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (p.cluster_split > 0 && (cluster_size() != static_cast<uint32_t>(p.cluster_split) || p.splits != p.cluster_split ||
-                                p.units != static_cast<int>(gridDim.x) || p.sk_tiles != 0)) {
-        // not launched as the plan's clusters of one unit per CTA: do nothing (before any barrier or copy)
+    if (CL ? (p.cluster_split <= 0 || cluster_size() != static_cast<uint32_t>(p.cluster_split) ||
+              p.splits != p.cluster_split || p.units != static_cast<int>(gridDim.x) || p.sk_tiles != 0)
+           : p.cluster_split != 0) {
+        // not launched as the plan's form (clusters of one unit per CTA, or no
+        // clusters): do nothing (before any barrier or copy)
         if (threadIdx.x == 0) report_status(p.status, kNotSupportedCode | kWhereClusterShape);
         return;
     }
 
     if (threadIdx.x == 0) {
-        if (p.cluster_split > 0)
+        if constexpr (CL)
             *reinterpret_cast<volatile uint32_t *>(bar_ptr + (2 * T::STAGES + (T::EPI > 0 ? 2 : 0) + 2 * T::XB) * 8 +
                                                    4) = smem_addr(cs_stage);
         for (int s = 0; s < T::STAGES; ++s) {
@@ -739,7 +773,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if constexpr (T::EPI > 0) {
         if (warp > T::CONSUMERS + XW) {
             // (split-K within clusters: the compute warps write C themselves)
-            if (p.cluster_split == 0)
+            if constexpr (!CL)
                 epilogue_warp_loop<T>(p, smem_addr(stg), staged_bar, freed_bar, abort_flag,
                                       warp - T::CONSUMERS - 1 - XW, lane);
             return;
@@ -773,7 +807,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 32 / kRows; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
-        bool failed = false;
+        [[maybe_unused]] bool failed = false;
         for (int kb = kb0; kb < kb1; ++kb) {
             const uint32_t full = bar_base + 8 * stage;
             bool ok = mbar_wait_bounded(full, phase, abort_flag, p.timeout_ns);
@@ -784,12 +818,13 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     *abort_flag = 1;
                     report_status(p.status, kTimeoutCode | kWhereConsumerFull);
                 }
-                if (p.cluster_split > 0) {  // still meet the cluster's barriers
+                if constexpr (CL) {  // still meet the cluster's barriers
                     failed = true;
                     break;
                 }
                 return;
             }
+            index_ok(stage < T::STAGES && (AL != kASmemT || xs < T::XB), p.status, kWhereIdxRing);
             if constexpr (AL == kASmemT)
                 compute_slab_mmajor<T>(a_base + xs * (T::A_BYTES / 4), b_cols_base + stage * (T::B_BYTES / 4), acc);
             else if constexpr (AT)
@@ -814,7 +849,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-        if (p.cluster_split > 0) {  // one unit per CTA
+        if constexpr (CL) {  // one unit per CTA
             cluster_split_epilogue<T, AT>(p, acc, cs_stage, layout_word, smem_addr(cs_stage), wm, wn, r, c, !failed);
             return;
         }
@@ -829,7 +864,7 @@ ffma_sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 return;
             }
-            stage_tile<T, AT>(stg, acc, wm, wn, r, c);
+            stage_tile<T, AT>(stg, acc, wm, wn, r, c, p.status);
             __syncwarp();
             if (lane == 0) mbar_arrive(staged_bar);
         } else {
@@ -865,29 +900,37 @@ cudaError_t set_attr()
     if ((e = cudaFuncSetAttribute(ffma_sgemm_kernel<R, kAKMajor>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   R::SMEM_BYTES)) != cudaSuccess)
         return e;
-    return cudaFuncSetAttribute(ffma_sgemm_kernel<X, kASmemT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(ffma_sgemm_kernel<X, kASmemT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  X::SMEM_BYTES)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(ffma_sgemm_kernel<X, kASmemT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 X::SMEM_BYTES);
 }
 
-// Split-K within clusters launches clusters of p.cluster_split CTAs along x.
+// Split-K within clusters (A transposed in shared memory only) launches its
+// own kernel form in clusters of p.cluster_split CTAs along x.
 template <int I>
 cudaError_t launch(int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB, const FfmaParams &p, int grid,
                    cudaStream_t stream, bool dependent)
 {
     using R = typename Row<I>::R;
     using X = typename Row<I>::X;
-    const int cl = p.cluster_split > 0 ? p.cluster_split : 1;
-    if (cl > 8 || grid % cl != 0) return cudaErrorInvalidValue;
+    if (p.cluster_split > 0) {
+        const int cl = p.cluster_split;
+        if (a_layout != kASmemT || cl > 8 || grid % cl != 0) return cudaErrorInvalidValue;
+        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<X, kASmemT, true>, dim3(grid),
+                                     dim3(X::THREADS), X::SMEM_BYTES, stream, tmA, tmB, p);
+    }
     switch (a_layout) {
     case kAMMajor:
-        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<R, kAMMajor>, dim3(grid), dim3(R::THREADS),
-                                     R::SMEM_BYTES, stream, tmA, tmB, p);
+        return launch_kernel(dependent, ffma_sgemm_kernel<R, kAMMajor>, dim3(grid), dim3(R::THREADS), R::SMEM_BYTES,
+                             stream, tmA, tmB, p);
     case kAKMajor:
-        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<R, kAKMajor>, dim3(grid), dim3(R::THREADS),
-                                     R::SMEM_BYTES, stream, tmA, tmB, p);
+        return launch_kernel(dependent, ffma_sgemm_kernel<R, kAKMajor>, dim3(grid), dim3(R::THREADS), R::SMEM_BYTES,
+                             stream, tmA, tmB, p);
     case kASmemT:
-        return launch_kernel_cluster(dependent, cl, ffma_sgemm_kernel<X, kASmemT>, dim3(grid), dim3(X::THREADS),
-                                     X::SMEM_BYTES, stream, tmA, tmB, p);
+        return launch_kernel(dependent, ffma_sgemm_kernel<X, kASmemT>, dim3(grid), dim3(X::THREADS), X::SMEM_BYTES,
+                             stream, tmA, tmB, p);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -898,7 +941,7 @@ cudaError_t launch(int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB,
 // consecutive columns of a row.
 __global__ void splitk_reduce_kernel(const float *__restrict__ W, long long ldw, long long wstride, int splits,
                                      int M, int N, float alpha, float beta, float *__restrict__ C, long long ldc,
-                                     int vec_c)
+                                     int vec_c, long long w_elems, int *status)
 {
     pdl_wait();  // the mainloop's slices are complete and visible
     const int n4 = (N + 3) >> 2;
@@ -908,6 +951,9 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, long long ldw,
         const int row = static_cast<int>(idx / n4);
         const int col = static_cast<int>(idx - static_cast<long long>(row) * n4) * 4;
         const float *w = W + static_cast<long long>(row) * ldw + col;
+        if (!index_ok(col + 4 <= ldw && static_cast<long long>(splits - 1) * wstride + row * ldw + col + 4 <= w_elems,
+                      status, kWhereIdxSplitReduce))
+            continue;
         float4 s = __ldg(reinterpret_cast<const float4 *>(w));
         for (int q = 1; q < splits; ++q) {
             const float4 t = __ldg(reinterpret_cast<const float4 *>(w + q * wstride));
@@ -977,7 +1023,8 @@ __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int 
             const int t = t0 + 32 * k;
             const int lr = t / bn, lc = t - lr * bn;
             const int row = tm * bm + lr, col = tn * bn + lc;
-            in[k] = row < p.M && col < p.N;
+            in[k] = row < p.M && col < p.N &&
+                    index_ok(off[0] >= 0 && off[0] + t < p.w_elems, p.status, kWhereIdxSkReduce);
             cidx[k] = static_cast<long long>(row) * p.ldc + col;
             s[k] = in[k] ? __ldg(p.W + off[0] + t) : 0.0f;
         }
@@ -989,6 +1036,7 @@ __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int 
                 const long long g = g0 + j;
                 o = (2 * g + (rel == (g * S / G) / p.kblocks ? 0 : 1)) * bm * bn;
             }
+            if (!index_ok(o >= 0 && o + t0 + 96 < p.w_elems, p.status, kWhereIdxSkReduce)) continue;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 if (in[k]) s[k] += __ldg(p.W + o + t0 + 32 * k);
@@ -1008,6 +1056,7 @@ __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int 
     const int row = tm * bm + lr, col = tn * bn + lc;
     if (row >= p.M || col >= p.N) return;
     const float *w = p.W + lr * bn + lc;
+    if (!index_ok(off[0] >= 0 && off[0] + lr * bn + lc + 4 <= p.w_elems, p.status, kWhereIdxSkReduce)) return;
     float4 s = *reinterpret_cast<const float4 *>(w + off[0]);
     for (int j = 1; j < nseg; ++j) {
         long long o;
@@ -1017,6 +1066,7 @@ __global__ void __launch_bounds__(256) sk_reduce_kernel(const FfmaParams p, int 
             const long long g = g0 + j;
             o = (2 * g + (rel == (g * S / G) / p.kblocks ? 0 : 1)) * bm * bn;
         }
+        if (!index_ok(o >= 0 && o + lr * bn + lc + 4 <= p.w_elems, p.status, kWhereIdxSkReduce)) continue;
         const float4 v = *reinterpret_cast<const float4 *>(w + o);
         s.x += v.x;
         s.y += v.y;
@@ -1155,11 +1205,11 @@ cudaError_t launch_ffma(int config, int a_layout, const CUtensorMap &tmA, const 
 
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits, int M, int N,
                                  float alpha, float beta, float *C, long long ldc, int vec_c, int num_sms,
-                                 cudaStream_t stream)
+                                 cudaStream_t stream, long long w_elems, int *status)
 {
     const long long work = static_cast<long long>(M) * ((N + 3) / 4);
     return launch_kernel(true, splitk_reduce_kernel, dim3(elementwise_grid(work, 256, num_sms)), dim3(256), 0, stream,
-                         W, ldw, wstride, splits, M, N, alpha, beta, C, ldc, vec_c);
+                         W, ldw, wstride, splits, M, N, alpha, beta, C, ldc, vec_c, w_elems, status);
 }
 
 cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream)

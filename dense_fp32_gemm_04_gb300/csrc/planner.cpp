@@ -335,8 +335,10 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     // 8-CTA clusters of the one-CTA-per-SM row and grids of several waves ran
     // slower (512^3 row 0 with 8 splits 19 -> 27 us; 768^3 rows 1-2 with 8 splits
     // 27 -> 33 us).
+    // (the cluster form reads A transposed in shared memory: not with another A layout forced)
     const long long slots_c = static_cast<long long>(q.num_sms) * c.ctas_per_sm;
-    const bool cl_fits = out->sk_tiles == 0 && S >= 2 && S <= kMaxClusterSplits;
+    const bool cl_fits = out->sk_tiles == 0 && S >= 2 && S <= kMaxClusterSplits &&
+                         (ov.force_transpose_a < 0 || ov.force_transpose_a == 2);
     const bool cl = ov.cluster_split == 1 ? cl_fits
                     : ov.cluster_split < 0
                         ? cl_fits && out->units <= slots_c && (c.ctas_per_sm > 1 || S <= 4)
@@ -354,7 +356,7 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
     if (ov.force_transpose_a >= 0) {
         out->transpose_a = ov.force_transpose_a;
     } else {
-        out->transpose_a = transpose_pays(q, t_plan) ? 1 : 2;
+        out->transpose_a = !cl && transpose_pays(q, t_plan) ? 1 : 2;
     }
     if (out->transpose_a == 1) out->repack_a = 0;  // the transposed copy is aligned whatever A was
     if (out->transpose_a == 2) {

@@ -210,6 +210,7 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         p.W = reinterpret_cast<float *>(ws + w.w_off);
         p.sk_tiles = plan.sk_tiles;
         p.sk_grid = plan.sk_grid;
+        p.w_elems = (w.total - w.w_off) / 4;
     }
     const bool dependent = plan.repack_a || plan.repack_b || (plan.repack_c && beta != 0.0f);
     const cudaError_t le = pair ? launch_tf32_pair(tmA, tmB, p, plan.grid, stream, dependent)
@@ -233,6 +234,8 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
         r.vec_c = p.vec_c;
         r.sk_tiles = p.sk_tiles;
         r.sk_grid = p.sk_grid;
+        r.status = h->d_status;
+        r.w_elems = p.w_elems;
         if (launch_sk_reduce(r, plan.bm, plan.bn, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
     }
     // (an ordinary launch: it waits for the kernels above to complete)
@@ -405,6 +408,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         p.sk_grid = plan.sk_grid;
     }
     p.cluster_split = plan.cluster_split ? plan.splits : 0;
+    p.w_elems = p.W != nullptr ? (w.total - w.w_off) / 4 : 0;
     // Right after this call's transpose / repack: launched as its programmatic dependent.
     const bool after_copy = plan.transpose_a == 1 || plan.repack_a || plan.repack_b;
     if (launch_ffma(plan.config, plan.transpose_a, tmA, tmB, p, plan.grid, stream, after_copy) != cudaSuccess)
@@ -413,7 +417,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1 && !plan.cluster_split) {
         if (launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
-                                 h->num_sms, stream) != cudaSuccess)
+                                 h->num_sms, stream, p.w_elems, h->d_status) != cudaSuccess)
             return SGEMM_ERR_LAUNCH;
     }
     return SGEMM_OK;
@@ -801,6 +805,7 @@ const char *sgemm_status_string(int status)
     case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait ran out";
     case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA runtime or driver call failed";
     case SGEMM_ERR_NOT_SUPPORTED: return "SGEMM_ERR_NOT_SUPPORTED: valid request that is not implemented";
+    case SGEMM_ERR_INDEX: return "SGEMM_ERR_INDEX: a device-side index check of a debug build failed (access skipped)";
     default: return "unknown sgemm status";
     }
 }

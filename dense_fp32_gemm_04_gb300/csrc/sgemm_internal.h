@@ -27,8 +27,22 @@ enum : int {
     kWhereStaging = 8,       // FFMA: a wait on the epilogue's staging tile ran out
     kWhereTransposer = 9,    // FFMA, A transposed in shared memory: the transposer warp's wait for a
                              // filled stage or a free M-major buffer ran out
-    kWhereClusterShape = 10  // FFMA split-K within clusters: the launch's cluster shape or the CTAs'
+    kWhereClusterShape = 10, // FFMA split-K within clusters: the launch's cluster shape or the CTAs'
                              // shared-memory layouts do not match the plan (nothing computed)
+    // Index checks of debug builds (SGEMM_DEBUG_CHECKS=1), reported as SGEMM_ERR_INDEX:
+    kWhereIdxCopy = 20,       // TMA tile coordinate outside the tiles / k-blocks (FFMA)
+    kWhereIdxTranspose = 21,  // transposer warp's shared-memory offsets
+    kWhereIdxRing = 22,       // compute warp's ring stage / M-major buffer
+    kWhereIdxStaging = 23,    // staging tile (or the partial tile staged for a cluster)
+    kWhereIdxStoreC = 24,     // store to C outside M x N
+    kWhereIdxSplit = 25,      // split-K slice outside the workspace
+    kWhereIdxPartial = 26,    // stream-K partial tile outside the workspace
+    kWhereIdxEpiRead = 27,    // epilogue warps' staging-tile reads
+    kWhereIdxCluster = 28,    // distributed shared memory read (split-K within clusters)
+    kWhereIdxSkReduce = 29,   // stream-K reduction's partial-tile reads
+    kWhereIdxSplitReduce = 30,// split-K reduction's slice reads
+    kWhereIdxTf32Copy = 33,   // TF32 TMA tile coordinate
+    kWhereIdxTf32Store = 34   // TF32 store to C or to a partial tile
 };
 
 // Everything the FFMA mainloop needs besides the two tensor maps.
@@ -61,6 +75,7 @@ struct FfmaParams {
     // (= splits; one (tile, slice) unit per CTA, cluster rank = slice): the
     // partial tiles meet in distributed shared memory, W is not used.
     int cluster_split;
+    long long w_elems;  // floats the workspace holds at W (checked by debug builds; 0 without W)
 };
 
 // Everything the TF32 tcgen05 mainloops need besides the two tensor maps
@@ -82,6 +97,7 @@ struct Tf32Params {
     float *W;
     int sk_tiles;
     int sk_grid;
+    long long w_elems;  // floats the workspace holds at W (checked by debug builds)
 };
 
 // Plain-launch helpers implemented in the .cu files. All return the CUDA
@@ -94,9 +110,10 @@ cudaError_t ffma_set_attributes();  // opt in to large dynamic shared memory (cu
 // (transpose / repack), whose completion its copy issue waits for.
 cudaError_t launch_ffma(int config, int a_layout, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const FfmaParams &p, int grid, cudaStream_t stream, bool dependent);
+// w_elems: floats at W (checked by debug builds); status: the device status word.
 cudaError_t launch_splitk_reduce(const float *W, long long ldw, long long wstride, int splits,
                                  int M, int N, float alpha, float beta, float *C, long long ldc,
-                                 int vec_c, int num_sms, cudaStream_t stream);
+                                 int vec_c, int num_sms, cudaStream_t stream, long long w_elems, int *status);
 cudaError_t launch_sk_reduce(const FfmaParams &p, int bm, int bn, int num_sms, cudaStream_t stream);
 cudaError_t launch_ladder(int rung, int M, int N, int K, float alpha, const float *A, const float *B, float beta,
                           float *C, cudaStream_t stream);

@@ -221,11 +221,12 @@ extern "C" int sgemm_run_splitk_static(int M, int N, int K, float alpha, const f
     p.status = status;
     p.timeout_ns = kTimeoutNs;
     p.inject_skip = -1;
+    p.w_elems = p.W != nullptr ? (w.total - w.w_off) / 4 : 0;
     if (sgemm_impl::launch_ffma(plan.config, plan.transpose_a, tmA, tmB, p, plan.grid, st, false) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     if (plan.splits > 1 &&
         sgemm_impl::launch_splitk_reduce(p.W, w.ldw, w.wstride, plan.splits, M, N, alpha, beta, C, ldc, plan.vec_c,
-                                         s->num_sms, st) != cudaSuccess)
+                                         s->num_sms, st, p.w_elems, status) != cudaSuccess)
         return SGEMM_ERR_LAUNCH;
     return SGEMM_OK;
 }

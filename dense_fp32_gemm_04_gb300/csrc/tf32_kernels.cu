@@ -135,13 +135,16 @@ __device__ __forceinline__ void load_row_chunks(uint32_t t_col, uint32_t (&v)[NB
 }
 
 // Raw partial row of a stream-K piece (tile-packed workspace row of BN floats).
+// Every lane loads (warp-collective TMEM loads); `ok` false skips this lane's stores
+// (a failed index check of a debug build).
 template <int NB>
-__device__ __forceinline__ void store_partial_row(uint32_t t_row, float *wrow)
+__device__ __forceinline__ void store_partial_row(uint32_t t_row, float *wrow, bool ok)
 {
 #pragma unroll 1
     for (int ch = 0; ch < BN / 16; ch += NB) {
         uint32_t v[NB][16];
         load_row_chunks<NB>(t_row + ch * 16, v);
+        if (!ok) continue;
 #pragma unroll
         for (int q = 0; q < 4 * NB; ++q) {
             const uint32_t *w = &v[q >> 2][4 * (q & 3)];
@@ -379,6 +382,8 @@ tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 }
                 const uint32_t a_dst = a_base + stage * S::A_BYTES;
                 const uint32_t b_dst = b_base + stage * S::B_BYTES;
+                // a box outside the problem would only read fill values: recorded, not skipped
+                index_ok(w.tm < p.tiles_m && w.tn < p.tiles_n && kb < p.kblocks, p.status, kWhereIdxTf32Copy);
                 if (rank == 0) mbar_arrive_expect_tx(smem_addr(&bars->full[stage]), S::CTAS * S::STAGE_BYTES);
                 if constexpr (PAIR) {
                     const uint32_t full = mapa_shared(smem_addr(&bars->full[stage]), 0);  // rank 0's barrier
@@ -502,10 +507,13 @@ tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 // fill); the stream-K reduction adds the pieces in k order and
                 // applies alpha / beta.
                 float *wrow = p.W + static_cast<long long>(w.idx) * (S::BM * BN) + static_cast<long long>(cta_row) * BN;
+                const bool wok = index_ok(w.idx >= 0 && static_cast<long long>(w.idx) * (S::BM * BN) +
+                                                            static_cast<long long>(cta_row + 1) * BN <= p.w_elems,
+                                          p.status, kWhereIdxTf32Store);
                 if (p.kblocks <= kShortK)
-                    store_partial_row<4>(t_row, wrow);
+                    store_partial_row<4>(t_row, wrow, wok);
                 else
-                    store_partial_row<1>(t_row, wrow);
+                    store_partial_row<1>(t_row, wrow, wok);
             } else {
                 const int row = w.tm * S::BM + cta_row;
                 if (p.kblocks <= kShortK)

@@ -57,7 +57,10 @@ typedef enum sgemm_status {
     SGEMM_ERR_LAUNCH = 4,        /* a kernel launch failed (cudaGetLastError) */
     SGEMM_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (see sgemm_check_device_status) */
     SGEMM_ERR_CUDA = 6,          /* another CUDA runtime/driver call failed */
-    SGEMM_ERR_NOT_SUPPORTED = 7  /* the request is valid but not implemented */
+    SGEMM_ERR_NOT_SUPPORTED = 7, /* the request is valid but not implemented */
+    SGEMM_ERR_INDEX = 8          /* debug builds only (SGEMM_DEBUG_CHECKS): a device-side index
+                                    check failed and its access was skipped (see
+                                    sgemm_check_device_status for the location codes) */
 } sgemm_status_t;
 
 typedef enum sgemm_math_mode {
@@ -290,7 +293,18 @@ int sgemm_set_option(sgemm_handle_t h, int option, long long value);
  * warp's wait for a filled stage or a free M-major A buffer, 10 (with
  * SGEMM_ERR_NOT_SUPPORTED) a split-K cluster launched in another shape than
  * planned or with CTAs whose shared memory is laid out differently, in which
- * case nothing is computed (6 is not used). Returns that
+ * case nothing is computed (6 is not used). Debug builds of the library
+ * (compiled with SGEMM_DEBUG_CHECKS=1, `python -m dense_fp32_gemm_04_gb300._build
+ * --debug`, loaded when SGEMM_GB300_DEBUG_CHECKS=1) check the indices of their
+ * accesses and report a failed check as SGEMM_ERR_INDEX with the location: 20 a
+ * TMA tile coordinate outside the problem's tiles or k-blocks, 21 the
+ * transposer warp's shared-memory offsets, 22 a compute warp's ring stage or
+ * M-major buffer, 23 the staging tile, 24 a store to C outside M x N, 25 a
+ * split-K slice outside the workspace, 26 a stream-K partial tile outside the
+ * workspace, 27 the epilogue warps' staging reads, 28 a distributed shared
+ * memory read of split-K within clusters, 29 the stream-K reduction's partial
+ * reads, 30 the split-K reduction's slice reads, 33 a TF32 TMA coordinate, 34 a
+ * TF32 store to C or to a partial tile. Returns that
  * sgemm_status value, or SGEMM_ERR_CUDA if synchronizing failed (e.g. a sticky
  * device error).
  */
