@@ -56,6 +56,8 @@
 //    in flight and returns — it never traps or spins forever.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <type_traits>
 
@@ -1093,42 +1095,86 @@ __global__ void scale_kernel(int M, int N, float beta, float *__restrict__ C, lo
 // 16-byte-aligned base and row stride so the TMA path can read it.
 constexpr int kRepackThreads = 256, kRepackPerThread = 8;
 constexpr int kRepackChunk = kRepackThreads * kRepackPerThread;  // columns per work item
+
+// Work item `it` = (row, chunk of kRepackChunk columns) of a repack: the block's
+// threads stride along the chunk (coalesced on both sides; kRepackThreads threads),
+// kRepackPerThread loads in flight per thread before any store.
+__device__ __forceinline__ void repack_item(const float *__restrict__ src, long long lds, float *__restrict__ dst,
+                                            long long ldd, int cols, long long nchunks, long long it)
+{
+    const long long row = it / nchunks;
+    const int c0 = static_cast<int>(it - row * nchunks) * kRepackChunk;
+    const int c1 = min(cols, c0 + kRepackChunk);
+    const float *s = src + row * lds;
+    float *d = dst + row * ldd;
+    float v[kRepackPerThread];
+#pragma unroll
+    for (int j = 0; j < kRepackPerThread; ++j) {
+        const int col = c0 + static_cast<int>(threadIdx.x) + j * kRepackThreads;
+        if (col < c1) v[j] = __ldg(s + col);
+    }
+#pragma unroll
+    for (int j = 0; j < kRepackPerThread; ++j) {
+        const int col = c0 + static_cast<int>(threadIdx.x) + j * kRepackThreads;
+        if (col < c1) d[col] = v[j];
+    }
+}
+
 __global__ void repack_kernel(const float *__restrict__ src, long long lds, float *__restrict__ dst, long long ldd,
                               int rows, int cols)
 {
     pdl_trigger();  // the call's mainloop may become resident; it waits for this grid to finish
-    // work items: (row, chunk of kRepackChunk columns); one division per item, the
-    // block's threads stride along the chunk (coalesced on both sides; launched with
-    // kRepackThreads threads)
     const long long nchunks = (cols + kRepackChunk - 1) / kRepackChunk;
     const long long items = static_cast<long long>(rows) * nchunks;
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-        const long long row = it / nchunks;
-        const int c0 = static_cast<int>(it - row * nchunks) * kRepackChunk;
-        const int c1 = min(cols, c0 + kRepackChunk);
-        const float *s = src + row * lds;
-        float *d = dst + row * ldd;
-        // kRepackPerThread loads in flight per thread before any store
-        float v[kRepackPerThread];
-#pragma unroll
-        for (int j = 0; j < kRepackPerThread; ++j) {
-            const int col = c0 + static_cast<int>(threadIdx.x) + j * kRepackThreads;
-            if (col < c1) v[j] = __ldg(s + col);
-        }
-#pragma unroll
-        for (int j = 0; j < kRepackPerThread; ++j) {
-            const int col = c0 + static_cast<int>(threadIdx.x) + j * kRepackThreads;
-            if (col < c1) d[col] = v[j];
-        }
-    }
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) repack_item(src, lds, dst, ldd, cols, nchunks, it);
 }
 
-// XT (cols x ldxt) = X^T for X (rows x cols, row stride ldx) through 64 x 64
-// tiles in shared memory, so both the reads of X rows and the writes of XT rows
-// are coalesced; interior tiles move 16 bytes per thread access when X allows
-// it (VEC: X 16-byte aligned and ldx % 4 == 0; ldxt is always a multiple of 4).
-// Grid-stride over tile rows, so any row count fits the grid's y limit. Gives
-// the FFMA mainloop A^T and the TF32 mainloop B^T.
+// The 64 x 64 tile of X at (r0, c0) into XT (cols x ldxt) = X^T through shared
+// memory, so both the reads of X rows and the writes of XT rows are coalesced;
+// interior tiles move 16 bytes per thread access when X allows it (VEC: X 16-byte
+// aligned and ldx % 4 == 0; ldxt is always a multiple of 4). 256 threads; ends
+// with a barrier, so the tile can be reused at once.
+template <bool VEC>
+__device__ __forceinline__ void transpose_tile(const float *__restrict__ X, long long ldx, float *__restrict__ XT,
+                                               long long ldxt, int rows, int cols, int r0, int c0,
+                                               float (&tile)[64][65])
+{
+    const int t = threadIdx.x;
+    const bool interior = VEC && r0 + 64 <= rows && c0 + 64 <= cols;
+    if (interior) {
+        const int c = (t % 16) * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int r = t / 16 + 16 * q;
+            const float4 v = *reinterpret_cast<const float4 *>(X + static_cast<long long>(r0 + r) * ldx + c0 + c);
+            tile[r][c] = v.x;
+            tile[r][c + 1] = v.y;
+            tile[r][c + 2] = v.z;
+            tile[r][c + 3] = v.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int n = t / 16 + 16 * q;
+            *reinterpret_cast<float4 *>(XT + static_cast<long long>(c0 + n) * ldxt + r0 + c) =
+                make_float4(tile[c][n], tile[c + 1][n], tile[c + 2][n], tile[c + 3][n]);
+        }
+    } else {
+        for (int e = t; e < 64 * 64; e += 256) {
+            const int r = e / 64, c = e % 64;
+            if (r0 + r < rows && c0 + c < cols) tile[r][c] = X[static_cast<long long>(r0 + r) * ldx + c0 + c];
+        }
+        __syncthreads();
+        for (int e = t; e < 64 * 64; e += 256) {
+            const int n = e / 64, k = e % 64;
+            if (c0 + n < cols && r0 + k < rows) XT[static_cast<long long>(c0 + n) * ldxt + r0 + k] = tile[k][n];
+        }
+    }
+    __syncthreads();  // the tile is reused by the next row block
+}
+
+// XT = X^T (see transpose_tile), grid-stride over tile rows, so any row count fits
+// the grid's y limit. Gives the FFMA mainloop A^T.
 template <bool VEC>
 __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ X, long long ldx,
                                                         float *__restrict__ XT, long long ldxt, int rows, int cols)
@@ -1136,41 +1182,56 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
     __shared__ float tile[64][65];
     pdl_trigger();  // the call's mainloop may become resident; it waits for this grid to finish
     const int c0 = blockIdx.x * 64;
-    const int t = threadIdx.x;
-    for (long long r0l = blockIdx.y * 64LL; r0l < rows; r0l += gridDim.y * 64LL) {
-        const int r0 = static_cast<int>(r0l);
-        const bool interior = VEC && r0 + 64 <= rows && c0 + 64 <= cols;
-        if (interior) {
-            const int c = (t % 16) * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int r = t / 16 + 16 * q;
-                const float4 v = *reinterpret_cast<const float4 *>(X + static_cast<long long>(r0 + r) * ldx + c0 + c);
-                tile[r][c] = v.x;
-                tile[r][c + 1] = v.y;
-                tile[r][c + 2] = v.z;
-                tile[r][c + 3] = v.w;
-            }
-            __syncthreads();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = t / 16 + 16 * q;
-                *reinterpret_cast<float4 *>(XT + static_cast<long long>(c0 + n) * ldxt + r0 + c) =
-                    make_float4(tile[c][n], tile[c + 1][n], tile[c + 2][n], tile[c + 3][n]);
-            }
+    for (long long r0l = blockIdx.y * 64LL; r0l < rows; r0l += gridDim.y * 64LL)
+        transpose_tile<VEC>(X, ldx, XT, ldxt, rows, cols, static_cast<int>(r0l), c0, tile);
+}
+
+// Both operand copies of a call in one launch (instead of one launch each):
+// blocks [0, a_blocks) do job A, the others job B. Job A is A^T (one 64 x 64 tile
+// per block, a_transpose) or a repack of A (grid-stride over its items); job B is
+// a repack of B. 256 threads.
+struct PrepJobs {
+    const float *a;
+    long long lda;
+    float *a_dst;
+    long long a_ldd;
+    int a_rows, a_cols;
+    int a_transpose;  // 1: A^T (tiles of 64 x 64, one per block), 0: repack
+    int a_vec;        // A^T: 16-byte accesses inside interior tiles
+    int a_blocks;
+    const float *b;
+    long long ldb;
+    float *b_dst;
+    long long b_ldd;
+    int b_rows, b_cols;
+};
+
+__global__ void __launch_bounds__(256) prep_kernel(const PrepJobs j)
+{
+    __shared__ float tile[64][65];
+    pdl_trigger();  // the call's mainloop may become resident; it waits for this grid to finish
+    const int bid = static_cast<int>(blockIdx.x);
+    if (bid < j.a_blocks) {
+        if (j.a_transpose) {
+            const int tiles_c = (j.a_cols + 63) / 64;
+            const int r0 = (bid / tiles_c) * 64, c0 = (bid % tiles_c) * 64;
+            if (j.a_vec)
+                transpose_tile<true>(j.a, j.lda, j.a_dst, j.a_ldd, j.a_rows, j.a_cols, r0, c0, tile);
+            else
+                transpose_tile<false>(j.a, j.lda, j.a_dst, j.a_ldd, j.a_rows, j.a_cols, r0, c0, tile);
         } else {
-            for (int e = t; e < 64 * 64; e += 256) {
-                const int r = e / 64, c = e % 64;
-                if (r0 + r < rows && c0 + c < cols) tile[r][c] = X[static_cast<long long>(r0 + r) * ldx + c0 + c];
-            }
-            __syncthreads();
-            for (int e = t; e < 64 * 64; e += 256) {
-                const int n = e / 64, k = e % 64;
-                if (c0 + n < cols && r0 + k < rows) XT[static_cast<long long>(c0 + n) * ldxt + r0 + k] = tile[k][n];
-            }
+            const long long nchunks = (j.a_cols + kRepackChunk - 1) / kRepackChunk;
+            const long long items = static_cast<long long>(j.a_rows) * nchunks;
+            for (long long it = bid; it < items; it += j.a_blocks)
+                repack_item(j.a, j.lda, j.a_dst, j.a_ldd, j.a_cols, nchunks, it);
         }
-        __syncthreads();  // the tile is reused by the next row block
+        return;
     }
+    const int nb = static_cast<int>(gridDim.x) - j.a_blocks;
+    const long long nchunks = (j.b_cols + kRepackChunk - 1) / kRepackChunk;
+    const long long items = static_cast<long long>(j.b_rows) * nchunks;
+    for (long long it = bid - j.a_blocks; it < items; it += nb)
+        repack_item(j.b, j.ldb, j.b_dst, j.b_ldd, j.b_cols, nchunks, it);
 }
 
 int elementwise_grid(long long work, int threads, int num_sms)
@@ -1234,6 +1295,41 @@ cudaError_t launch_repack(const float *src, long long lds, float *dst, long long
     const long long cap = 8LL * num_sms;
     const int grid = static_cast<int>(items < 1 ? 1 : (items < cap ? items : cap));
     repack_kernel<<<grid, kRepackThreads, 0, stream>>>(src, lds, dst, ldd, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const float *A, long long lda, float *a_dst, long long a_ldd, int a_rows, int a_cols,
+                        bool a_transpose, const float *B, long long ldb, float *b_dst, long long b_ldd, int b_rows,
+                        int b_cols, int num_sms, cudaStream_t stream)
+{
+    PrepJobs j{};
+    j.a = A;
+    j.lda = lda;
+    j.a_dst = a_dst;
+    j.a_ldd = a_ldd;
+    j.a_rows = a_rows;
+    j.a_cols = a_cols;
+    j.a_transpose = a_transpose ? 1 : 0;
+    j.a_vec = (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && lda % 4 == 0 && a_ldd % 4 == 0;
+    j.b = B;
+    j.ldb = ldb;
+    j.b_dst = b_dst;
+    j.b_ldd = b_ldd;
+    j.b_rows = b_rows;
+    j.b_cols = b_cols;
+    const long long chunk = kRepackChunk;
+    const long long b_items = static_cast<long long>(b_rows) * ((b_cols + chunk - 1) / chunk);
+    long long a_blocks;
+    if (a_transpose) {
+        a_blocks = static_cast<long long>((a_rows + 63) / 64) * ((a_cols + 63) / 64);
+    } else {
+        const long long a_items = static_cast<long long>(a_rows) * ((a_cols + chunk - 1) / chunk);
+        a_blocks = std::min<long long>(a_items, 4LL * num_sms);
+    }
+    const long long b_blocks = std::min<long long>(std::max<long long>(b_items, 1), 4LL * num_sms);
+    if (a_blocks < 1 || a_blocks + b_blocks > INT_MAX) return cudaErrorInvalidValue;
+    j.a_blocks = static_cast<int>(a_blocks);
+    prep_kernel<<<static_cast<unsigned>(a_blocks + b_blocks), 256, 0, stream>>>(j);
     return cudaGetLastError();
 }
 

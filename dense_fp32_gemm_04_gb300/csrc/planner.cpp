@@ -285,7 +285,8 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
         // copy measured slower at every size (ragged 2047 x 3001 x 1531: 87 vs 95 us).
         if (!out->vec_c && ov.force_repack_c == 1) out->repack_c = 1;
         out->workspace_bytes = workspace_layout(q, *out).total;
-        out->launches = out->repack_a + out->repack_b + 1 + (out->sk_tiles > 0 ? 1 : 0) +
+        // (both operand copies go in one launch)
+        out->launches = (out->repack_a || out->repack_b ? 1 : 0) + 1 + (out->sk_tiles > 0 ? 1 : 0) +
                         (out->repack_c ? (q.beta != 0.0f ? 2 : 1) : 0);
         return SGEMM_OK;
     }
@@ -366,7 +367,8 @@ int make_plan(const Problem &q, const Overrides &ov, sgemm_plan_t *out)
 
     const Workspace w = workspace_layout(q, *out);
     out->workspace_bytes = w.total;
-    out->launches = 1 + (out->transpose_a == 1 ? 1 : 0) + out->repack_a + out->repack_b +
+    // (both operand copies, A^T or A repacked and B repacked, go in one launch)
+    out->launches = 1 + (out->transpose_a == 1 || out->repack_a || out->repack_b ? 1 : 0) +
                     ((S > 1 && !out->cluster_split) || out->sk_tiles > 0 ? 1 : 0);
     return SGEMM_OK;
 }

@@ -155,13 +155,22 @@ int run_tf32(sgemm_handle_t h, const sgemm_plan_t &plan, const Workspace &w, int
     char *ws = static_cast<char *>(h->workspace);
     const float *a_src = A, *b_src = B;
     long long a_ld = lda, b_ld = ldb;
-    if (plan.repack_a) {
+    if (plan.repack_a && plan.repack_b) {  // both copies in one launch
+        float *a_dst = reinterpret_cast<float *>(ws + w.a_off);
+        float *b_dst = reinterpret_cast<float *>(ws + w.b_off);
+        if (launch_prep(A, lda, a_dst, w.lda, M, K, false, B, ldb, b_dst, w.ldb, K, N, h->num_sms, stream) !=
+            cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+        a_src = a_dst;
+        a_ld = w.lda;
+        b_src = b_dst;
+        b_ld = w.ldb;
+    } else if (plan.repack_a) {
         float *dst = reinterpret_cast<float *>(ws + w.a_off);
         if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_src = dst;
         a_ld = w.lda;
-    }
-    if (plan.repack_b) {
+    } else if (plan.repack_b) {
         float *dst = reinterpret_cast<float *>(ws + w.b_off);
         if (launch_repack(B, ldb, dst, w.ldb, K, N, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         b_src = dst;
@@ -353,7 +362,18 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
     const float *b_src = B;
     long long b_ld = ldb;
     if (plan.kernel == SGEMM_KERNEL_TF32) return run_tf32(h, plan, w, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
-    if (plan.transpose_a == 1) {
+    const bool copy_a = plan.transpose_a == 1 || plan.repack_a;
+    if (copy_a && plan.repack_b) {  // both operand copies in one launch
+        float *a_dst = reinterpret_cast<float *>(ws + w.a_off);
+        float *b_dst = reinterpret_cast<float *>(ws + w.b_off);
+        if (launch_prep(A, lda, a_dst, w.lda, M, K, plan.transpose_a == 1, B, ldb, b_dst, w.ldb, K, N, h->num_sms,
+                        stream) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
+        a_src = a_dst;
+        a_ld = w.lda;
+        b_src = b_dst;
+        b_ld = w.ldb;
+    } else if (plan.transpose_a == 1) {
         float *dst = reinterpret_cast<float *>(ws + w.a_off);
         if (launch_transpose(A, lda, dst, w.lda, M, K, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_src = dst;
@@ -363,8 +383,7 @@ int run_device(sgemm_handle_t h, int M, int N, int K, float alpha, const float *
         if (launch_repack(A, lda, dst, w.lda, M, K, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         a_src = dst;
         a_ld = w.lda;
-    }
-    if (plan.repack_b) {
+    } else if (plan.repack_b) {
         float *dst = reinterpret_cast<float *>(ws + w.b_off);
         if (launch_repack(B, ldb, dst, w.ldb, K, N, h->num_sms, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         b_src = dst;

@@ -139,5 +139,10 @@ cudaError_t launch_transpose(const float *X, long long ldx, float *XT, long long
                              cudaStream_t stream);
 cudaError_t launch_repack(const float *src, long long lds, float *dst, long long ldd, int rows,
                           int cols, int num_sms, cudaStream_t stream);
+// Both operand copies of a call in one launch: A^T (a_transpose) or a repack of A
+// into a_dst, and a repack of B into b_dst.
+cudaError_t launch_prep(const float *A, long long lda, float *a_dst, long long a_ldd, int a_rows, int a_cols,
+                        bool a_transpose, const float *B, long long ldb, float *b_dst, long long b_ldd, int b_rows,
+                        int b_cols, int num_sms, cudaStream_t stream);
 
 }  // namespace sgemm_impl

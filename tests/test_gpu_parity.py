@@ -121,7 +121,7 @@ def test_cluster_split_matches_workspace_split(h, cfg, splits, ta):
                     assert p.cluster_split == (cl if ta == 2 else 0), p.as_dict()
                     assert p.splits == min(splits, (K + 31) // 32), p.as_dict()
                     if p.cluster_split:  # no reduction launch; the workspace holds operand copies at most
-                        assert p.grid == p.units and p.launches == 1 + (p.transpose_a == 1) + p.repack_a + p.repack_b
+                        assert p.grid == p.units and p.launches == 1 + int(p.transpose_a == 1 or p.repack_a or p.repack_b)
                 finally:
                     force(h)
                     h.set_option(sg.OPT_CLUSTER_SPLIT, -1)
