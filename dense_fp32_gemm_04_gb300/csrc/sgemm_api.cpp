@@ -279,14 +279,16 @@ int ensure_host_pipeline(sgemm_handle_t h)
 // about three times longer to compute (2NK / ~70 TFLOP/s) than its A and C rows
 // take to copy (4 (K + N) bytes at 200 GB/s, at 4096^3), so only the start of the
 // pipeline is copy-bound: nothing can be computed before B has arrived. So B is
-// copied in column blocks (up to 4, multiples of 128 columns), and panel 0 (about
-// M / 8 rows) is computed block by block as they arrive. Then panels grow, each
-// at most three times its predecessor, so its copy-in finishes while the previous
-// panel computes; the last panel is again about M / 8 rows, so the copy-out after
-// the last GEMM is short. Problems with less than two rounds of 128 x 128 tiles
-// outside the edge panels are one panel and one block. All panels but the last
-// have a multiple of 128 rows. (M = N = K = 4096: panels 512 (4 blocks of 1024
-// columns), 512, 1536, 1024, 512.)
+// copied in column blocks (up to 4, multiples of 128 columns), and panel 0 is
+// computed block by block as they arrive. Panel 0 is sized so that computing it
+// takes about as long as B takes to arrive: 2 p N K / ~60 TFLOP/s (its GEMMs are
+// small) against 4 K N / ~200 GB/s gives p ~ 600 rows whatever N and K; 768 (at
+// most M / 4) measured best. Then panels grow, each at most three times its
+// predecessor, so its copy-in finishes while the previous panel computes; the
+// last panel is half of panel 0, so the copy-out after the last GEMM is short.
+// Problems with less than two rounds of 128 x 128 tiles outside the edge panels
+// are one panel and one block. All panels but the last have a multiple of 128
+// rows. (M = N = K = 4096: panels 768 (4 blocks of 1024 columns), 768, 2176, 384.)
 struct HostSchedule {
     int panels = 1;
     int start[kMaxHostPanels + 1] = {};
@@ -300,15 +302,16 @@ HostSchedule host_schedule(const sgemm_handle_s *h, int M, int N, int K, bool sp
     sc.start[1] = M;
     sc.col[1] = N;
     if (static_cast<double>(M) * N * K < 1.0e9 || M < 1024) return sc;
-    const int edge = std::max(128, M / 8 / 128 * 128);
+    const int edge = std::max(128, std::min(768, M / 4 / 128 * 128));
+    const int last = std::max(128, edge / 2 / 128 * 128);
     const long long mid_tiles = static_cast<long long>((M - 2 * edge + 127) / 128) * ((N + 127) / 128);
     if (mid_tiles < 2LL * h->num_sms) return sc;
     int P = 0, r = 0, size = edge;
     for (int i = 0;; ++i) {
         const int left = M - r;
         int take = i < 2 ? edge : 3 * size;
-        take = std::min(take, left - edge) / 128 * 128;  // leave at least `edge` rows for the last panel
-        if (left <= edge || P == kMaxHostPanels - 1 || take <= 0) {
+        take = std::min(take, left - last) / 128 * 128;  // leave at least `last` rows for the last panel
+        if (left <= last || P == kMaxHostPanels - 1 || take <= 0) {
             sc.start[++P] = M;
             break;
         }
