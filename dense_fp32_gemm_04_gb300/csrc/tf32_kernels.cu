@@ -88,7 +88,7 @@ struct Tf32Shape {
     static constexpr int SMEM = PAIR ? sgemm_cfg::tf32_pair_smem_bytes() : sgemm_cfg::tf32_smem_bytes();
     static_assert(CTA_M == 128, "an accumulator holds 128 TMEM lanes");
     static_assert(CTA_N % kBoxN == 0, "whole B boxes");
-    static_assert(SMEM == 1024 + STAGES * STAGE_BYTES + 256, "smem layout");
+    static_assert(SMEM == 1024 + STAGES * STAGE_BYTES + 256 + sgemm_cfg::kTf32StagingBytes, "smem layout");
 };
 
 template <int STAGES>
@@ -116,182 +116,169 @@ __device__ __forceinline__ void raise_abort(Tf32Bars<STAGES> *b, const Tf32Param
     }
 }
 
-// Epilogue of one accumulator row (a thread's TMEM lane: 256 columns), NB x 16
-// columns per step: NB TMEM loads, one wait, then (beta != 0) all of the step's
-// C loads before any use. Short K (few k-blocks per tile) makes the epilogue the
-// critical path, so there NB = 4 keeps 16 loads in flight per thread; with long
-// K it overlaps the next tile's mainloop and NB = 1 keeps its memory traffic
-// from crowding the operand copies (measured: NB = 4 everywhere cost 2-4 % at
-// 4096^3 and 8192^2 x 4096, and saved 44 % at K = 32).
-constexpr int kShortK = 16;  // k-blocks of 32
+// Epilogue. A warp holds 32 rows of a CTA's accumulator (its TMEM lane
+// quarter); tcgen05.ld hands thread l the columns of row l, so stores made
+// straight from those registers touch 32 rows, 16 bytes each, per instruction.
+// Instead each 32-column block goes through the warp's staging area in shared
+// memory and leaves it coalesced:
+//  - 16-byte rows (the partial tiles in W, or C with vec_c): lane l takes
+//    16-byte chunk l % 8 of rows 4k + l / 8 (k = 0..7), so 8 lanes cover one
+//    row's 128 bytes;
+//  - other C: lane l takes column l of each of the 32 rows (4-byte accesses,
+//    128 contiguous bytes per instruction, whatever the row's alignment).
+// With beta != 0 the next block's C loads are issued before the current block
+// is turned and written, so two blocks' loads are in flight.
+constexpr int kStgPitch = 36;  // floats between staged rows (see stage_block)
+static_assert(sgemm_cfg::kTf32StagingBytes == 4 * 32 * kStgPitch * 4, "four epilogue warps' staging areas");
 
-template <int NB>
-__device__ __forceinline__ void load_row_chunks(uint32_t t_col, uint32_t (&v)[NB][16])
+__device__ __forceinline__ float4 lds128(uint32_t addr)
 {
-#pragma unroll
-    for (int j = 0; j < NB; ++j) tmem_ld_16(t_col + j * 16, v[j]);
-#pragma unroll
-    for (int j = 0; j < NB; ++j) tmem_wait_ld(v[j]);
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
-// Raw partial row of a stream-K piece (tile-packed workspace row of BN floats).
-// Every lane loads (warp-collective TMEM loads); `ok` false skips this lane's stores
-// (a failed index check of a debug build).
-template <int NB>
-__device__ __forceinline__ void store_partial_row(uint32_t t_row, float *wrow, bool ok)
+__device__ __forceinline__ float lds32(uint32_t addr)
 {
-#pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ch += NB) {
-        uint32_t v[NB][16];
-        load_row_chunks<NB>(t_row + ch * 16, v);
-        if (!ok) continue;
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+// Thread l: TMEM row l, columns [t_col, t_col + 32) into staged row l. With a
+// pitch of 36 floats the 8 rows of a quarter-warp's 16-byte stores, and the 8
+// chunks of one row that a quarter-warp reads back, fall in 8 different 16-byte
+// bank groups.
+__device__ __forceinline__ void stage_block(uint32_t t_col, uint32_t stg, int lane)
+{
+    uint32_t v[2][16];
+    tmem_ld_16(t_col, v[0]);  // every lane: .sync.aligned
+    tmem_ld_16(t_col + 16, v[1]);
+    tmem_wait_ld(v[0]);
+    tmem_wait_ld(v[1]);
+    const uint32_t row = stg + static_cast<uint32_t>(lane * kStgPitch * 4);
 #pragma unroll
-        for (int q = 0; q < 4 * NB; ++q) {
-            const uint32_t *w = &v[q >> 2][4 * (q & 3)];
-            *reinterpret_cast<float4 *>(wrow + ch * 16 + 4 * q) =
-                make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
-                            __uint_as_float(w[3]));
+    for (int i = 0; i < 8; ++i)
+        sts128(row + 16 * i, v[i >> 2][4 * (i & 3)], v[i >> 2][4 * (i & 3) + 1], v[i >> 2][4 * (i & 3) + 2],
+               v[i >> 2][4 * (i & 3) + 3]);
+    __syncwarp();
+}
+
+__device__ __forceinline__ float epi_value(const Tf32Params &p, float acc, float c)
+{
+    return p.beta != 0.0f ? fmaf(p.alpha, acc, p.beta * c) : p.alpha * acc;
+}
+
+// C of block cb for this lane (0 outside the problem): 16-byte form, rows
+// 4k + sub, chunk q; or 4-byte form, column `lane` of rows 0..31.
+__device__ __forceinline__ void load_c_block(const Tf32Params &p, int grow0, int col0, int cb, int lane,
+                                             float (&c)[32])
+{
+    if (p.vec_c) {
+        const int sub = lane >> 3, col = col0 + cb * 32 + 4 * (lane & 7);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int grow = grow0 + 4 * k + sub;
+            if (grow < p.M && col + 3 < p.N) {
+                const float4 x = *reinterpret_cast<const float4 *>(p.C + static_cast<long long>(grow) * p.ldc + col);
+                c[4 * k] = x.x;
+                c[4 * k + 1] = x.y;
+                c[4 * k + 2] = x.z;
+                c[4 * k + 3] = x.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    c[4 * k + e] = (grow < p.M && col + e < p.N) ? p.C[static_cast<long long>(grow) * p.ldc + col + e]
+                                                                 : 0.0f;
+            }
         }
-    }
-}
-
-// Shifted frame for a row of C that is not 16-byte aligned. With s the number of
-// elements before the row's first 16-byte boundary (C itself is 4-byte aligned),
-// the row is written in 4-element chunks at columns s - 4 + 4j: every chunk that
-// lies wholly inside [0, lim) is one 16-byte access, the rest (the first chunk,
-// the last one when s != 0, chunks past N) go element by element. The step's
-// accumulator values come after the previous step's last four (x[0..3]), so
-// chunk j of a step holds x[4j + s .. 4j + s + 3]; `pick` makes that runtime
-// offset a choice among four registers (i is a constant once the loops unroll).
-__device__ __forceinline__ float pick(const float *x, int i, int s)
-{
-    return s == 0 ? x[i] : s == 1 ? x[i + 1] : s == 2 ? x[i + 2] : x[i + 3];
-}
-
-__device__ __forceinline__ bool chunk_whole(int r0, int lim) { return r0 >= 0 && r0 + 3 < lim; }
-
-__device__ __forceinline__ float4 load_chunk(const float *cbase, int r0, int lim)
-{
-    if (chunk_whole(r0, lim)) return *reinterpret_cast<const float4 *>(cbase + r0);
-    float e[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) e[q] = (r0 + q >= 0 && r0 + q < lim) ? cbase[r0 + q] : 0.0f;
-    return make_float4(e[0], e[1], e[2], e[3]);
-}
-
-__device__ __forceinline__ void store_chunk(const Tf32Params &p, float *cbase, int r0, int lim, const float (&a)[4],
-                                            float4 c)
-{
-    float4 out;
-    if (p.beta != 0.0f)
-        out = make_float4(fmaf(p.alpha, a[0], p.beta * c.x), fmaf(p.alpha, a[1], p.beta * c.y),
-                          fmaf(p.alpha, a[2], p.beta * c.z), fmaf(p.alpha, a[3], p.beta * c.w));
-    else
-        out = make_float4(p.alpha * a[0], p.alpha * a[1], p.alpha * a[2], p.alpha * a[3]);
-    if (chunk_whole(r0, lim)) {
-        *reinterpret_cast<float4 *>(cbase + r0) = out;
     } else {
-        const float e[4] = {out.x, out.y, out.z, out.w};
+        const int col = col0 + cb * 32 + lane;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (r0 + q >= 0 && r0 + q < lim) cbase[r0 + q] = e[q];
+        for (int r = 0; r < 32; ++r) {
+            const int grow = grow0 + r;
+            c[r] = (grow < p.M && col < p.N) ? p.C[static_cast<long long>(grow) * p.ldc + col] : 0.0f;
+        }
     }
 }
 
-// The tile's part of row `row` of C (cbase = its first column, lim = the columns
-// of the tile inside N) in the shifted frame; same steps and load batching as
-// store_c_row.
-template <int NB>
-__device__ __forceinline__ void store_c_row_shifted(const Tf32Params &p, uint32_t t_row, int row, float *cbase,
-                                                    int lim)
+// One finished tile, this warp's 32 rows (tile rows row0 .. row0 + 31; TMEM
+// lanes of t_row): to C with alpha / beta, or raw into the tile's partial tile
+// in W (tile-packed rows of BN floats; rows and columns past M and N hold sums
+// of the copy engine's zero fill, and the stream-K reduction adds the pieces in
+// k order). `stg`: the warp's staging area.
+template <class S>
+__device__ __forceinline__ void write_tile(const Tf32Params &p, uint32_t t_row, uint32_t stg, const Work &w, int row0,
+                                           int lane)
 {
-    const int s = static_cast<int>((4u - ((static_cast<uint32_t>(reinterpret_cast<uintptr_t>(cbase)) >> 2) & 3u)) & 3u);
-    float x[16 * NB + 4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[i] = 0.0f;
+    const int sub = lane >> 3, q = lane & 7;
+    if (w.dest == kToPartial) {
+        float *wb = p.W + static_cast<long long>(w.idx) * (S::BM * BN) + static_cast<long long>(row0) * BN;
+        const bool ok = index_ok(w.idx >= 0 && static_cast<long long>(w.idx) * (S::BM * BN) +
+                                                   static_cast<long long>(row0 + 32) * BN <= p.w_elems,
+                                 p.status, kWhereIdxTf32Store);
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ch += NB) {
-        uint32_t v[NB][16];
-        load_row_chunks<NB>(t_row + ch * 16, v);  // every lane: .sync.aligned
-        if (row >= p.M) continue;
+        for (int cb = 0; cb < BN / 32; ++cb) {
+            stage_block(t_row + cb * 32, stg, lane);
+            if (ok) {
 #pragma unroll
-        for (int i = 0; i < 16 * NB; ++i) x[4 + i] = __uint_as_float(v[i >> 4][i & 15]);
-        const int cb = ch * 16 + s - 4;  // column of chunk 0
-        float4 c[4 * NB];
-        if (p.beta != 0.0f) {
-#pragma unroll
-            for (int j = 0; j < 4 * NB; ++j) c[j] = load_chunk(cbase, cb + 4 * j, lim);
-        }
-#pragma unroll
-        for (int j = 0; j < 4 * NB; ++j) {
-            const float a[4] = {pick(x, 4 * j, s), pick(x, 4 * j + 1, s), pick(x, 4 * j + 2, s),
-                                pick(x, 4 * j + 3, s)};
-            store_chunk(p, cbase, cb + 4 * j, lim, a, c[j]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = x[16 * NB + i];
-    }
-    if (row >= p.M) return;
-    // last chunk: columns BN - 4 + s .. BN - 1 (x[s..3]); the rest of it is the next tile's
-    float y[8] = {x[0], x[1], x[2], x[3], 0.0f, 0.0f, 0.0f, 0.0f};
-    const int r0 = BN - 4 + s;
-    const int lim_last = min(lim, BN);
-    const float4 c = p.beta != 0.0f ? load_chunk(cbase, r0, lim_last) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    const float a[4] = {pick(y, 0, s), pick(y, 1, s), pick(y, 2, s), pick(y, 3, s)};
-    store_chunk(p, cbase, r0, lim_last, a, c);
-}
-
-// C[row, tn*BN ...] = alpha * acc + beta * C (beta == 0: C not read).
-template <int NB>
-__device__ __forceinline__ void store_c_row(const Tf32Params &p, uint32_t t_row, int row, int tn)
-{
-    float *crow = p.C + static_cast<long long>(row) * p.ldc;
-    if (!p.vec_c) {
-        store_c_row_shifted<(NB > 2 ? 2 : NB)>(p, t_row, row, crow + tn * BN, min(BN, p.N - tn * BN));
-        return;
-    }
-#pragma unroll 1
-    for (int ch = 0; ch < BN / 16; ch += NB) {
-        uint32_t v[NB][16];
-        load_row_chunks<NB>(t_row + ch * 16, v);  // every lane: .sync.aligned
-        if (row >= p.M) continue;
-        const int colb = tn * BN + ch * 16;
-        if (p.vec_c && colb + 16 * NB - 1 < p.N) {
-            float4 c[4 * NB];
-            if (p.beta != 0.0f) {
-#pragma unroll
-                for (int q = 0; q < 4 * NB; ++q) c[q] = *reinterpret_cast<const float4 *>(crow + colb + 4 * q);
-            }
-#pragma unroll
-            for (int q = 0; q < 4 * NB; ++q) {
-                const uint32_t *w = &v[q >> 2][4 * (q & 3)];
-                const float4 acc = make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
-                                               __uint_as_float(w[3]));
-                float4 out;
-                if (p.beta != 0.0f)
-                    out = make_float4(fmaf(p.alpha, acc.x, p.beta * c[q].x), fmaf(p.alpha, acc.y, p.beta * c[q].y),
-                                      fmaf(p.alpha, acc.z, p.beta * c[q].z), fmaf(p.alpha, acc.w, p.beta * c[q].w));
-                else
-                    out = make_float4(p.alpha * acc.x, p.alpha * acc.y, p.alpha * acc.z, p.alpha * acc.w);
-                *reinterpret_cast<float4 *>(crow + colb + 4 * q) = out;
-            }
-        } else {
-            // N edge: element by element, every C load of the step issued before any
-            // use (one memory latency per step, not one per element)
-            float c[16 * NB];
-            if (p.beta != 0.0f) {
-#pragma unroll
-                for (int q = 0; q < 16 * NB; ++q) c[q] = colb + q < p.N ? crow[colb + q] : 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < 16 * NB; ++q) {
-                const int col = colb + q;
-                if (col < p.N) {
-                    const float a = __uint_as_float(v[q >> 4][q & 15]);
-                    crow[col] = (p.beta != 0.0f) ? fmaf(p.alpha, a, p.beta * c[q]) : p.alpha * a;
+                for (int k = 0; k < 8; ++k) {
+                    const int r = 4 * k + sub;
+                    *reinterpret_cast<float4 *>(wb + static_cast<long long>(r) * BN + cb * 32 + 4 * q) =
+                        lds128(stg + static_cast<uint32_t>((r * kStgPitch + 4 * q) * 4));
                 }
             }
+            __syncwarp();
         }
+        return;
+    }
+    const int grow0 = w.tm * S::BM + row0, col0 = w.tn * BN;
+    const bool use_c = p.beta != 0.0f;
+    float cn[32];
+    if (use_c) load_c_block(p, grow0, col0, 0, lane, cn);
+#pragma unroll 1
+    for (int cb = 0; cb < BN / 32; ++cb) {
+        float cc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) cc[i] = use_c ? cn[i] : 0.0f;
+        if (use_c && cb + 1 < BN / 32) load_c_block(p, grow0, col0, cb + 1, lane, cn);
+        stage_block(t_row + cb * 32, stg, lane);
+        if (p.vec_c) {
+            const int col = col0 + cb * 32 + 4 * q;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int grow = grow0 + 4 * k + sub;
+                const float4 a = lds128(stg + static_cast<uint32_t>(((4 * k + sub) * kStgPitch + 4 * q) * 4));
+                const float4 out = make_float4(epi_value(p, a.x, cc[4 * k]), epi_value(p, a.y, cc[4 * k + 1]),
+                                               epi_value(p, a.z, cc[4 * k + 2]), epi_value(p, a.w, cc[4 * k + 3]));
+                float *dst = p.C + static_cast<long long>(grow) * p.ldc + col;
+                if (grow < p.M && col + 3 < p.N) {
+                    *reinterpret_cast<float4 *>(dst) = out;
+                } else if (grow < p.M) {
+                    const float e[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col + j < p.N) dst[j] = e[j];
+                }
+            }
+        } else {
+            const int col = col0 + cb * 32 + lane;
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                const int grow = grow0 + r;
+                const float a = lds32(stg + static_cast<uint32_t>((r * kStgPitch + lane) * 4));
+                if (grow < p.M && col < p.N) p.C[static_cast<long long>(grow) * p.ldc + col] = epi_value(p, a, cc[r]);
+            }
+        }
+        __syncwarp();
     }
 }
 
@@ -307,6 +294,7 @@ tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const uint32_t a_base = smem_addr(smem);
     const uint32_t b_base = a_base + STAGES * S::A_BYTES;
     Tf32Bars<STAGES> *bars = reinterpret_cast<Tf32Bars<STAGES> *>(smem + STAGES * S::STAGE_BYTES);
+    const uint32_t stg_base = a_base + STAGES * S::STAGE_BYTES + 256;  // after the barrier block
     volatile int *abort_flag = &bars->abort_flag;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -487,7 +475,7 @@ tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else if (warp >= 2) {
         // ---- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 of this CTA ----
         const int quarter = warp & 3;
-        const int cta_row = static_cast<int>(rank) * S::CTA_M + quarter * 32 + lane;  // row within the tile
+        const uint32_t stg = stg_base + static_cast<uint32_t>(quarter * 32 * kStgPitch * 4);  // this warp's staging area
         int it = 0;
         Work w;
         for (int item = 0; work_at_g(p, item, w, worker, workers); ++item, ++it) {
@@ -501,26 +489,7 @@ tf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
             tc_fence_after_sync();
             const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-            if (w.dest == kToPartial) {
-                // Stream-K piece: this CTA's rows of the raw, tile-packed partial tile
-                // (rows and columns past M and N hold sums of the copy engine's zero
-                // fill); the stream-K reduction adds the pieces in k order and
-                // applies alpha / beta.
-                float *wrow = p.W + static_cast<long long>(w.idx) * (S::BM * BN) + static_cast<long long>(cta_row) * BN;
-                const bool wok = index_ok(w.idx >= 0 && static_cast<long long>(w.idx) * (S::BM * BN) +
-                                                            static_cast<long long>(cta_row + 1) * BN <= p.w_elems,
-                                          p.status, kWhereIdxTf32Store);
-                if (p.kblocks <= kShortK)
-                    store_partial_row<4>(t_row, wrow, wok);
-                else
-                    store_partial_row<1>(t_row, wrow, wok);
-            } else {
-                const int row = w.tm * S::BM + cta_row;
-                if (p.kblocks <= kShortK)
-                    store_c_row<4>(p, t_row, row, w.tn);
-                else
-                    store_c_row<1>(p, t_row, row, w.tn);
-            }
+            write_tile<S>(p, t_row, stg, w, static_cast<int>(rank) * S::CTA_M + quarter * 32, lane);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
