@@ -104,6 +104,21 @@ def test_unaligned_and_padded(h):
         _check(got, A, B, C, 1.0, -1.0, exact=True)
 
 
+@pytest.mark.parametrize("K", [130, 700])
+def test_aligned_c_with_a_partial_last_chunk(h, K):
+    """C 16-byte accessible (ldc a multiple of 4) but N = 301: the write-out's last
+    16-byte chunk of every row is cut by N and goes element by element; rows past M
+    in the last tile row are skipped. Pad columns and guard bands stay untouched."""
+    M, N = 190, 301
+    A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=23, dist=("int", "int", "int"))
+    for beta in (0.5, 0.0):
+        got, guards, st = run_gemm(torch, h, A, B, C, 1.5, beta, lds=(K + 4, N + 7, 304))
+        assert st == sg.SGEMM_OK and guards
+        plan = h.last_plan()
+        assert plan.vec_c == 1 and plan.repack_c == 0, plan.as_dict()
+        _check(got, A, B, C, 1.5, beta, exact=True)
+
+
 @pytest.mark.parametrize("name", ["square4096", "square4096_int"])
 def test_square4096(h, name):
     p = inputs.PROBLEMS[name]
@@ -168,11 +183,10 @@ def _stream_k_case(h, shape):
 @pytest.mark.parametrize("repack_c", [0, 1])
 @pytest.mark.parametrize("K", [96, 600])
 def test_unaligned_c_in_place_or_through_a_copy(h, repack_c, K):
-    """A C that is not 16-byte accessible, written in place (16-byte accesses inside
-    each row, whose first aligned column differs from row to row, element by element
-    at the row ends and past N) or computed in an aligned workspace copy (filled from
-    C first when beta != 0). Short K (3 k-blocks) and long K (19) take the epilogue's
-    two step widths; N = 700 leaves a partial last tile. Pad columns and guard bands
+    """A C that is not 16-byte accessible, written in place (4-byte accesses, lane l
+    on column l of each staged row, whatever the row's alignment) or computed in an
+    aligned workspace copy (filled from C first when beta != 0). Short K (3 k-blocks)
+    and long K (19); N = 700 leaves a partial last tile. Pad columns and guard bands
     around C stay untouched."""
     M, N = 600, 700
     A, B, C = inputs.problem_operands(M=M, N=N, K=K, seed=17, dist=("int", "int", "int"))
