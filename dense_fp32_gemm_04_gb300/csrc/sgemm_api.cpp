@@ -53,8 +53,6 @@ static_assert(kMaxHostSteps <= 12, "events per pipeline step");
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA; }
-
 // Bind the handle's device for the duration of a call.
 struct DeviceGuard {
     int prev = -1;
