@@ -277,8 +277,9 @@ int ensure_host_pipeline(sgemm_handle_t h)
 // about three times longer to compute (2NK / ~70 TFLOP/s) than its A and C rows
 // take to copy (4 (K + N) bytes at 200 GB/s, at 4096^3), so only the start of the
 // pipeline is copy-bound: nothing can be computed before B has arrived. So B is
-// copied in column blocks (up to 4, multiples of 128 columns), and panel 0 is
-// computed block by block as they arrive. Panel 0 is sized so that computing it
+// copied in column blocks (up to 4, multiples of 128 columns: the first one small,
+// 3N/16, so that the first GEMM starts early, then N/4 and two halves of the
+// rest), and panel 0 is computed block by block as they arrive. Panel 0 is sized so that computing it
 // takes about as long as B takes to arrive: 2 p N K / ~60 TFLOP/s (its GEMMs are
 // small) against 4 K N / ~200 GB/s gives p ~ 600 rows whatever N and K; 768 (at
 // most M / 4) measured best. Then panels grow, each at most three times its
@@ -286,7 +287,8 @@ int ensure_host_pipeline(sgemm_handle_t h)
 // last panel is half of panel 0, so the copy-out after the last GEMM is short.
 // Problems with less than two rounds of 128 x 128 tiles outside the edge panels
 // are one panel and one block. All panels but the last have a multiple of 128
-// rows. (M = N = K = 4096: panels 768 (4 blocks of 1024 columns), 768, 2176, 384.)
+// rows. (M = N = K = 4096: panels 768 (blocks of 768, 1024, 1152 and 1152
+// columns), 768, 2176, 384.)
 struct HostSchedule {
     int panels = 1;
     int start[kMaxHostPanels + 1] = {};
@@ -318,9 +320,21 @@ HostSchedule host_schedule(const sgemm_handle_s *h, int M, int N, int K, bool sp
         size = take;
     }
     sc.panels = P;
-    if (split_b) {
-        const int nb = N >= 1024 ? kMaxColBlocks : (N >= 512 ? 2 : 1);
-        const int w = ((N + nb - 1) / nb + 127) / 128 * 128;
+    if (split_b && N >= 1024) {
+        // The first block small (3N/16: the first GEMM waits for less), the second
+        // N/4, the rest in two halves; multiples of 128 columns.
+        static_assert(kMaxColBlocks >= 4, "four column blocks");
+        const int w0 = std::max(128, N * 3 / 16 / 128 * 128);
+        const int w1 = std::max(128, N / 4 / 128 * 128);
+        const int w2 = ((N - w0 - w1 + 1) / 2 + 127) / 128 * 128;
+        sc.col[0] = 0;
+        sc.col[1] = w0;
+        sc.col[2] = w0 + w1;
+        sc.blocks = w0 + w1 + w2 < N ? 4 : 3;
+        if (sc.blocks == 4) sc.col[3] = w0 + w1 + w2;
+        sc.col[sc.blocks] = N;
+    } else if (split_b && N >= 512) {
+        const int w = ((N + 1) / 2 + 127) / 128 * 128;
         sc.blocks = (N + w - 1) / w;
         for (int j = 0; j <= sc.blocks; ++j) sc.col[j] = std::min(N, j * w);
     }
