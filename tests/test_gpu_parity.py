@@ -369,9 +369,12 @@ def _stream_k_case(h, shape):
     assert h.check_device_status() == (sg.SGEMM_OK, 0)
 
 
-def test_run_host_pipelined_panels(h):
-    """Large host-buffer calls are pipelined over row panels: results match the oracle."""
-    M, N, K = 4100, 3001, 300
+@pytest.mark.parametrize("shape", [(4100, 3001, 300), (6000, 1100, 160)])
+def test_run_host_pipelined_panels(h, shape):
+    """Large host-buffer calls are pipelined over row panels (the first panel over
+    column blocks of B; N = 1100 makes the first block a single 128-column tile):
+    results match the oracle."""
+    M, N, K = shape
     A, B, C = ops(M, N, K, seed=41, dist=("int", "int", "int"))
     Ab = inputs.with_ld(A, K + 3)
     Cb = inputs.with_ld(C, N + 5)
